@@ -1,0 +1,216 @@
+"""CPU oracle for the paged-KV-cache decode path -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library
+(``paged_kv_cache_pa_gb300``) never imports, links or calls it, and the two
+share no code: the arithmetic lives in ``pa_oracle.c`` (plain C, fp64), this
+module only marshals numpy arrays into it.
+
+What each function computes, and the passage it follows, is stated in the
+header of ``pa_oracle.c``.  In short:
+
+* ``half_to_double`` / ``double_to_half``: IEEE binary16 and bfloat16 from
+  their bit layouts, round-to-nearest-even on encode.
+* ``cache_write``: byte copy of every new token's K/V rows into the pool slot
+  named by ``slot_mapping`` (block ``slot // 16``, offset ``slot % 16``).
+* ``copy_blocks``: byte copy of block ``src`` onto block ``dst`` in every
+  layer's K and V pool.
+* ``decode_attention``: softmax(scale * q.K^T) V over the sequence's
+  ``context_lens[s]`` tokens reached through ``block_tables[s]``, two-pass,
+  accumulated in double.
+* ``decode_attention_blockwise``: the same through per-block partial states
+  and a merge (the block-wise form of the attention equation).
+* ``attention_weights``: the normalised weights a_t alongside the output.
+
+Pins: every function above is checked in ``tests/test_oracle_pins.py``
+against library routines, closed forms, invariants and brute force.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_LIB = os.path.join(_HERE, "libpa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+DTYPES = {"f16": 0, "bf16": 1}
+BLOCK = 16
+
+
+def build(force: bool = False) -> str:
+    """Compile pa_oracle.c into libpa_oracle.so beside it (gcc, no fast-math,
+    no FMA contraction, no host-specific flags)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+           "-shared", "-fPIC", "-pthread", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            lib.pa_oracle_half_to_double.restype = ctypes.c_double
+            lib.pa_oracle_half_to_double.argtypes = [ctypes.c_uint16, I]
+            lib.pa_oracle_double_to_half.restype = ctypes.c_uint16
+            lib.pa_oracle_double_to_half.argtypes = [ctypes.c_double, I]
+            lib.pa_oracle_decode_halves.argtypes = [P, P, ctypes.c_int64, I]
+            lib.pa_oracle_encode_halves.argtypes = [P, P, ctypes.c_int64, I]
+            lib.pa_oracle_cache_write.restype = I
+            lib.pa_oracle_cache_write.argtypes = [P, P, P, P, P, I, I, I, I]
+            lib.pa_oracle_copy_blocks.restype = I
+            lib.pa_oracle_copy_blocks.argtypes = [P, P, I, P, I, I, I, I]
+            attn = [P, P, P, P, P, I, P, I, I, I, I, I, ctypes.c_double, I, I]
+            lib.pa_oracle_decode_attention.restype = I
+            lib.pa_oracle_decode_attention.argtypes = attn
+            lib.pa_oracle_decode_attention_blockwise.restype = I
+            lib.pa_oracle_decode_attention_blockwise.argtypes = attn
+            lib.pa_oracle_attention_weights.restype = I
+            lib.pa_oracle_attention_weights.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I,
+                                                        ctypes.c_double, I]
+            _lib = lib
+    return _lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+_RC = {1: "invalid argument", 2: "block id out of range", 3: "slot out of range",
+       4: "out of memory"}
+
+
+def _check(rc: int) -> None:
+    if rc:
+        raise OracleError(f"oracle returned {rc}: {_RC.get(rc, 'unknown')}")
+
+
+def _u16(a: np.ndarray) -> np.ndarray:
+    """View 16-bit float codes (float16 or uint16/int16 arrays) as uint16."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float16 or a.dtype == np.int16:
+        return a.view(np.uint16)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected 16-bit codes, got {a.dtype}")
+    return a
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def half_to_double(codes: np.ndarray, dtype: str) -> np.ndarray:
+    c = _u16(codes)
+    out = np.empty(c.shape, np.float64)
+    _load().pa_oracle_decode_halves(_ptr(c), _ptr(out), c.size, DTYPES[dtype])
+    return out
+
+
+def double_to_half(x: np.ndarray, dtype: str) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, np.uint16)
+    _load().pa_oracle_encode_halves(_ptr(x), _ptr(out), x.size, DTYPES[dtype])
+    return out
+
+
+def cache_write(key, value, k_cache, v_cache, slot_mapping) -> None:
+    """In place on k_cache / v_cache ([num_blocks][Hkv][16][D] 16-bit codes).
+    key / value: [num_tokens][Hkv][D]."""
+    key, value = _u16(key), _u16(value)
+    kc, vc = _u16(k_cache), _u16(v_cache)
+    if not (np.shares_memory(kc, k_cache) and np.shares_memory(vc, v_cache)):
+        raise ValueError("pools must be contiguous 16-bit arrays (written in place)")
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    nb, hkv, bs, d = kc.shape
+    assert bs == BLOCK and key.shape[1:] == (hkv, d)
+    _check(_load().pa_oracle_cache_write(_ptr(key), _ptr(value), _ptr(kc), _ptr(vc),
+                                         _ptr(slots), key.shape[0], nb, hkv, d))
+
+
+def copy_blocks(k_caches, v_caches, block_pairs) -> None:
+    """In place: for every layer, pools[dst] = pools[src] for each (src, dst)."""
+    pairs = np.ascontiguousarray(block_pairs, dtype=np.int64).reshape(-1, 2)
+    ks = [_u16(k) for k in k_caches]
+    vs = [_u16(v) for v in v_caches]
+    for a, b in zip(ks + vs, list(k_caches) + list(v_caches)):
+        if not np.shares_memory(a, b):
+            raise ValueError("pools must be contiguous 16-bit arrays")
+    nb, hkv, bs, d = ks[0].shape
+    kp = (ctypes.c_void_p * len(ks))(*[_ptr(k) for k in ks])
+    vp = (ctypes.c_void_p * len(vs))(*[_ptr(v) for v in vs])
+    _check(_load().pa_oracle_copy_blocks(ctypes.cast(kp, ctypes.c_void_p),
+                                         ctypes.cast(vp, ctypes.c_void_p), len(ks),
+                                         _ptr(pairs), pairs.shape[0], nb, hkv, d))
+
+
+def _attn_args(q, k_cache, v_cache, block_tables, context_lens):
+    q, kc, vc = _u16(q), _u16(k_cache), _u16(v_cache)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    s, h, d = q.shape
+    nb, hkv, bs, d2 = kc.shape
+    assert bs == BLOCK and d2 == d and vc.shape == kc.shape
+    assert bt.ndim == 2 and bt.shape[0] == s and cl.shape == (s,)
+    return q, kc, vc, bt, cl, s, h, d, nb, hkv
+
+
+def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                     dtype: str, nthreads: int | None = None) -> np.ndarray:
+    """float64 [S][H][D] output of paged decode attention (token-wise, two-pass)."""
+    q, kc, vc, bt, cl, s, h, d, nb, hkv = _attn_args(q, k_cache, v_cache, block_tables,
+                                                       context_lens)
+    out = np.zeros((s, h, d), np.float64)
+    _check(_load().pa_oracle_decode_attention(
+        _ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cl), s, h, hkv,
+        d, nb, float(scale), DTYPES[dtype], nthreads or default_threads()))
+    return out
+
+
+def decode_attention_blockwise(q, k_cache, v_cache, block_tables, context_lens,
+                               scale: float, dtype: str,
+                               nthreads: int | None = None) -> np.ndarray:
+    """float64 [S][H][D] output through per-block partial states and a merge."""
+    q, kc, vc, bt, cl, s, h, d, nb, hkv = _attn_args(q, k_cache, v_cache, block_tables,
+                                                       context_lens)
+    out = np.zeros((s, h, d), np.float64)
+    _check(_load().pa_oracle_decode_attention_blockwise(
+        _ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cl), s, h, hkv,
+        d, nb, float(scale), DTYPES[dtype], nthreads or default_threads()))
+    return out
+
+
+def attention_weights(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                      dtype: str):
+    """(out [S][H][D], weights [S][H][max_ctx]) -- weights a_t = w_t / Z, zero past L."""
+    q, kc, vc, bt, cl, s, h, d, nb, hkv = _attn_args(q, k_cache, v_cache, block_tables,
+                                                       context_lens)
+    max_ctx = int(cl.max()) if s else 0
+    out = np.zeros((s, h, d), np.float64)
+    w = np.zeros((s, h, max(max_ctx, 1)), np.float64)
+    _check(_load().pa_oracle_attention_weights(
+        _ptr(out), _ptr(w), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cl), s,
+        h, hkv, d, nb, float(scale), DTYPES[dtype]))
+    return out, w[:, :, :max_ctx]

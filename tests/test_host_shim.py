@@ -1,0 +1,159 @@
+"""Host block manager and workload recipes, replayed against the worked
+examples the pages print (tests/golden/*.txt carry the citations)."""
+import math
+
+import numpy as np
+import pytest
+
+from conftest import golden
+from paged_kv_cache_pa_gb300 import synthetic
+from paged_kv_cache_pa_gb300.block_manager import BlockPool, OutOfBlocks, Sequence, blocks_for
+
+
+def _ints(v):
+    return [int(x) for x in v]
+
+
+def test_interleaved_sequences_tables():
+    g = golden("interleaved_tables.txt")
+    B, NB, steps = int(g["block_size"][0][0]), int(g["pool_blocks"][0][0]), int(g["steps"][0][0])
+    rows = {int(r[0]): r for r in g["seq"]}
+    prompts = {i: int(r[r.index("prompt") + 1]) for i, r in rows.items()}
+    pool = BlockPool(NB, block_size=B)
+    seqs = [Sequence(pool) for _ in rows]
+    for t in range(steps):
+        for i, s in enumerate(seqs):
+            s.reserve(prompts[i] if t == 0 else 1)
+    for i, r in rows.items():
+        assert seqs[i].n == int(r[r.index("stored") + 1])
+        assert seqs[i].table == _ints(r[r.index("table") + 1:])
+    assert pool.num_free == int(g["free"][0][0])
+    assert pool.copies == []
+
+
+def test_parallel_sampling_copy_on_write():
+    g = golden("parallel_sampling.txt")
+    B = int(g["block_size"][0][0])
+    prompt, samples, new = (int(g[k][0][0]) for k in ("prompt", "samples", "new_tokens"))
+    pool = BlockPool(64, block_size=B)
+    first = Sequence(pool)
+    first.reserve(prompt)
+    assert len(first.table) == int(g["prompt_blocks"][0][0])
+    assert first.fills()[-1][1] == int(g["last_block_fill"][0][0])
+    seqs = [first] + [first.fork() for _ in range(samples - 1)]
+    for _ in range(new - 1):          # the first new token is sampled from the prompt
+        for s in seqs:
+            s.reserve(1)
+    in_use = pool.num_blocks - pool.num_free
+    assert in_use == int(g["blocks_in_use"][0][0])
+    assert samples * blocks_for(seqs[0].n, B) == int(g["blocks_unshared"][0][0])
+    assert len(pool.copies) == int(g["cow_copies"][0][0])
+    for row in g["table"]:
+        assert seqs[int(row[0])].table == _ints(row[1:])
+    # the copies are of the shared partial prompt block into fresh blocks
+    assert all(src == 2 for src, _ in pool.copies)
+
+
+def test_figure6_block_table_walkthrough():
+    g = golden("figure6_walkthrough.txt")
+    B = int(g["block_size"][0][0])
+    pool = BlockPool(8, block_size=B, free_order=_ints(g["free_order"][0]))
+    seq = Sequence(pool)
+
+    def fills():
+        return [f"{b}:{n}" for b, n in seq.fills()]
+
+    seq.reserve(7)
+    assert fills() == g["after_prompt"][0]
+    seq.reserve(1)                                   # "fathers"
+    assert fills() == g["after_token8"][0]
+    slot = seq.reserve(1)[0]                         # "brought"
+    assert fills() == g["after_token9"][0]
+    assert slot == int(g["slot_token9"][0][0])
+
+
+def test_cow_trace_two_samples():
+    g = golden("cow_trace.txt")
+    pool = BlockPool(16, block_size=int(g["block_size"][0][0]),
+                     free_order=_ints(g["free_order"][0]))
+    a1 = Sequence(pool)
+    a1.reserve(int(g["prompt"][0][0]))
+    a2 = a1.fork()
+    a1.reserve(1)
+    a2.reserve(1)
+    assert [tuple(p) for p in pool.copies] == [tuple(_ints(g["copies"][0]))]
+    assert a1.table == _ints(g["table_A1"][0])
+    assert a2.table == _ints(g["table_A2"][0])
+    for item in g["refs"][0]:
+        b, r = item.split(":")
+        assert pool.refs[int(b)] == int(r)
+
+
+def test_free_returns_blocks_and_out_of_blocks_raises():
+    pool = BlockPool(4)
+    s = Sequence(pool)
+    s.reserve(64)
+    with pytest.raises(OutOfBlocks):
+        Sequence(pool).reserve(1)
+    s.free()
+    assert pool.num_free == 4 and all(r == 0 for r in pool.refs)
+
+
+# ---------------------------------------------------------------------------
+# workload recipes
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", [n for n in synthetic.CONFIGS])
+def test_workload_tables_and_slots_are_consistent(name):
+    wl = synthetic.make(name)
+    S = wl.num_seqs
+    assert wl.context_lens.min() >= 1
+    used = []
+    for s in range(S):
+        L = int(wl.context_lens[s])
+        nb = blocks_for(L)
+        row = wl.block_tables[s]
+        assert np.all(row[:nb] >= 0) and np.all(row[:nb] < wl.num_blocks)
+        assert np.all(row[nb:] == -1)
+        used.extend(row[:nb].tolist())
+        # the step's new token is position L-1
+        pos = L - 1
+        assert wl.slot_mapping[s] == row[pos // 16] * 16 + pos % 16
+    if name != "beams":
+        assert len(set(used)) == len(used)            # no sharing outside beams
+    else:
+        assert len(set(used)) < len(used)             # beams share prompt blocks
+        # copy-on-write destinations are fresh and distinct; sources are shared
+        dst = wl.copy_pairs[:, 1]
+        assert len(set(dst.tolist())) == len(dst)
+        assert not set(dst.tolist()) & set(wl.copy_pairs[:, 0].tolist())
+    slots = wl.slot_mapping
+    assert len(set(slots.tolist())) == S              # one slot per new token
+
+
+def test_workload_recipes_follow_the_stated_shapes():
+    t = synthetic.make("tiny")
+    assert (t.num_seqs, t.num_heads, t.num_kv_heads, t.head_dim, t.num_blocks) == (4, 8, 8, 64, 64)
+    assert t.context_lens.max() <= 128
+    o = synthetic.make("opt13b")
+    assert (o.num_seqs, o.num_heads, o.head_dim, o.dtype) == (256, 40, 128, "f16")
+    assert o.context_lens.max() <= 2048 and o.context_lens.min() >= 2
+    assert o.num_blocks == sum(blocks_for(int(L)) for L in o.context_lens)
+    q = synthetic.make("gqa")
+    assert (q.num_heads, q.num_kv_heads, q.dtype) == (12, 2, "bf16")
+    assert 512 <= q.context_lens.min() and q.context_lens.max() <= 4096
+    # the GQA shape's KV bytes per token over 28 layers: 28 KiB
+    assert 28 * 2 * q.num_kv_heads * q.head_dim * 2 == 28 * 1024
+    lg = synthetic.make("long")
+    assert lg.num_blocks * 40 * 16 * 128 * 2 * 2 == 60 * (1 << 30)
+    assert 16384 <= lg.context_lens.min() and lg.context_lens.max() <= 32768
+    b = synthetic.make("beams")
+    assert b.num_seqs == 192 and b.context_lens.min() >= 513
+    # beams of one group have equal length
+    assert all(len(set(b.context_lens[i * 6:(i + 1) * 6].tolist())) == 1 for i in range(32))
+
+
+def test_lognormal_reading():
+    rng = np.random.default_rng(0)
+    x = synthetic._lognormal_int(rng, 220.0, 200000, 1, 10 ** 9)
+    assert abs(x.mean() / 220.0 - 1) < 0.02
