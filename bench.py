@@ -1,0 +1,428 @@
+"""Benchmark of the paged decode path on the OPT-13B-shaped decode step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config opt13b]
+
+One step = one pass of the whole path over the batch: copy-on-write block
+copies (when the workload has shared blocks; the OPT-13B-shaped batch has
+none), the cache write of one new token per sequence, and paged decode
+attention (plan, attention, merge kernels) over every sequence's context.
+Inputs are synthetic and seeded (paged_kv_cache_pa_gb300.synthetic).
+
+Metric: decode-attention achieved HBM GB/s = algorithmic bytes of the step /
+step time, where the algorithmic bytes are what the method itself must move:
+    attention: sum_s L_s * Hkv * D * 2 (K and V) * elt + q + out + table
+               entries read (ceil(L_s/16) int32 each) + context_lens
+    cache write: the new K/V rows read and written + slot_mapping
+(last-block padding, workspace and L2 re-reads excluded).  Also reported:
+sequences/s per layer, the roofline of the attention call, the CPU oracle as
+a baseline, and an end-to-end number through the Python API with host
+buffers.  Timed region: K steps between CUDA events on the launching stream,
+bracketed by a barrier and device synchronisation; the K/V read per step
+(~1.9 GB) is far larger than L2, so no flush is needed between steps.
+
+With N > 1 (torchrun, one rank per GPU) every rank runs its own replica on
+its own seeded batch (weak scaling; no collective on the data path); value =
+all ranks' bytes / the slowest rank's time.
+
+--impl reference times the CPU oracle (plain C, fp64, all host cores) on a
+bounded sample of the same workload, same metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and sequences/sec per layer"
+UNIT = "GB/s"
+
+
+def algorithmic_bytes(wl, out_elt=4):
+    """(attention bytes, cache-write bytes, copy bytes) of one step."""
+    S, H, Hkv, D, elt = wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, 2
+    L = wl.context_lens.astype(np.int64)
+    nb = (L + 15) // 16
+    attn = int(L.sum()) * Hkv * D * elt * 2 + S * H * D * elt + S * H * D * out_elt + \
+        int(nb.sum()) * 4 + S * 4
+    write = 2 * (S * Hkv * D * elt * 2) + S * 8
+    copy = 2 * len(wl.copy_pairs) * Hkv * 16 * D * elt * 2
+    return attn, write, copy
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_pa_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.startswith("pa_decode") or f == "pa_ptx.cuh":
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode())
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config):
+    """DRAM bytes per attention call from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        e = rec.get(config)
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return e.get("dram_bytes_per_call")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.5)
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts + frac, parts))
+                except Exception:
+                    continue
+        os.unlink(self.path)
+        inside = [p for ts, p in rows if t0 - 0.15 <= ts <= t1 + 0.15] or [p for _, p in rows]
+        if not inside:
+            return None
+        sm = [float(p[2]) for p in inside if p[2].replace(".", "").isdigit()]
+        mx = [float(p[3]) for p in inside if p[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in inside for n, v in zip(names, p[6:10]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside)}
+
+
+def cpu_oracle_run(wl, seqs, threads=None, seed=0, host_vals=None):
+    """Time the oracle on sequences ``seqs`` of ``wl``; returns (seconds,
+    algorithmic bytes of those sequences, threads)."""
+    import torch
+    import oracle
+    seqs = np.asarray(seqs)
+    tables = wl.block_tables[seqs]
+    lens = wl.context_lens[seqs]
+    used = np.unique(tables[tables >= 0])
+    rel = np.where(tables >= 0, np.searchsorted(used, np.maximum(tables, 0)), -1).astype(np.int32)
+    if host_vals is None:
+        g = torch.Generator().manual_seed(seed)
+        dt = torch.float16 if wl.dtype == "f16" else torch.bfloat16
+
+        def r(*shape):
+            return torch.randn(*shape, generator=g).to(dt).view(torch.int16).numpy().view(np.uint16)
+        q = r(len(seqs), wl.num_heads, wl.head_dim)
+        kc = r(len(used), wl.num_kv_heads, 16, wl.head_dim)
+        vc = r(len(used), wl.num_kv_heads, 16, wl.head_dim)
+    else:
+        q, kc, vc = host_vals(seqs, used)
+    threads = threads or oracle.default_threads()
+    t = time.perf_counter()
+    oracle.decode_attention(q, kc, vc, rel, lens, wl.scale, wl.dtype, nthreads=threads)
+    dt_s = time.perf_counter() - t
+    sub = type(wl)(**{**wl.__dict__, "num_seqs": len(seqs), "context_lens": lens,
+                      "block_tables": tables, "slot_mapping": wl.slot_mapping[seqs],
+                      "copy_pairs": np.zeros((0, 2), np.int64)})
+    return dt_s, algorithmic_bytes(sub)[0], threads
+
+
+def run_reference(args, wl, rank, world):
+    """CPU oracle arm: rank 0 only."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    # size the per-step sample so the whole run stays within ~2 minutes
+    t1, b1, _ = cpu_oracle_run(wl, [0], threads)
+    rate = b1 / max(t1, 1e-6)
+    per_seq = algorithmic_bytes(wl)[0] / wl.num_seqs
+    budget_s = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(wl.num_seqs, budget_s * rate / per_seq)))
+    rng = np.random.default_rng(0)
+    samples = [rng.choice(wl.num_seqs, n, replace=False) for _ in range(args.steps + args.warmup)]
+    for i in range(args.warmup):
+        cpu_oracle_run(wl, samples[i], threads, seed=i)
+    tot_t = tot_b = 0.0
+    for i in range(args.steps):
+        t, b, _ = cpu_oracle_run(wl, samples[args.warmup + i], threads, seed=args.warmup + i)
+        tot_t += t
+        tot_b += b
+    value = tot_b / tot_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_t / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "opt13b-shaped decode step (S=256, H=Hkv=40, D=128, fp16)",
+                   "sample_seqs_per_step": n},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{n} random sequences of the workload per step"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="opt13b")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from paged_kv_cache_pa_gb300 import synthetic
+    wl = synthetic.make(args.config, seed=synthetic.SEEDS[args.config] + 100 * rank)
+
+    if args.impl == "reference":
+        run_reference(args, wl, rank, world)
+        return
+
+    import torch
+    import paged_kv_cache_pa_gb300 as pa
+    from paged_kv_cache_pa_gb300.build import build
+    build()
+    pa.load_library()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    vals = synthetic.make_values(wl, device=dev)
+    S, H, Hkv, D = wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim
+    tables = torch.as_tensor(wl.block_tables, device=dev)
+    lens = torch.as_tensor(wl.context_lens, device=dev)
+    slots = torch.as_tensor(wl.slot_mapping, device=dev)
+    pairs = torch.as_tensor(wl.copy_pairs, device=dev) if len(wl.copy_pairs) else None
+    out = torch.empty(S, H, D, dtype=torch.float32, device=dev)
+    ws = torch.empty(pa.decode_workspace_size(S, H, Hkv, D, wl.max_context_len),
+                     dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    merge = wl.max_context_len > pa.decode_partition_tokens(S, Hkv, wl.max_context_len)
+    # our kernels per step: [copy] + cache write + plan + attention + [merge]
+    launches_per_step = (pairs is not None) + 1 + 2 + int(merge)
+
+    def step(ev_a=None, ev_b=None):
+        if pairs is not None:
+            pa.copy_blocks([vals["k_cache"]], [vals["v_cache"]], pairs, error_word=err)
+        pa.cache_write(vals["key"], vals["value"], vals["k_cache"], vals["v_cache"], slots,
+                       error_word=err)
+        if ev_a is not None:
+            ev_a.record(stream)
+        pa.decode_attention(vals["q"], vals["k_cache"], vals["v_cache"], tables, lens,
+                            wl.max_context_len, wl.scale, out=out, workspace=ws, error_word=err)
+        if ev_b is not None:
+            ev_b.record(stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    assert int(err.item()) == 0, f"device error word {int(err.item())}"
+
+    K = args.steps
+    evs_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    evs_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank) if rank == 0 or world > 1 else None
+    if sampler:
+        sampler.start()
+    barrier()
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(K):
+        step(evs_a[i], evs_b[i])
+    t_end.record(stream)
+    barrier()
+    wall1 = time.time()
+    clocks = sampler.stop(wall0, wall1) if sampler else None
+    total_ms = t_start.elapsed_time(t_end)
+    attn_ms = sum(a.elapsed_time(b) for a, b in zip(evs_a, evs_b)) / K
+    if dist is not None:
+        tm = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        total_ms = float(tm.item())
+    ms_per_step = total_ms / K
+
+    b_attn, b_write, b_copy = algorithmic_bytes(wl)
+    b_step = b_attn + b_write + b_copy
+    value = world * b_step / (ms_per_step * 1e-3) / 1e9
+    attn_gbs = b_attn / (attn_ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+
+    # end to end through the Python API: pinned host inputs in, output out
+    e2e = None
+    if not args.no_e2e:
+        hq = vals["q"].cpu().pin_memory()
+        hk = vals["key"].cpu().pin_memory()
+        hv = vals["value"].cpu().pin_memory()
+        hslots = torch.as_tensor(wl.slot_mapping).pin_memory()
+        htab = torch.as_tensor(wl.block_tables).pin_memory()
+        hlens = torch.as_tensor(wl.context_lens).pin_memory()
+        hout = torch.empty(S, H, D, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hslots, htab, hlens))
+        d2h = hout.numel() * hout.element_size()
+
+        def e2e_step():
+            q_d = hq.to(dev, non_blocking=True)
+            k_d = hk.to(dev, non_blocking=True)
+            v_d = hv.to(dev, non_blocking=True)
+            s_d = hslots.to(dev, non_blocking=True)
+            t_d = htab.to(dev, non_blocking=True)
+            l_d = hlens.to(dev, non_blocking=True)
+            if pairs is not None:
+                pa.copy_blocks([vals["k_cache"]], [vals["v_cache"]], pairs)
+            pa.cache_write(k_d, v_d, vals["k_cache"], vals["v_cache"], s_d)
+            o = pa.decode_attention(q_d, vals["k_cache"], vals["v_cache"], t_d, l_d,
+                                    wl.max_context_len, wl.scale, out=out, workspace=ws)
+            hout.copy_(o, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        if dist is not None:
+            tm = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+            e_ms = float(tm.item())
+        e2e = {"value": round(world * b_step / (e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e_ms, 4)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        kc_h = vals["k_cache"].view(torch.int16).cpu().numpy().view(np.uint16)
+        vc_h = vals["v_cache"].view(torch.int16).cpu().numpy().view(np.uint16)
+        q_h = vals["q"].view(torch.int16).cpu().numpy().view(np.uint16)
+
+        def host_vals(seqs, used):
+            return q_h[seqs], kc_h[used], vc_h[used]
+        t_cpu, b_cpu, threads = cpu_oracle_run(wl, np.arange(S), host_vals=host_vals)
+        cpu = {"value": round(b_cpu / t_cpu / 1e9, 4), "unit": UNIT, "cores": threads,
+               "kind": "oracle", "seconds": round(t_cpu, 2),
+               "sample": f"all {S} sequences of the batch, attention only, once"}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": "opt13b-shaped decode step: S=256, H=Hkv=40, D=128, fp16, "
+                               "block 16, lognormal prompt 220 + output 204, <=2048 tokens, "
+                               "scattered blocks, one layer",
+                   "mean_context": round(float(wl.context_lens.mean()), 1),
+                   "kv_bytes_per_step": int(wl.kv_bytes()),
+                   "l2": "inputs larger than L2 (K/V read per step >> 126 MB L2)",
+                   "parallelism": f"replicas x{world}"},
+        "seqs_per_s_per_layer": round(world * S / (ms_per_step * 1e-3), 1),
+        "pct_of_peak": {"measured_copy": round(100 * value / world / peak, 2),
+                        "spec_8000": round(100 * value / world / 8000.0, 2)},
+        "roofline": {"bound": "hbm", "achieved": round(attn_gbs, 2), "peak": peak,
+                     "peak_kind": f"{peak_kind} HBM copy GB/s", "unit": "GB/s",
+                     "frac": round(attn_gbs / peak, 4),
+                     "traffic": recorded_traffic(args.config),
+                     "kernel": "pa_decode_attention (plan + attention + merge)",
+                     "ms_per_call": round(attn_ms, 4), "algorithmic_bytes": int(b_attn)},
+        "gpu_launches": int(K * launches_per_step),
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

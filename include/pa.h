@@ -1,0 +1,205 @@
+/*
+ * pa.h -- C ABI of the paged-KV-cache decode path for one GB300 (sm_103a).
+ *
+ * The KV cache of every layer is a pool of fixed-size blocks of 16 tokens;
+ * each sequence reaches its tokens through a block table of physical block
+ * ids, and the kernels see nothing but those ids and the sequence lengths
+ * [Efficient Memory Management for Large Language Model Serving with
+ * PagedAttention, "KV Cache Manager: Block Table Mapping" (logical-to-physical
+ * separation) and "Kernel-Level Optimizations"].
+ *
+ * Three operations, one per kernel family the pages name:
+ *   pa_cache_write       fused reshape and block write of the new tokens' K/V
+ *   pa_decode_attention  fused block read and attention (with context-split
+ *                        partitions and a merge for long sequences)
+ *   pa_copy_blocks       fused copy-on-write block copy, all pairs and layers
+ *
+ * Conventions for every entry point:
+ *   - Every pointer named "device" is device memory owned by the caller; the
+ *     library allocates nothing, keeps no state between calls and never
+ *     synchronises the stream.  Work is enqueued on `stream` (a
+ *     cudaStream_t; NULL is the legacy default stream) and runs
+ *     asynchronously.
+ *   - Tensors are dense and row-major in the layouts stated below, with base
+ *     addresses aligned to 16 bytes.
+ *   - Problems visible on the host (null pointers, unsupported sizes, dtype
+ *     mismatch, small workspace) return a status before anything is enqueued.
+ *   - Problems only visible on the device (a block id or slot out of range, a
+ *     context length above the stated bound) skip the offending unit and OR a
+ *     PA_ERRBIT_* bit into *dev_error_word (a device unsigned int the caller
+ *     zeroes and reads after synchronising; may be NULL).  No kernel traps,
+ *     asserts or spins without a bound.
+ *   - Launch failures return PA_ERR_CUDA (the CUDA error is left for
+ *     cudaGetLastError).
+ *
+ * Block layout (both pools of a layer):
+ *   k_cache, v_cache: [num_blocks][num_kv_heads][PA_BLOCK_SIZE][head_dim]
+ *   element type pa_dtype_t (PA_F16 or PA_BF16).  Token t of a sequence lives
+ *   at block block_tables[s][t / 16], offset t % 16, for every KV head
+ *   [Paged Attention: Managing the KV Cache Like Virtual Memory, "A paged KV
+ *   cache, in code": pools of [blocks, key-value heads, 16 tokens, head
+ *   dimension]; "Attention over scattered blocks": row() addressing].
+ */
+#ifndef PA_GB300_H
+#define PA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (struct CUstream_st *), declared without CUDA headers. */
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2 } pa_dtype_t;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned base, bad enum */
+    PA_ERR_UNSUPPORTED = 2,   /* a size this build has no kernel for */
+    PA_ERR_CUDA = 3,          /* a CUDA launch or attribute call failed */
+    PA_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required */
+    PA_ERR_TIMEOUT = 5        /* reserved: reported through PA_ERRBIT_TIMEOUT */
+} pa_status_t;
+
+#define PA_BLOCK_SIZE 16
+
+/* Bits OR-ed into *dev_error_word by the kernels. */
+#define PA_ERRBIT_BLOCK_OOB   1u  /* a block id (table entry or copy pair) outside [0, num_blocks) */
+#define PA_ERRBIT_SLOT_OOB    2u  /* a slot >= num_blocks * 16 */
+#define PA_ERRBIT_CONTEXT_LEN 4u  /* context_lens[s] < 0 or > max_context_len */
+#define PA_ERRBIT_TIMEOUT     8u  /* a bounded wait inside a kernel gave up */
+
+/*
+ * pa_cache_write -- write each new token's key and value rows into the pool
+ * slot named by slot_mapping.
+ *
+ * Defines: for every token t with slot = slot_mapping[t] >= 0 and every KV head
+ * h, k_cache[slot / 16][h][slot % 16][:] = key[t][h][:], and the same for
+ * value / v_cache; the bytes are copied unchanged.  slot_mapping[t] < 0 skips
+ * token t (padding).
+ * [Efficient Memory Management ..., "Kernel-Level Optimizations", 1. fused
+ * reshape and block write; Paged Attention: Managing the KV Cache ...,
+ * PagedLayer.update (writes through block and offset) and the slot-mapping
+ * note after the interleaving test]
+ *
+ * key, value    device, [num_tokens][num_kv_heads][head_dim], dtype
+ * k_cache, v_cache  device pools, layout above, written in place
+ * slot_mapping  device int64 [num_tokens]
+ * head_dim      64, 128 or 256
+ * dev_error_word  device, may be NULL: PA_ERRBIT_SLOT_OOB for a slot past the
+ *               pool (that token is skipped)
+ * Distinct tokens must name distinct slots (two writes to one slot race).
+ */
+pa_status_t pa_cache_write(const void *key, const void *value, void *k_cache, void *v_cache,
+                           const int64_t *slot_mapping, int num_tokens, int num_blocks,
+                           int num_kv_heads, int head_dim, pa_dtype_t dtype,
+                           unsigned int *dev_error_word, pa_stream_t stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of device workspace pa_decode_attention
+ * needs for these sizes (0 never; always at least the scheduling header).
+ * The result depends only on its arguments.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int max_context_len);
+
+/*
+ * pa_decode_partition_tokens -- context-partition size (tokens, a multiple of
+ * 16 between 64 and 512) that pa_decode_attention uses for these sizes.  A
+ * sequence longer than this is split into partitions whose partial results
+ * a merge kernel combines; the merge kernel is enqueued only when
+ * max_context_len exceeds it.  Returns 0 for invalid sizes.
+ */
+int pa_decode_partition_tokens(int num_seqs, int num_kv_heads, int max_context_len);
+
+/*
+ * pa_decode_attention -- one decode step of attention over a paged KV cache.
+ *
+ * Defines: for sequence s and query head h, with KV head hk = h / G,
+ * G = num_heads / num_kv_heads (query heads hk*G .. hk*G+G-1 share KV head
+ * hk), L = context_lens[s], and token t read at block block_tables[s][t/16],
+ * offset t%16:
+ *     x_t = scale * <query[s][h], k_t>,
+ *     out[s][h] = sum_t exp(x_t - max x) v_t / sum_t exp(x_t - max x),
+ * the standard attention equation evaluated block by block, blocks visited
+ * in any order and combined exactly.  Scores, softmax and sums are computed
+ * in fp32 from the 16-bit inputs.  L = 0 gives a zero row.
+ * [Efficient Memory Management ..., "PagedAttention Algorithm": attention
+ * equation and its block-wise reformulation; "Kernel-Level Optimizations",
+ * 2. fused block read and attention; Paged Attention: Managing the KV Cache
+ * ..., "Attention over scattered blocks" (running softmax for the query heads
+ * that share a KV head); vLLM Internals ..., "The kernel pays for the
+ * indirection" (a partition axis in the grid)]
+ *
+ * out           device [num_seqs][num_heads][head_dim], out_dtype = PA_F32 or
+ *               the input dtype (round to nearest even from the fp32 result)
+ * query         device [num_seqs][num_heads][head_dim], dtype
+ * k_cache, v_cache  device pools, layout above
+ * block_tables  device int32 [num_seqs][max_blocks_per_seq]; entries past a
+ *               sequence's ceil(L/16) blocks are never read
+ * context_lens  device int32 [num_seqs], each in [0, max_context_len]
+ * max_context_len  host-known upper bound on context_lens,
+ *               <= 16 * max_blocks_per_seq
+ * num_heads % num_kv_heads == 0, num_heads / num_kv_heads <= 8,
+ * head_dim in {64, 128, 256}, dtype PA_F16 or PA_BF16
+ * workspace     device, >= pa_decode_workspace_size(...) bytes, 256-byte
+ *               aligned; holds the work plan and the per-partition partial
+ *               results; its contents need no initialisation, and two calls
+ *               in flight at once must not share one workspace
+ * dev_error_word  device, may be NULL: PA_ERRBIT_BLOCK_OOB (the block is
+ *               skipped), PA_ERRBIT_CONTEXT_LEN (the sequence gets a zero
+ *               row), PA_ERRBIT_TIMEOUT
+ * Enqueues two to three kernels (plan, attention, merge when some sequence
+ * may span more than one partition), chained with programmatic dependent
+ * launch.
+ */
+pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, const void *query,
+                                const void *k_cache, const void *v_cache,
+                                const int32_t *block_tables, int max_blocks_per_seq,
+                                const int32_t *context_lens, int max_context_len,
+                                int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int num_blocks, float scale, pa_dtype_t dtype,
+                                void *workspace, size_t workspace_bytes,
+                                unsigned int *dev_error_word, pa_stream_t stream);
+
+/* Upper bound on num_layers accepted by pa_copy_blocks. */
+#define PA_MAX_LAYERS 128
+
+/*
+ * pa_copy_blocks -- copy-on-write block copies, every pair and every layer in
+ * one launch.
+ *
+ * Defines: for every layer l < num_layers and pair i < num_pairs with
+ * (src, dst) = (block_pairs[2i], block_pairs[2i+1]):
+ *     k_caches[l][dst] = k_caches[l][src] and v_caches[l][dst] = v_caches[l][src],
+ * whole blocks (num_kv_heads * 16 * head_dim elements), bytes unchanged;
+ * the source blocks are left as they were.
+ * [Efficient Memory Management ..., "Kernel-Level Optimizations", 3. fused
+ * block copy; "Copy-on-write mechanism" (copy the entire old block into the
+ * new one)]
+ *
+ * k_caches, v_caches  HOST arrays of num_layers device pool pointers, each
+ *               pool [num_blocks][num_kv_heads][16][head_dim]
+ * block_pairs   device int64 [num_pairs][2] (src, dst)
+ * num_layers    1 .. PA_MAX_LAYERS
+ * Each dst must be distinct and must not be another pair's src (true of
+ * copy-on-write, whose destinations are fresh blocks); a pair with
+ * src == dst is a no-op.
+ * dev_error_word  device, may be NULL: PA_ERRBIT_BLOCK_OOB (pair skipped)
+ */
+pa_status_t pa_copy_blocks(void *const *k_caches, void *const *v_caches, int num_layers,
+                           const int64_t *block_pairs, int num_pairs, int num_blocks,
+                           int num_kv_heads, int head_dim, pa_dtype_t dtype,
+                           unsigned int *dev_error_word, pa_stream_t stream);
+
+/* Static, human-readable name of a status. */
+const char *pa_status_string(pa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_GB300_H */

@@ -1,0 +1,205 @@
+"""GB300-native paged KV cache decode path.
+
+Python binding of ``libpa_gb300.so`` (the C ABI declared in ``include/pa.h``)
+with the same operation names.  This module only marshals arguments (device
+pointers of torch tensors, sizes, the current CUDA stream); every step of the
+path runs in the library's CUDA kernels.  There is no CPU fallback: calling an
+operation without the built library, or with tensors that are not on a CUDA
+device, raises.
+
+    cache_write(key, value, k_cache, v_cache, slot_mapping)
+    decode_attention(query, k_cache, v_cache, block_tables, context_lens,
+                     max_context_len, scale, out=None, ...)
+    copy_blocks(k_caches, v_caches, block_pairs)
+
+Build the library with ``python -m paged_kv_cache_pa_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence
+
+__all__ = ["cache_write", "decode_attention", "decode_workspace_size", "decode_partition_tokens", "copy_blocks",
+           "status_string", "PaError", "library_path", "load_library", "BLOCK_SIZE",
+           "ERRBIT_BLOCK_OOB", "ERRBIT_SLOT_OOB", "ERRBIT_CONTEXT_LEN", "ERRBIT_TIMEOUT",
+           "MAX_LAYERS"]
+
+BLOCK_SIZE = 16
+MAX_LAYERS = 128
+PA_F16, PA_BF16, PA_F32 = 0, 1, 2
+ERRBIT_BLOCK_OOB, ERRBIT_SLOT_OOB, ERRBIT_CONTEXT_LEN, ERRBIT_TIMEOUT = 1, 2, 4, 8
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libpa_gb300.so")
+_lib = None
+_lock = threading.Lock()
+
+# entry point -> (restype, argtypes)
+_P, _I, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
+_SIGNATURES = {
+    "pa_cache_write": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "pa_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
+    "pa_decode_partition_tokens": (_I, [_I, _I, _I]),
+    "pa_decode_attention": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I,
+                                 ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P]),
+    "pa_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "pa_status_string": (ctypes.c_char_p, [_I]),
+}
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, op: str):
+        self.status = status
+        super().__init__(f"{op}: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libpa_gb300.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it with "
+                    "`python -m paged_kv_cache_pa_gb300.build` (there is no fallback path)")
+            lib = ctypes.CDLL(_LIB_PATH)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().pa_status_string(int(status)).decode()
+
+
+def _check(status: int, op: str) -> None:
+    if status != 0:
+        raise PaError(status, op)
+
+
+def _dtype_code(dt) -> int:
+    import torch
+    if dt == torch.float16:
+        return PA_F16
+    if dt == torch.bfloat16:
+        return PA_BF16
+    if dt == torch.float32:
+        return PA_F32
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def _dev(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_ptr(stream, device) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _opt_ptr(t, name):
+    return None if t is None else _dev(t, name)
+
+
+def cache_write(key, value, k_cache, v_cache, slot_mapping, error_word=None,
+                stream=None) -> None:
+    """Write key[t] / value[t] ([T][Hkv][D]) into pool slot slot_mapping[t]
+    (int64; < 0 skips).  Pools: [num_blocks][Hkv][16][D]."""
+    import torch
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    nb, hkv, bs, d = k_cache.shape
+    if bs != BLOCK_SIZE or tuple(key.shape[1:]) != (hkv, d) or key.shape != value.shape:
+        raise ValueError("shape mismatch between key/value and the pools")
+    if v_cache.shape != k_cache.shape or k_cache.dtype != key.dtype or v_cache.dtype != key.dtype:
+        raise ValueError("pools must match each other and the key dtype")
+    st = load_library().pa_cache_write(
+        _dev(key, "key"), _dev(value, "value"), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _dev(slot_mapping, "slot_mapping"), key.shape[0], nb, hkv, d,
+        _dtype_code(key.dtype), _opt_ptr(error_word, "error_word"),
+        _stream_ptr(stream, key.device))
+    _check(st, "pa_cache_write")
+
+
+def decode_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                          max_context_len: int) -> int:
+    return int(load_library().pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads,
+                                                       head_dim, max_context_len))
+
+
+def decode_partition_tokens(num_seqs: int, num_kv_heads: int, max_context_len: int) -> int:
+    """Partition size pa_decode_attention uses; a merge kernel runs when
+    max_context_len exceeds it."""
+    return int(load_library().pa_decode_partition_tokens(num_seqs, num_kv_heads,
+                                                         max_context_len))
+
+
+def decode_attention(query, k_cache, v_cache, block_tables, context_lens,
+                     max_context_len: int, scale: float, out=None, out_dtype=None,
+                     workspace=None, error_word=None, stream=None):
+    """Paged decode attention; returns ``out`` [S][H][D] (fp32 unless
+    ``out_dtype`` / ``out`` says the input dtype).  ``workspace`` (uint8, >=
+    decode_workspace_size bytes) is allocated here when not given."""
+    import torch
+    S, H, D = query.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if bs != BLOCK_SIZE or d2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("pool shape mismatch")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S][max_blocks], context_lens [S]")
+    if out is None:
+        out = torch.empty(S, H, D, dtype=out_dtype or torch.float32, device=query.device)
+    if workspace is None:
+        nbytes = decode_workspace_size(S, H, hkv, D, int(max_context_len))
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=query.device)
+    st = load_library().pa_decode_attention(
+        _dev(out, "out"), _dtype_code(out.dtype), _dev(query, "query"), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"), block_tables.shape[1],
+        _dev(context_lens, "context_lens"), int(max_context_len), S, H, hkv, D, nb,
+        float(scale), _dtype_code(query.dtype), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _opt_ptr(error_word, "error_word"),
+        _stream_ptr(stream, query.device))
+    _check(st, "pa_decode_attention")
+    return out
+
+
+def copy_blocks(k_caches: Sequence, v_caches: Sequence, block_pairs, error_word=None,
+                stream=None) -> None:
+    """For every layer: pools[dst] = pools[src] for each (src, dst) row of
+    block_pairs (int64 [P][2], on the device)."""
+    import torch
+    if len(k_caches) != len(v_caches) or not k_caches:
+        raise ValueError("need the same, non-zero number of K and V pools")
+    if block_pairs.dtype != torch.int64:
+        raise TypeError("block_pairs must be int64")
+    nb, hkv, bs, d = k_caches[0].shape
+    for c in list(k_caches) + list(v_caches):
+        if c.shape != k_caches[0].shape or c.dtype != k_caches[0].dtype:
+            raise ValueError("all pools must have one shape and dtype")
+    L = len(k_caches)
+    kp = (ctypes.c_void_p * L)(*[_dev(c, "k_caches") for c in k_caches])
+    vp = (ctypes.c_void_p * L)(*[_dev(c, "v_caches") for c in v_caches])
+    npairs = block_pairs.shape[0] if block_pairs.numel() else 0
+    st = load_library().pa_copy_blocks(
+        ctypes.cast(kp, ctypes.c_void_p), ctypes.cast(vp, ctypes.c_void_p), L,
+        _dev(block_pairs, "block_pairs") if npairs else None, npairs, nb, hkv, d,
+        _dtype_code(k_caches[0].dtype), _opt_ptr(error_word, "error_word"),
+        _stream_ptr(stream, k_caches[0].device))
+    _check(st, "pa_copy_blocks")

@@ -1,0 +1,522 @@
+// pa_decode.cuh -- paged decode attention kernel for sm_103a.
+//
+// What it computes: for sequence s, query head h (KV head hk = h / G), the
+// softmax(scale * q . k_t) weighted sum of v_t over the L = context_lens[s]
+// tokens reached through block_tables[s], evaluated block by block with a
+// running (online) softmax and merged exactly across blocks, warps and
+// context partitions [Efficient Memory Management for Large Language Model
+// Serving with PagedAttention, "PagedAttention Algorithm": block-wise
+// reformulation of the attention equation; Paged Attention: Managing the KV
+// Cache Like Virtual Memory, "Attention over scattered blocks": running
+// softmax per query head sharing a KV head].
+//
+// How (one persistent CTA family per SM, warp-specialised):
+//   * A work item is (sequence, context partition of <= part_tokens tokens,
+//     KV head).  A plan kernel lists the (sequence, partition) pairs longest
+//     first; CTAs claim items with one atomic each, so the tail is short.
+//   * Warp 0 (producer) resolves the item's block-table slice once (one
+//     coalesced load for up to 32 blocks) and streams each block's K and V
+//     tiles -- 16 rows x head_dim contiguous, only the valid rows -- with 1-D
+//     bulk async copies (TMA) into an R-stage shared-memory ring guarded by
+//     mbarriers (full: transaction bytes; empty: one arrival per consumer
+//     warp).  The item's G query rows ride with its first block.
+//   * Warps 1..4 (consumers) each own 4 of a tile's 16 rows.  A row is split
+//     over head_dim/8 lanes (16-byte chunks), so a warp reads 512 contiguous
+//     bytes per instruction (no bank conflicts).  Scores: per-lane partial
+//     dots, reduced with xor shuffles over the row's lanes.  Every lane keeps
+//     its own running (max, sum, acc[8]) per query head over the rows it saw;
+//     states are merged (shuffles, then shared memory) when the item ends.
+//     Each K/V byte is read from HBM once and serves all G query heads.
+//   * Output: a one-partition item writes the normalised row (fp32 or the
+//     input type, round to nearest even); otherwise (max, sum, acc) go to the
+//     workspace and the merge kernel combines the partitions.
+// Scores are kept in base-2 units (q is pre-scaled by scale * log2 e) so the
+// exponentials are single ex2 instructions.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pa.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+constexpr int kBlock = PA_BLOCK_SIZE;  // tokens per KV block
+constexpr int kNCW = 4;                // consumer warps
+constexpr int kThreads = 32 * (kNCW + 1);
+constexpr int kRowsPerWarp = kBlock / kNCW;
+constexpr int kMaxPartTokens = 32 * kBlock;  // one producer lane per block of an item
+constexpr int kEndFlag = 1;
+
+struct alignas(16) StageMeta {
+    int s, hk, p, nparts;
+    int j, nblk, nvalid, flags;
+};
+
+struct WsHeader {
+    unsigned int counter;   // next item to claim
+    unsigned int n_items;   // (sequence, partition, kv head) items in the plan
+};
+
+struct DecodeParams {
+    void *out;
+    int out_dtype;  // PA_F16, PA_BF16 or PA_F32
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_tables;
+    int max_blocks_per_seq;
+    const int32_t *context_lens;
+    int max_context_len;
+    int num_seqs, num_heads, num_kv_heads, G, head_dim, num_blocks;
+    float scale_log2;  // scale * log2(e)
+    int part_tokens, max_parts;
+    WsHeader *hdr;
+    int4 *items;  // (s, p, ntok, nparts) per (sequence, partition)
+    float *part_m, *part_l, *part_acc;
+    unsigned int *err;
+};
+
+template <typename T>
+struct Cvt;
+template <>
+struct Cvt<__half> {
+    static __device__ __forceinline__ void to_f32(const uint4 &u, float *f) {
+        const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 x = __half22float2(h[i]);
+            f[2 * i] = x.x;
+            f[2 * i + 1] = x.y;
+        }
+    }
+};
+template <>
+struct Cvt<__nv_bfloat16> {
+    static __device__ __forceinline__ void to_f32(const uint4 &u, float *f) {
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 x = __bfloat1622float2(h[i]);
+            f[2 * i] = x.x;
+            f[2 * i + 1] = x.y;
+        }
+    }
+};
+
+__device__ __forceinline__ void store_out(void *out, int dtype, size_t idx, float v) {
+    if (dtype == PA_F32)
+        static_cast<float *>(out)[idx] = v;
+    else if (dtype == PA_F16)
+        static_cast<__half *>(out)[idx] = __float2half_rn(v);
+    else
+        static_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
+}
+
+// Shared-memory layout of one CTA.
+template <int D, int GM, int R>
+struct Layout {
+    static constexpr size_t kTileElems = (size_t)kBlock * D;
+    static constexpr size_t k_off = 0;
+    static constexpr size_t v_off = k_off + (size_t)R * kTileElems * 2;
+    static constexpr size_t q_off = v_off + (size_t)R * kTileElems * 2;
+    static constexpr size_t acc_off = q_off + (size_t)R * GM * D * 2;       // f32 [NCW][GM][D]
+    static constexpr size_t m_off = acc_off + (size_t)kNCW * GM * D * 4;    // f32 [NCW][GM]
+    static constexpr size_t l_off = m_off + (size_t)kNCW * GM * 4;          // f32 [NCW][GM]
+    static constexpr size_t meta_off = (l_off + (size_t)kNCW * GM * 4 + 15) / 16 * 16;
+    static constexpr size_t bar_off = meta_off + (size_t)R * sizeof(StageMeta);  // full[R], empty[R]
+    static constexpr size_t cbar_off = bar_off + (size_t)2 * R * 8;  // consumer item barriers [2]
+    static constexpr size_t flag_off = cbar_off + 2 * 8;
+    static constexpr size_t bytes = flag_off + 16;
+};
+
+// Ring depth and CTAs per SM for a (head_dim, group) instantiation: as many
+// 16-token K+V stages as fit the shared-memory share of one CTA.
+template <int D, int GM>
+struct Tuning {
+    static constexpr int kMinBlocks = GM <= 2 ? 3 : 2;
+    static constexpr size_t kBudget = 233472 / kMinBlocks - 1024 - 512;
+    static constexpr size_t kStage = (size_t)2 * kBlock * D * 2 + (size_t)GM * D * 2 + 32 + 16;
+    static constexpr size_t kFixed = (size_t)kNCW * GM * (D + 2) * 4 + 64;
+    static constexpr int kRaw = (int)((kBudget - kFixed) / kStage);
+    static constexpr int kStages = kRaw > 16 ? 16 : kRaw;
+    static_assert(kStages >= 2, "ring too shallow");
+};
+
+// ---------------------------------------------------------------------------
+// producer warp
+// ---------------------------------------------------------------------------
+template <int D, int GM, typename T, int R>
+__device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv, T *sq,
+                                             StageMeta *meta, uint64_t *full, uint64_t *empty,
+                                             volatile int *abort_flag, int lane) {
+    pdl_wait();  // the plan kernel's items and counter are ready
+    const unsigned n_items = P.hdr->n_items;
+    const unsigned Hkv = (unsigned)P.num_kv_heads;
+    const int G = P.G;
+    const int PB = P.part_tokens / kBlock;
+    const uint64_t policy = l2_evict_first_policy();
+    const T *kc = static_cast<const T *>(P.k_cache);
+    const T *vc = static_cast<const T *>(P.v_cache);
+    const T *qg = static_cast<const T *>(P.q);
+    constexpr size_t kTile = (size_t)kBlock * D;
+
+    auto claim = [&]() -> unsigned { return lane == 0 ? atomicAdd(&P.hdr->counter, 1u) : 0u; };
+    auto bcast = [&](unsigned v) -> unsigned { return __shfl_sync(0xffffffffu, v, 0); };
+    auto load_entry = [&](unsigned c) -> int4 {
+        return c < n_items ? P.items[c / Hkv] : make_int4(0, 0, 0, 0);
+    };
+    auto load_tab = [&](unsigned c, int4 e) -> int {
+        const int nblk = (e.z + kBlock - 1) / kBlock;
+        if (c < n_items && lane < nblk)
+            return __ldg(&P.block_tables[(size_t)e.x * P.max_blocks_per_seq + (size_t)e.y * PB +
+                                         lane]);
+        return -1;
+    };
+
+    // Software pipeline over items: claim (atomic) -> entry load -> table
+    // load -> copy issue, each stage one item ahead of the next, so the
+    // latencies of the dependent loads overlap the previous item's copies.
+    unsigned cA = bcast(claim());
+    int4 eA = load_entry(cA);
+    int tA = load_tab(cA, eA);
+    unsigned cB = bcast(claim());
+    int4 eB = load_entry(cB);
+    unsigned raw = claim();
+
+    uint32_t k = 0;  // stages issued so far
+    bool aborted = false;
+    while (cA < n_items) {
+        const int tB = load_tab(cB, eB);
+        const unsigned cC = bcast(raw);
+        const int4 eC = load_entry(cC);
+        raw = claim();
+
+        const int s = eA.x, part = eA.y, ntok = eA.z, nparts = eA.w;
+        const int hk = (int)(cA % Hkv);
+        const int nblk = (ntok + kBlock - 1) / kBlock;
+        for (int j = 0; j < nblk; ++j, ++k) {
+            const int slot = (int)(k % R);
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(&empty[slot], ((k / R) & 1u) ^ 1u, abort_flag);
+            if (!__shfl_sync(0xffffffffu, (int)ok, 0)) {  // warp-uniform outcome
+                aborted = true;
+                break;
+            }
+            const int phys = __shfl_sync(0xffffffffu, tA, j);
+            if (lane == 0) {
+                int nvalid = min(kBlock, ntok - j * kBlock);
+                if (phys < 0 || phys >= P.num_blocks) {
+                    if (P.err) atomicOr(P.err, PA_ERRBIT_BLOCK_OOB);
+                    nvalid = 0;  // skip the block
+                }
+                StageMeta m;
+                m.s = s; m.hk = hk; m.p = part; m.nparts = nparts;
+                m.j = j; m.nblk = nblk; m.nvalid = nvalid; m.flags = 0;
+                meta[slot] = m;
+                const uint32_t kv_bytes = (uint32_t)nvalid * D * (uint32_t)sizeof(T);
+                const uint32_t q_bytes = j == 0 ? (uint32_t)(G * D * sizeof(T)) : 0u;
+                mbar_arrive_expect_tx(&full[slot], 2 * kv_bytes + q_bytes);
+                if (kv_bytes) {
+                    const size_t off = ((size_t)phys * Hkv + hk) * kTile;
+                    bulk_g2s(sk + slot * kTile, kc + off, kv_bytes, &full[slot], policy);
+                    bulk_g2s(sv + slot * kTile, vc + off, kv_bytes, &full[slot], policy);
+                }
+                if (q_bytes)
+                    bulk_g2s_nohint(sq + (size_t)slot * GM * D,
+                                    qg + ((size_t)s * P.num_heads + (size_t)hk * G) * D, q_bytes,
+                                    &full[slot]);
+            }
+            __syncwarp();
+        }
+        if (aborted) break;
+        cA = cB; eA = eB; tA = tB;
+        cB = cC; eB = eC;
+    }
+    if (!aborted) {  // end-of-work marker for the consumers
+        const int slot = (int)(k % R);
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&empty[slot], ((k / R) & 1u) ^ 1u, abort_flag);
+        if (__shfl_sync(0xffffffffu, (int)ok, 0)) {
+            if (lane == 0) {
+                StageMeta m = {};
+                m.flags = kEndFlag;
+                meta[slot] = m;
+                mbar_arrive(&full[slot]);
+            }
+        } else {
+            aborted = true;
+        }
+    }
+    if (aborted) {
+        if (lane == 0) {
+            *abort_flag = 1;
+            if (P.err) atomicOr(P.err, PA_ERRBIT_TIMEOUT);
+        }
+        // let the copies already issued land before the CTA can exit
+        if (lane == 0) {
+            volatile int never = 0;
+            const uint32_t first = k > (uint32_t)R ? k - R : 0u;
+            for (uint32_t kk = first; kk < k; ++kk) mbar_wait(&full[kk % R], (kk / R) & 1u, &never);
+        }
+        __syncwarp();
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------
+// consumer warps
+// ---------------------------------------------------------------------------
+template <int D, int GM, typename T, int R>
+__device__ __forceinline__ void run_consumer(const DecodeParams &P, const T *sk, const T *sv,
+                                             const T *sq, const StageMeta *meta, uint64_t *full,
+                                             uint64_t *empty, uint64_t *cbar, float *s_acc,
+                                             float *s_m, float *s_l, volatile int *abort_flag,
+                                             int cw, int lane) {
+    constexpr int LPR = D / 8;           // lanes per row (16-byte chunks per row)
+    constexpr int RPI = 32 / LPR;        // rows per warp instruction
+    constexpr int NI = kRowsPerWarp / RPI;  // rows per lane per tile
+    static_assert(NI >= 1, "head_dim too large");
+    constexpr size_t kTile = (size_t)kBlock * D;
+    const int c = lane % LPR, rg = lane / LPR;
+    const int G = P.G;
+    const int tid = cw * 32 + lane;
+    uint32_t item_par = 0;  // phase parity of the consumer item barriers
+    // Bounded barrier over the 128 consumer threads; false if it gave up.
+    auto consumer_sync = [&](uint64_t *bar) -> bool {
+        mbar_arrive(bar);
+        const bool ok = mbar_wait(bar, item_par, abort_flag);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        if (lane == 0) {
+            *abort_flag = 1;
+            if (P.err) atomicOr(P.err, PA_ERRBIT_TIMEOUT);
+        }
+        return false;
+    };
+
+    float q[GM][8], acc[GM][8], m[GM], l[GM];
+#pragma unroll
+    for (int g = 0; g < GM; ++g) {
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[g][e] = acc[g][e] = 0.f;
+    }
+
+    for (uint32_t k = 0;; ++k) {
+        const int slot = (int)(k % R);
+        const bool ok = mbar_wait(&full[slot], (k / R) & 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {  // warp-uniform outcome
+            if (lane == 0) {
+                *abort_flag = 1;
+                if (P.err) atomicOr(P.err, PA_ERRBIT_TIMEOUT);
+            }
+            return;
+        }
+        const StageMeta mt = meta[slot];
+        if (mt.flags & kEndFlag) return;
+        const T *tk = sk + slot * kTile;
+        const T *tv = sv + slot * kTile;
+
+        if (mt.j == 0) {  // new item: load its query rows, reset the running state
+            const T *tq = sq + (size_t)slot * GM * D;
+#pragma unroll
+            for (int g = 0; g < GM; ++g) {
+                if (g < G) {
+                    float f[8];
+                    Cvt<T>::to_f32(*reinterpret_cast<const uint4 *>(tq + g * D + c * 8), f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) q[g][e] = f[e] * P.scale_log2;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) q[g][e] = 0.f;
+                }
+                m[g] = -INFINITY;
+                l[g] = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+            }
+        }
+
+        // scores for this lane's rows
+        float sc[NI][GM];
+        bool valid[NI];
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const int r = cw * kRowsPerWarp + i * RPI + rg;
+            valid[i] = r < mt.nvalid;
+            float kf[8];
+            if (valid[i]) {
+                Cvt<T>::to_f32(*reinterpret_cast<const uint4 *>(tk + r * D + c * 8), kf);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) kf[e] = 0.f;
+            }
+#pragma unroll
+            for (int g = 0; g < GM; ++g) {
+                float a = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a = fmaf(q[g][e], kf[e], a);
+                sc[i][g] = a;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NI; ++i)
+#pragma unroll
+            for (int g = 0; g < GM; ++g)
+#pragma unroll
+                for (int off = LPR / 2; off > 0; off >>= 1)
+                    sc[i][g] += __shfl_xor_sync(0xffffffffu, sc[i][g], off);
+
+        // running softmax over the rows this lane has seen
+        float pr[NI][GM];
+#pragma unroll
+        for (int g = 0; g < GM; ++g) {
+            float mx = m[g];
+#pragma unroll
+            for (int i = 0; i < NI; ++i)
+                if (valid[i]) mx = fmaxf(mx, sc[i][g]);
+            const float ms = mx == -INFINITY ? 0.f : mx;
+            const float alpha = ex2(m[g] - ms);
+            l[g] *= alpha;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
+#pragma unroll
+            for (int i = 0; i < NI; ++i) {
+                pr[i][g] = valid[i] ? ex2(sc[i][g] - ms) : 0.f;
+                l[g] += pr[i][g];
+            }
+            m[g] = mx;
+        }
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            if (valid[i]) {
+                const int r = cw * kRowsPerWarp + i * RPI + rg;
+                float vf[8];
+                Cvt<T>::to_f32(*reinterpret_cast<const uint4 *>(tv + r * D + c * 8), vf);
+#pragma unroll
+                for (int g = 0; g < GM; ++g)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(pr[i][g], vf[e], acc[g][e]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);  // tile consumed
+
+        if (mt.j != mt.nblk - 1) continue;
+
+        // ---- item complete: merge lane states, then warp states ----
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1) {
+#pragma unroll
+            for (int g = 0; g < GM; ++g) {
+                const float mo = __shfl_xor_sync(0xffffffffu, m[g], off);
+                const float lo = __shfl_xor_sync(0xffffffffu, l[g], off);
+                const float M = fmaxf(m[g], mo);
+                const float Ms = M == -INFINITY ? 0.f : M;
+                const float a = ex2(m[g] - Ms), b = ex2(mo - Ms);
+                l[g] = l[g] * a + lo * b;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float ao = __shfl_xor_sync(0xffffffffu, acc[g][e], off);
+                    acc[g][e] = acc[g][e] * a + ao * b;
+                }
+                m[g] = M;
+            }
+        }
+        if (rg == 0) {
+#pragma unroll
+            for (int g = 0; g < GM; ++g) {
+                float *dst = s_acc + ((size_t)cw * GM + g) * D + c * 8;
+                *reinterpret_cast<float4 *>(dst) = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+                *reinterpret_cast<float4 *>(dst + 4) = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
+                if (lane == 0) {
+                    s_m[cw * GM + g] = m[g];
+                    s_l[cw * GM + g] = l[g];
+                }
+            }
+        }
+        if (!consumer_sync(&cbar[0])) return;
+        const int H = P.num_heads;
+        for (int idx = tid; idx < G * D; idx += kNCW * 32) {
+            const int g = idx / D, d = idx - g * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kNCW; ++w) M = fmaxf(M, s_m[w * GM + g]);
+            const float Ms = M == -INFINITY ? 0.f : M;
+            float Lsum = 0.f, o = 0.f;
+#pragma unroll
+            for (int w = 0; w < kNCW; ++w) {
+                const float cf = ex2(s_m[w * GM + g] - Ms);
+                Lsum += s_l[w * GM + g] * cf;
+                o += s_acc[((size_t)w * GM + g) * D + d] * cf;
+            }
+            const int h = mt.hk * G + g;
+            if (mt.nparts == 1) {
+                store_out(P.out, P.out_dtype, ((size_t)mt.s * H + h) * D + d,
+                          Lsum > 0.f ? o / Lsum : 0.f);
+            } else {
+                const size_t pi = ((size_t)mt.s * H + h) * P.max_parts + mt.p;
+                P.part_acc[pi * D + d] = o;
+                if (d == 0) {
+                    P.part_m[pi] = M;
+                    P.part_l[pi] = Lsum;
+                }
+            }
+        }
+        if (!consumer_sync(&cbar[1])) return;  // merge buffer free for the next item
+        item_par ^= 1u;
+    }
+}
+
+template <int D, int GM, typename T, int R, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) paged_decode_kernel(const __grid_constant__ DecodeParams P) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    using L = Layout<D, GM, R>;
+    T *sk = reinterpret_cast<T *>(smem + L::k_off);
+    T *sv = reinterpret_cast<T *>(smem + L::v_off);
+    T *sq = reinterpret_cast<T *>(smem + L::q_off);
+    float *s_acc = reinterpret_cast<float *>(smem + L::acc_off);
+    float *s_m = reinterpret_cast<float *>(smem + L::m_off);
+    float *s_l = reinterpret_cast<float *>(smem + L::l_off);
+    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + L::meta_off);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bar_off);
+    uint64_t *empty = full + R;
+    uint64_t *cbar = reinterpret_cast<uint64_t *>(smem + L::cbar_off);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::flag_off);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int r = 0; r < R; ++r) {
+            mbar_init(&full[r], 1);
+            mbar_init(&empty[r], kNCW);
+        }
+        mbar_init(&cbar[0], kNCW * 32);
+        mbar_init(&cbar[1], kNCW * 32);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0)
+        run_producer<D, GM, T, R>(P, sk, sv, sq, meta, full, empty, abort_flag, lane);
+    else
+        run_consumer<D, GM, T, R>(P, sk, sv, sq, meta, full, empty, cbar, s_acc, s_m, s_l,
+                                  abort_flag, warp - 1, lane);
+}
+
+// Host-side launcher for one head_dim (defined in pa_decode_d{64,128,256}.cu).
+pa_status_t launch_decode_d64(const DecodeParams &P, pa_dtype_t dtype, int grid_cap,
+                              cudaStream_t stream);
+pa_status_t launch_decode_d128(const DecodeParams &P, pa_dtype_t dtype, int grid_cap,
+                               cudaStream_t stream);
+pa_status_t launch_decode_d256(const DecodeParams &P, pa_dtype_t dtype, int grid_cap,
+                               cudaStream_t stream);
+
+// Number of streaming multiprocessors of the current device (cached).
+int current_sm_count();
+
+}  // namespace pa

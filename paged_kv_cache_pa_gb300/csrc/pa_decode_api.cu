@@ -1,0 +1,285 @@
+// pa_decode_api.cu -- pa_decode_attention / pa_decode_workspace_size: the plan
+// kernel, the partition merge kernel and the host-side checks and launches.
+//
+// Context split: a sequence longer than part_tokens is cut into partitions of
+// part_tokens tokens; every (sequence, partition, KV head) is an independent
+// work item whose partial softmax state (max m, sum l, weighted values acc)
+// is merged exactly afterwards:
+//     M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  o = sum_p acc_p 2^(m_p - M) / L
+// [vLLM Internals ..., "The kernel pays for the indirection": a grid axis over
+// partitions; Paged Attention: Managing the KV Cache Like Virtual Memory,
+// "Attention over scattered blocks": slices and a merge kernel; Efficient
+// Memory Management ..., "PagedAttention Algorithm": blocks may be processed
+// in any order and combined].
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+
+#include "pa_decode.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr int kMinPartTokens = 64;
+constexpr long long kTargetItems = 2048;  // ~ 152 SMs x resident CTAs x a few items each
+
+int choose_part_tokens(int num_seqs, int num_kv_heads, int max_context_len) {
+    int p = kMaxPartTokens;
+    const long long units = (long long)num_seqs * num_kv_heads;
+    while (p > kMinPartTokens) {
+        const long long items = units * ((max_context_len + p - 1) / p);
+        if (items >= kTargetItems) break;
+        p /= 2;
+    }
+    return p;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct WsLayout {
+    int part_tokens, max_parts;
+    size_t items_off, m_off, l_off, acc_off, bytes;
+};
+
+WsLayout ws_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                   int max_context_len) {
+    WsLayout w;
+    w.part_tokens = choose_part_tokens(num_seqs, num_kv_heads, max_context_len);
+    w.max_parts = max_context_len > 0 ? (max_context_len + w.part_tokens - 1) / w.part_tokens : 1;
+    size_t off = align256(sizeof(WsHeader));
+    w.items_off = off;
+    off = align256(off + (size_t)num_seqs * w.max_parts * sizeof(int4));
+    if (w.max_parts > 1) {
+        const size_t n = (size_t)num_seqs * num_heads * w.max_parts;
+        w.m_off = off;
+        off = align256(off + n * 4);
+        w.l_off = off;
+        off = align256(off + n * 4);
+        w.acc_off = off;
+        off = align256(off + n * head_dim * 4);
+    } else {
+        w.m_off = w.l_off = w.acc_off = off;
+    }
+    w.bytes = off;
+    return w;
+}
+
+// One CTA: count (sequence, partition) pairs by size, lay them out longest
+// first (a counting sort on the number of blocks), reset the claim counter,
+// and zero the output rows of empty sequences.
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ lens, int num_seqs,
+                                                    int max_context_len, int part_tokens,
+                                                    int num_kv_heads, int num_heads, int head_dim,
+                                                    int4 *__restrict__ items, WsHeader *hdr,
+                                                    void *out, int out_dtype, unsigned int *err) {
+    pdl_trigger();  // the attention CTAs may start their set-up now
+    __shared__ int hist[kMaxPartTokens / kBlock + 1];
+    __shared__ int offs[kMaxPartTokens / kBlock + 1];
+    const int PB = part_tokens / kBlock;
+    for (int i = threadIdx.x; i <= PB; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
+        int L = lens[s];
+        if (L < 0 || L > max_context_len) {
+            if (err) atomicOr(err, PA_ERRBIT_CONTEXT_LEN);
+            L = 0;
+        }
+        if (L == 0) continue;
+        const int np = (L + part_tokens - 1) / part_tokens;
+        if (np > 1) atomicAdd(&hist[PB], np - 1);
+        const int last = L - (np - 1) * part_tokens;
+        atomicAdd(&hist[(last + kBlock - 1) / kBlock], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int key = PB; key >= 1; --key) {
+            offs[key] = run;
+            run += hist[key];
+        }
+        hdr->counter = 0u;
+        hdr->n_items = (unsigned)run * (unsigned)num_kv_heads;
+    }
+    __syncthreads();
+    for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
+        const int L = lens[s];
+        if (L <= 0 || L > max_context_len) continue;
+        const int np = (L + part_tokens - 1) / part_tokens;
+        for (int p = 0; p < np; ++p) {
+            const int ntok = min(part_tokens, L - p * part_tokens);
+            const int pos = atomicAdd(&offs[(ntok + kBlock - 1) / kBlock], 1);
+            items[pos] = make_int4(s, p, ntok, np);
+        }
+    }
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nw = blockDim.x / 32;
+    for (int s = warp; s < num_seqs; s += nw) {
+        const int L = lens[s];
+        if (L > 0 && L <= max_context_len) continue;
+        const size_t base = (size_t)s * num_heads * head_dim;
+        for (int i = lane; i < num_heads * head_dim; i += 32) store_out(out, out_dtype, base + i, 0.f);
+    }
+}
+
+// One warp per (sequence, query head) of a multi-partition sequence.
+template <int D>
+__global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ DecodeParams P) {
+    pdl_wait();  // partials from the attention kernel
+    constexpr int E = D / 32;
+    const int s = blockIdx.x;
+    const int h = blockIdx.y * 4 + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (h >= P.num_heads) return;
+    const int L = P.context_lens[s];
+    if (L <= P.part_tokens || L > P.max_context_len) return;  // one partition, or invalid
+    const int np = (L + P.part_tokens - 1) / P.part_tokens;
+    const size_t base = ((size_t)s * P.num_heads + h) * P.max_parts;
+    float M = -INFINITY;
+    for (int p = lane; p < np; p += 32) M = fmaxf(M, P.part_m[base + p]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float Ms = M == -INFINITY ? 0.f : M;
+    float o[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] = 0.f;
+    float Lsum = 0.f;
+    for (int p = 0; p < np; ++p) {
+        const float cf = ex2(P.part_m[base + p] - Ms);
+        Lsum += P.part_l[base + p] * cf;
+        const float *a = P.part_acc + (base + p) * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = fmaf(a[e], cf, o[e]);
+    }
+    const size_t ob = ((size_t)s * P.num_heads + h) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) store_out(P.out, P.out_dtype, ob + e, Lsum > 0.f ? o[e] / Lsum : 0.f);
+}
+
+std::atomic<int> g_sm_count[64];
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+int current_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            n = 1;
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                           int head_dim, int max_context_len) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len < 0)
+        return 0;
+    return ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len).bytes;
+}
+
+extern "C" int pa_decode_partition_tokens(int num_seqs, int num_kv_heads, int max_context_len) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || max_context_len < 0) return 0;
+    return choose_part_tokens(num_seqs, num_kv_heads, max_context_len);
+}
+
+extern "C" pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, const void *query,
+                                           const void *k_cache, const void *v_cache,
+                                           const int32_t *block_tables, int max_blocks_per_seq,
+                                           const int32_t *context_lens, int max_context_len,
+                                           int num_seqs, int num_heads, int num_kv_heads,
+                                           int head_dim, int num_blocks, float scale,
+                                           pa_dtype_t dtype, void *workspace,
+                                           size_t workspace_bytes, unsigned int *dev_error_word,
+                                           pa_stream_t stream) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
+        max_blocks_per_seq <= 0 || max_context_len < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (out_dtype != PA_F32 && out_dtype != dtype) return PA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
+    if (num_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
+    if ((long long)max_context_len > (long long)PA_BLOCK_SIZE * max_blocks_per_seq)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(query, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return PA_ERR_WORKSPACE;
+    const WsLayout w = ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len);
+    if (workspace_bytes < w.bytes) return PA_ERR_WORKSPACE;
+
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    DecodeParams P;
+    P.out = out;
+    P.out_dtype = (int)out_dtype;
+    P.q = query;
+    P.k_cache = k_cache;
+    P.v_cache = v_cache;
+    P.block_tables = block_tables;
+    P.max_blocks_per_seq = max_blocks_per_seq;
+    P.context_lens = context_lens;
+    P.max_context_len = max_context_len;
+    P.num_seqs = num_seqs;
+    P.num_heads = num_heads;
+    P.num_kv_heads = num_kv_heads;
+    P.G = num_heads / num_kv_heads;
+    P.head_dim = head_dim;
+    P.num_blocks = num_blocks;
+    P.scale_log2 = scale * 1.4426950408889634f;
+    P.part_tokens = w.part_tokens;
+    P.max_parts = w.max_parts;
+    P.hdr = reinterpret_cast<WsHeader *>(ws);
+    P.items = reinterpret_cast<int4 *>(ws + w.items_off);
+    P.part_m = reinterpret_cast<float *>(ws + w.m_off);
+    P.part_l = reinterpret_cast<float *>(ws + w.l_off);
+    P.part_acc = reinterpret_cast<float *>(ws + w.acc_off);
+    P.err = dev_error_word;
+    cudaStream_t st = (cudaStream_t)stream;
+
+    plan_kernel<<<1, 1024, 0, st>>>(context_lens, num_seqs, max_context_len, w.part_tokens,
+                                    num_kv_heads, num_heads, head_dim, P.items, P.hdr, out,
+                                    (int)out_dtype, dev_error_word);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+
+    long long cap = (long long)num_seqs * w.max_parts * num_kv_heads;
+    if (cap > INT_MAX) cap = INT_MAX;
+    pa_status_t st_launch;
+    if (head_dim == 64)
+        st_launch = launch_decode_d64(P, dtype, (int)cap, st);
+    else if (head_dim == 128)
+        st_launch = launch_decode_d128(P, dtype, (int)cap, st);
+    else
+        st_launch = launch_decode_d256(P, dtype, (int)cap, st);
+    if (st_launch != PA_OK) return st_launch;
+
+    if (w.max_parts > 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)num_seqs, (unsigned)((num_heads + 3) / 4));
+        cfg.blockDim = dim3(128);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e;
+        if (head_dim == 64)
+            e = cudaLaunchKernelEx(&cfg, merge_kernel<64>, P);
+        else if (head_dim == 128)
+            e = cudaLaunchKernelEx(&cfg, merge_kernel<128>, P);
+        else
+            e = cudaLaunchKernelEx(&cfg, merge_kernel<256>, P);
+        if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}

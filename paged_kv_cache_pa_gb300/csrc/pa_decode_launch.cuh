@@ -1,0 +1,73 @@
+// pa_decode_launch.cuh -- host-side launch of one paged_decode_kernel
+// instantiation: shared-memory attribute and occupancy (cached per device),
+// persistent grid of min(items, SMs x resident CTAs), programmatic dependent
+// launch after the plan kernel.
+#pragma once
+
+#include <atomic>
+
+#include "pa_decode.cuh"
+
+namespace pa {
+
+constexpr int kMaxDevices = 64;
+
+template <int D, int GM, typename T>
+pa_status_t launch_one(const DecodeParams &P, int grid_cap, cudaStream_t stream) {
+    using Tn = Tuning<D, GM>;
+    constexpr int R = Tn::kStages;
+    constexpr int MINB = Tn::kMinBlocks;
+    using L = Layout<D, GM, R>;
+    auto kern = paged_decode_kernel<D, GM, T, R, MINB>;
+    static std::atomic<int> occ_cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+    int occ = occ_cache[dev].load(std::memory_order_relaxed);
+    if (occ == 0) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)L::bytes) != cudaSuccess)
+            return PA_ERR_CUDA;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, L::bytes) !=
+            cudaSuccess)
+            return PA_ERR_CUDA;
+        if (occ < 1) return PA_ERR_UNSUPPORTED;
+        occ_cache[dev].store(occ, std::memory_order_relaxed);
+    }
+    long long grid = (long long)current_sm_count() * occ;
+    if (grid > grid_cap) grid = grid_cap;
+    if (grid < 1) grid = 1;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, P) != cudaSuccess) return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+template <int D, typename T>
+pa_status_t dispatch_group(const DecodeParams &P, int grid_cap, cudaStream_t stream) {
+    const int G = P.G;
+    if (G == 1) return launch_one<D, 1, T>(P, grid_cap, stream);
+    if (G == 2) return launch_one<D, 2, T>(P, grid_cap, stream);
+    if (G <= 4) return launch_one<D, 4, T>(P, grid_cap, stream);
+    if (G <= 6) return launch_one<D, 6, T>(P, grid_cap, stream);
+    if (G <= 8) return launch_one<D, 8, T>(P, grid_cap, stream);
+    return PA_ERR_UNSUPPORTED;
+}
+
+template <int D>
+pa_status_t dispatch_dtype(const DecodeParams &P, pa_dtype_t dtype, int grid_cap,
+                           cudaStream_t stream) {
+    if (dtype == PA_F16) return dispatch_group<D, __half>(P, grid_cap, stream);
+    if (dtype == PA_BF16) return dispatch_group<D, __nv_bfloat16>(P, grid_cap, stream);
+    return PA_ERR_INVALID_ARG;
+}
+
+}  // namespace pa

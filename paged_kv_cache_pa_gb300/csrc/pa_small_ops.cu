@@ -1,0 +1,150 @@
+// pa_small_ops.cu -- pa_cache_write, pa_copy_blocks, pa_status_string.
+//
+// Both kernels move bytes unchanged with 16-byte vector loads and stores:
+//   - cache write: one CTA per new token; the token's Hkv rows of K and of V
+//     (Hkv * head_dim * 2 bytes each) go to block slot/16, offset slot%16
+//     [Efficient Memory Management for Large Language Model Serving with
+//     PagedAttention, "Kernel-Level Optimizations", 1. fused reshape and
+//     block write].
+//   - block copy: a grid over (pair, layer x {K, V}, chunk); every CTA copies
+//     one contiguous chunk of one block, so all pairs and layers go in a
+//     single launch [same section, 3. fused block copy].
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pa.h"
+
+namespace {
+
+constexpr int kBlock = PA_BLOCK_SIZE;
+
+__global__ void __launch_bounds__(128) cache_write_kernel(
+    const uint4 *__restrict__ key, const uint4 *__restrict__ value, uint4 *__restrict__ k_cache,
+    uint4 *__restrict__ v_cache, const int64_t *__restrict__ slot_mapping, long long num_slots,
+    int num_kv_heads, int chunks_per_row, unsigned int *err) {
+    const int t = blockIdx.x;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) return;                                  // padding token
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0 && err) atomicOr(err, PA_ERRBIT_SLOT_OOB);
+        return;
+    }
+    const int64_t blk = slot / kBlock, off = slot % kBlock;
+    const int total = num_kv_heads * chunks_per_row;
+    const size_t src_base = (size_t)t * total;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int h = i / chunks_per_row, c = i - h * chunks_per_row;
+        const size_t dst = (((size_t)blk * num_kv_heads + h) * kBlock + off) * chunks_per_row + c;
+        const uint4 kv = __ldg(key + src_base + i);
+        const uint4 vv = __ldg(value + src_base + i);
+        k_cache[dst] = kv;
+        v_cache[dst] = vv;
+    }
+}
+
+struct LayerPools {
+    uint4 *k[PA_MAX_LAYERS];
+    uint4 *v[PA_MAX_LAYERS];
+};
+
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+
+__global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
+    const LayerPools pools, const int64_t *__restrict__ pairs, int num_blocks,
+    long long chunks_per_block, long long chunks_per_cta, unsigned int *err) {
+    const int pair = blockIdx.x;
+    const int layer = blockIdx.y >> 1;
+    const int which = blockIdx.y & 1;
+    const int64_t src = pairs[2 * pair], dst = pairs[2 * pair + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && err)
+            atomicOr(err, PA_ERRBIT_BLOCK_OOB);
+        return;
+    }
+    if (src == dst) return;
+    uint4 *base = which ? pools.v[layer] : pools.k[layer];
+    const uint4 *s = base + (size_t)src * chunks_per_block;
+    uint4 *d = base + (size_t)dst * chunks_per_block;
+    const long long c0 = (long long)blockIdx.z * chunks_per_cta;
+    long long c1 = c0 + chunks_per_cta;
+    if (c1 > chunks_per_block) c1 = chunks_per_block;
+    long long i = c0 + threadIdx.x;
+    for (; i + (kCopyUnroll - 1) * kCopyThreads < c1; i += kCopyUnroll * kCopyThreads) {
+        uint4 r[kCopyUnroll];
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) r[u] = __ldcs(s + i + u * kCopyThreads);
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) __stcs(d + i + u * kCopyThreads, r[u]);
+    }
+    for (; i < c1; i += kCopyThreads) __stcs(d + i, __ldcs(s + i));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
+
+}  // namespace
+
+extern "C" pa_status_t pa_cache_write(const void *key, const void *value, void *k_cache,
+                                      void *v_cache, const int64_t *slot_mapping, int num_tokens,
+                                      int num_blocks, int num_kv_heads, int head_dim,
+                                      pa_dtype_t dtype, unsigned int *dev_error_word,
+                                      pa_stream_t stream) {
+    if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0) return PA_ERR_INVALID_ARG;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (!head_dim_ok(head_dim)) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    const int chunks_per_row = head_dim * 2 / 16;
+    cache_write_kernel<<<num_tokens, 128, 0, (cudaStream_t)stream>>>(
+        (const uint4 *)key, (const uint4 *)value, (uint4 *)k_cache, (uint4 *)v_cache,
+        slot_mapping, (long long)num_blocks * kBlock, num_kv_heads, chunks_per_row,
+        dev_error_word);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" pa_status_t pa_copy_blocks(void *const *k_caches, void *const *v_caches,
+                                      int num_layers, const int64_t *block_pairs, int num_pairs,
+                                      int num_blocks, int num_kv_heads, int head_dim,
+                                      pa_dtype_t dtype, unsigned int *dev_error_word,
+                                      pa_stream_t stream) {
+    if (num_layers <= 0 || num_pairs < 0 || num_blocks <= 0 || num_kv_heads <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_layers > PA_MAX_LAYERS) return PA_ERR_UNSUPPORTED;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (!head_dim_ok(head_dim)) return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PA_OK;
+    if (!k_caches || !v_caches || !block_pairs) return PA_ERR_INVALID_ARG;
+    LayerPools pools = {};
+    for (int l = 0; l < num_layers; ++l) {
+        if (!k_caches[l] || !v_caches[l] || !aligned16(k_caches[l]) || !aligned16(v_caches[l]))
+            return PA_ERR_INVALID_ARG;
+        pools.k[l] = (uint4 *)k_caches[l];
+        pools.v[l] = (uint4 *)v_caches[l];
+    }
+    const long long chunks_per_block = (long long)num_kv_heads * kBlock * head_dim * 2 / 16;
+    // about 32 KiB per CTA: enough bytes in flight per CTA, enough CTAs per copy
+    const long long chunks_per_cta = 2048;
+    const long long splits = (chunks_per_block + chunks_per_cta - 1) / chunks_per_cta;
+    if (num_pairs > 2147483647 || splits > 65535) return PA_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)num_pairs, (unsigned)(2 * num_layers), (unsigned)splits);
+    copy_blocks_kernel<<<grid, kCopyThreads, 0, (cudaStream_t)stream>>>(
+        pools, block_pairs, num_blocks, chunks_per_block, chunks_per_cta, dev_error_word);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" const char *pa_status_string(pa_status_t s) {
+    switch (s) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+        case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+    }
+    return "PA_ERR_UNKNOWN";
+}

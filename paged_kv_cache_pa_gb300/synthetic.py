@@ -109,9 +109,9 @@ def _deal_tables(lens: np.ndarray, ids: np.ndarray, max_blocks: Optional[int] = 
 
 def _slots_of_last(tables: np.ndarray, lens: np.ndarray) -> np.ndarray:
     """Slot of position L-1 of each sequence (the token the step writes)."""
-    pos = lens.astype(np.int64) - 1
+    pos = np.maximum(lens.astype(np.int64) - 1, 0)
     blk = tables[np.arange(len(lens)), pos // BLOCK_SIZE].astype(np.int64)
-    return blk * BLOCK_SIZE + pos % BLOCK_SIZE
+    return np.where(lens > 0, blk * BLOCK_SIZE + pos % BLOCK_SIZE, -1)   # empty: no token
 
 
 def _from_lengths(name, lens, num_heads, num_kv_heads, head_dim, dtype, seed,

@@ -1,0 +1,68 @@
+"""The C ABI library builds, loads on a machine without a GPU, and exports
+every entry point include/pa.h declares; the header is valid C; the product
+package never reaches the oracle.  No compute call is made here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_pa_gb300.build import build
+    path = build()
+    return ctypes.CDLL(path), path
+
+
+def test_header_declares_the_operations():
+    names = _declared()
+    for op in ("pa_cache_write", "pa_decode_attention", "pa_copy_blocks",
+               "pa_decode_workspace_size", "pa_status_string"):
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    cdll, path = lib
+    for name in _declared():
+        assert hasattr(cdll, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True)
+    exported = set(re.findall(r"\sT\s+(pa_\w+)", out.stdout))
+    assert set(_declared()) <= exported
+
+
+def test_header_is_plain_c():
+    subprocess.run(["gcc", "-fsyntax-only", "-std=c99", "-Wall", "-Werror", "-x", "c", HEADER],
+                   check=True)
+
+
+def test_status_strings_and_workspace_size(lib):
+    import paged_kv_cache_pa_gb300 as pa
+    assert pa.status_string(0) == "PA_OK"
+    assert pa.status_string(4) == "PA_ERR_WORKSPACE"
+    a = pa.decode_workspace_size(256, 40, 40, 128, 2048)
+    assert a == pa.decode_workspace_size(256, 40, 40, 128, 2048) > 0
+    # a larger bound never needs less workspace
+    assert pa.decode_workspace_size(256, 40, 40, 128, 4096) >= a
+    assert pa.decode_workspace_size(-1, 40, 40, 128, 2048) == 0
+
+
+def test_product_package_does_not_use_the_oracle():
+    pkg = os.path.join(ROOT, "paged_kv_cache_pa_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
+                assert "pa_oracle" not in src, f

@@ -1,0 +1,263 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+Bars: cache write and block copy bit-exact over whole pools (so stray writes
+show); attention max |gpu - oracle| <= 2e-3 on fp32 output; half-precision
+output within 2e-3 plus half an ulp of the output type at the oracle value,
+and bit-identical to rounding the fp32 output to nearest even.
+"""
+import numpy as np
+import pytest
+import torch
+
+from paritylib import (ATOL, codes, custom_workload, gpu_step, host_inputs, max_abs,
+                       oracle_step, step_blocks)
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU, skipped
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import paged_kv_cache_pa_gb300 as pa  # noqa: E402
+from paged_kv_cache_pa_gb300 import synthetic  # noqa: E402
+
+DEV = torch.device("cuda:0")
+
+
+def _err_word():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def _run_and_check(wl, poison=False, out_dtype=torch.float32, whole_pool=True,
+                   fill_all_blocks=None):
+    vals = synthetic.make_values(wl, device=DEV, fill_all_blocks=fill_all_blocks,
+                                 poison_unused=poison)
+    blocks = None if whole_pool else step_blocks(wl)
+    h = host_inputs(wl, vals, blocks)
+    err = _err_word()
+    out = gpu_step(wl, vals, out_dtype=out_dtype, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want = oracle_step(wl, h)
+    # pools after copy + write: bit-exact
+    if blocks is None:
+        got_k, got_v = codes(vals["k_cache"]), codes(vals["v_cache"])
+    else:
+        idx = torch.as_tensor(blocks, device=DEV)
+        got_k = codes(vals["k_cache"].index_select(0, idx))
+        got_v = codes(vals["v_cache"].index_select(0, idx))
+    assert np.array_equal(got_k, h["k_cache"])
+    assert np.array_equal(got_v, h["v_cache"])
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    return got, want
+
+
+# ---------------------------------------------------------------------------
+# the five workloads at full size
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "opt13b", "gqa", "beams"])
+def test_workload_step_parity(name):
+    wl = synthetic.make(name)
+    got, want = _run_and_check(wl)
+    err = max_abs(got, want)
+    print(f"{name}: max|gpu-oracle| = {err:.3e}")
+    assert err <= ATOL
+
+
+def test_long_context_partitions_parity():
+    """8 sequences of 16K-32K tokens scattered over a 60 GiB pool; the oracle
+    gets the blocks the step touches.  Untouched blocks stay as they were."""
+    wl = synthetic.make("long")
+    vals = synthetic.make_values(wl, device=DEV, fill_all_blocks=False)
+    blocks = step_blocks(wl)
+    rng = np.random.default_rng(0)
+    bystanders = np.setdiff1d(rng.choice(wl.num_blocks, 256, replace=False), blocks)
+    bidx = torch.as_tensor(bystanders, device=DEV)
+    before = codes(vals["k_cache"].index_select(0, bidx)), codes(vals["v_cache"].index_select(0, bidx))
+    h = host_inputs(wl, vals, blocks)
+    err = _err_word()
+    out = gpu_step(wl, vals, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want = oracle_step(wl, h)
+    idx = torch.as_tensor(blocks, device=DEV)
+    assert np.array_equal(codes(vals["k_cache"].index_select(0, idx)), h["k_cache"])
+    assert np.array_equal(codes(vals["v_cache"].index_select(0, idx)), h["v_cache"])
+    assert np.array_equal(codes(vals["k_cache"].index_select(0, bidx)), before[0])
+    assert np.array_equal(codes(vals["v_cache"].index_select(0, bidx)), before[1])
+    e = max_abs(out.cpu().numpy(), want)
+    print(f"long: max|gpu-oracle| = {e:.3e}")
+    assert e <= ATOL
+
+
+# ---------------------------------------------------------------------------
+# shapes, lengths and edge cases at sizes the oracle finishes in seconds
+# ---------------------------------------------------------------------------
+
+EDGE_LENS = [1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257, 511, 512,
+             513, 1023, 1024, 1025, 1500]
+
+
+@pytest.mark.parametrize("H,Hkv,D,dtype", [
+    (8, 8, 64, "f16"), (4, 4, 128, "f16"), (4, 4, 128, "bf16"), (4, 4, 256, "bf16"),
+    (8, 4, 128, "f16"), (12, 2, 128, "bf16"), (6, 2, 64, "f16"), (16, 2, 128, "f16"),
+    (10, 2, 256, "f16"), (5, 1, 128, "bf16"), (7, 1, 64, "bf16"),
+])
+def test_shapes_and_block_edges(H, Hkv, D, dtype):
+    wl = custom_workload(EDGE_LENS, H, Hkv, D, dtype, seed=H * 1000 + D)
+    got, want = _run_and_check(wl, poison=True)
+    assert max_abs(got, want) <= ATOL
+
+
+def test_partition_edges_at_512():
+    """Enough (sequence, KV head) units that the plan uses 512-token
+    partitions; lengths straddle the partition boundaries."""
+    lens = ([511, 512, 513, 1023, 1024, 1025, 1536, 1537, 2047, 2048] * 7)[:64]
+    wl = custom_workload(lens, 40, 40, 128, "f16", seed=3)
+    got, want = _run_and_check(wl)
+    assert max_abs(got, want) <= ATOL
+
+
+def test_poisoned_padding_is_never_read():
+    """NaN in every slot past each sequence's length and in every unused
+    block: the output stays finite and equal to the oracle's."""
+    wl = synthetic.make("tiny")
+    got, want = _run_and_check(wl, poison=True)
+    assert max_abs(got, want) <= ATOL
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_half_output_is_rounded_fp32_output(dtype):
+    wl = custom_workload([1, 5, 77, 300, 700], 8, 2, 128, dtype, seed=11)
+    tdt = torch.float16 if dtype == "f16" else torch.bfloat16
+    vals = synthetic.make_values(wl, device=DEV)
+    h = host_inputs(wl, vals)
+    # run twice on identical inputs: fp32 output and half output
+    vals2 = {k: v.clone() for k, v in vals.items()}
+    out32 = gpu_step(wl, vals)
+    out16 = gpu_step(wl, vals2, out_dtype=tdt)
+    torch.cuda.synchronize()
+    assert torch.equal(out32.to(tdt).view(torch.int16), out16.view(torch.int16))
+    want = oracle_step(wl, h)
+    # tolerance: 2e-3 plus half an ulp of the output type at |want|
+    mant = 10 if dtype == "f16" else 7
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(want), 2.0 ** -14))) - mant)
+    assert np.all(np.abs(out16.float().cpu().numpy() - want) <= ATOL + 0.5 * ulp)
+
+
+def test_context_of_one_returns_v0():
+    wl = custom_workload([1] * 9, 12, 2, 128, "bf16", seed=5)
+    vals = synthetic.make_values(wl, device=DEV)
+    out = gpu_step(wl, vals)
+    torch.cuda.synchronize()
+    # position 0 of every sequence is the token the step wrote: value[s]
+    v = vals["value"].float().repeat_interleave(6, dim=1)
+    assert torch.equal(out, v)
+
+
+def test_empty_sequences_give_zero_rows():
+    wl = custom_workload([0, 40, 0, 3], 4, 2, 64, "f16", seed=9)
+    got, want = _run_and_check(wl)
+    assert np.all(got[0] == 0) and np.all(got[2] == 0)
+    assert max_abs(got, want) <= ATOL
+
+
+def test_output_is_bit_reproducible():
+    wl = synthetic.make("gqa")
+    vals = synthetic.make_values(wl, device=DEV)
+    tables = torch.as_tensor(wl.block_tables, device=DEV)
+    lens = torch.as_tensor(wl.context_lens, device=DEV)
+    outs = [pa.decode_attention(vals["q"], vals["k_cache"], vals["v_cache"], tables, lens,
+                                wl.max_context_len, wl.scale) for _ in range(3)]
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+# ---------------------------------------------------------------------------
+# block copy across layers; device-detected errors; host-detected errors
+# ---------------------------------------------------------------------------
+
+def test_copy_blocks_all_layers_bit_exact():
+    import oracle
+    L, NB, Hkv, D = 5, 40, 4, 128
+    g = torch.Generator(device=DEV).manual_seed(3)
+    ks = [torch.randn(NB, Hkv, 16, D, generator=g, device=DEV).half() for _ in range(L)]
+    vs = [torch.randn(NB, Hkv, 16, D, generator=g, device=DEV).half() for _ in range(L)]
+    pairs = np.array([[3, 30], [7, 31], [3, 32], [12, 5], [0, 39]], np.int64)
+    hk = [codes(k) for k in ks]
+    hv = [codes(v) for v in vs]
+    oracle.copy_blocks(hk, hv, pairs)
+    err = _err_word()
+    pa.copy_blocks(ks, vs, torch.as_tensor(pairs, device=DEV), error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for l in range(L):
+        assert np.array_equal(codes(ks[l]), hk[l])
+        assert np.array_equal(codes(vs[l]), hv[l])
+
+
+def test_copy_blocks_out_of_range_pair_is_flagged_and_skipped():
+    NB = 8
+    k = torch.arange(NB * 16 * 64, device=DEV, dtype=torch.float32).half().view(NB, 1, 16, 64)
+    v = k.clone()
+    k0 = k.clone()
+    err = _err_word()
+    pairs = torch.tensor([[1, NB], [-1, 2], [3, 3]], device=DEV, dtype=torch.int64)
+    pa.copy_blocks([k], [v], pairs, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.ERRBIT_BLOCK_OOB
+    assert torch.equal(k, k0)
+
+
+def test_cache_write_out_of_range_slot_is_flagged_and_skipped():
+    NB, Hkv, D = 4, 2, 64
+    kc = torch.zeros(NB, Hkv, 16, D, dtype=torch.float16, device=DEV)
+    vc = kc.clone()
+    key = torch.ones(3, Hkv, D, dtype=torch.float16, device=DEV)
+    slots = torch.tensor([NB * 16, -1, 5], device=DEV, dtype=torch.int64)
+    err = _err_word()
+    pa.cache_write(key, key, kc, vc, slots, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.ERRBIT_SLOT_OOB
+    assert int((kc != 0).sum()) == Hkv * D          # only slot 5 written
+    assert torch.equal(kc[0, :, 5], key[2])
+
+
+def test_bad_table_entry_and_context_len_are_flagged():
+    wl = custom_workload([40, 40, 40], 4, 4, 128, "f16", seed=2)
+    vals = synthetic.make_values(wl, device=DEV)
+    tables = torch.as_tensor(wl.block_tables, device=DEV)
+    tables[1, 1] = wl.num_blocks + 7                   # out of range block id
+    lens = torch.as_tensor(wl.context_lens, device=DEV)
+    lens[2] = 10_000                                   # above max_context_len
+    err = _err_word()
+    out = pa.decode_attention(vals["q"], vals["k_cache"], vals["v_cache"], tables, lens, 40,
+                              wl.scale, error_word=err)
+    torch.cuda.synchronize()
+    e = int(err.item())
+    assert e & pa.ERRBIT_BLOCK_OOB and e & pa.ERRBIT_CONTEXT_LEN
+    assert torch.all(out[2] == 0)
+    assert torch.all(torch.isfinite(out))
+
+
+def test_host_detected_errors():
+    q = torch.zeros(2, 8, 128, dtype=torch.float16, device=DEV)
+    kc = torch.zeros(4, 1, 16, 128, dtype=torch.float16, device=DEV)
+    t = torch.zeros(2, 4, dtype=torch.int32, device=DEV)
+    ln = torch.ones(2, dtype=torch.int32, device=DEV)
+    with pytest.raises(pa.PaError) as ei:              # 8 query heads per KV head is fine;
+        pa.decode_attention(q.view(2, 8, 128).repeat(1, 2, 1), kc, kc, t, ln, 16, 0.1)
+    assert ei.value.status == 2                        # 16 per KV head is not
+    ws = torch.zeros(8, dtype=torch.uint8, device=DEV)
+    with pytest.raises(pa.PaError) as ei:
+        pa.decode_attention(q, kc, kc, t, ln, 16, 0.1, workspace=ws)
+    assert ei.value.status == 4
+    with pytest.raises(pa.PaError) as ei:              # max_context_len beyond the table
+        pa.decode_attention(q, kc, kc, t, ln, 65, 0.1)
+    assert ei.value.status == 1
+    q96 = torch.zeros(2, 1, 96, dtype=torch.float16, device=DEV)
+    k96 = torch.zeros(4, 1, 16, 96, dtype=torch.float16, device=DEV)
+    with pytest.raises(pa.PaError) as ei:
+        pa.decode_attention(q96, k96, k96, t, ln, 16, 0.1)
+    assert ei.value.status == 2
