@@ -165,6 +165,45 @@ pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, const void *que
                                 void *workspace, size_t workspace_bytes,
                                 unsigned int *dev_error_word, pa_stream_t stream);
 
+/* Size of the workspace array built into the library for
+ * pa_decode_attention_noalloc (32 MiB on every GPU that loads the library). */
+#define PA_NOALLOC_WORKSPACE_BYTES (32u << 20)
+
+/*
+ * pa_decode_attention_noalloc -- pa_decode_attention for callers that cannot
+ * allocate device memory.  The paper has no counterpart: this entry point
+ * exists for callers of this library, not for the method.
+ *
+ * Who needs it: code that runs attention where allocation is not allowed or
+ * not reachable -- inside another engine's execution phase (plugins whose
+ * enqueue step must not allocate, because all memory is planned up front),
+ * or from C code whose device allocator belongs to a framework it cannot
+ * call.  Such callers still own query, pools, tables, lengths and out, but
+ * cannot provide a workspace.
+ *
+ * Arguments, results and errors are those of pa_decode_attention, without
+ * the workspace: the workspace is an array of PA_NOALLOC_WORKSPACE_BYTES
+ * built into the library, which every GPU that loads the library keeps until
+ * the process exits.  It calls no allocator (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *   - Sizes whose pa_decode_workspace_size exceeds PA_NOALLOC_WORKSPACE_BYTES
+ *     are rejected with PA_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on each device, made with that device current, looks up
+ *     the array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents; nothing in it needs to start at zero.  Calls that overlap on
+ *     the GPU (e.g. on unordered streams) race on it: order them.
+ */
+pa_status_t pa_decode_attention_noalloc(void *out, pa_dtype_t out_dtype, const void *query,
+                                        const void *k_cache, const void *v_cache,
+                                        const int32_t *block_tables, int max_blocks_per_seq,
+                                        const int32_t *context_lens, int max_context_len,
+                                        int num_seqs, int num_heads, int num_kv_heads,
+                                        int head_dim, int num_blocks, float scale,
+                                        pa_dtype_t dtype, unsigned int *dev_error_word,
+                                        pa_stream_t stream);
+
 /* Upper bound on num_layers accepted by pa_copy_blocks. */
 #define PA_MAX_LAYERS 128
 
