@@ -6,7 +6,7 @@
 One step = one pass of the whole path over the batch: copy-on-write block
 copies (when the workload has shared blocks; the OPT-13B-shaped batch has
 none), the cache write of one new token per sequence, and paged decode
-attention (plan, attention, merge kernels) over every sequence's context.
+attention (plan, attention and merge kernels) over every sequence's context.
 Inputs are synthetic and seeded (paged_kv_cache_pa_gb300.synthetic).
 
 Metric: decode-attention achieved HBM GB/s = algorithmic bytes of the step /
@@ -421,7 +421,7 @@ def main():
                      "peak_kind": f"{peak_kind} HBM copy GB/s", "unit": "GB/s",
                      "frac": round(attn_gbs / peak, 4),
                      "traffic": recorded_traffic(args.config),
-                     "kernel": "pa_decode_attention (plan + attention + merge)",
+                     "kernel": "pa_decode_attention (plan + attention + merge kernels)",
                      "ms_per_call": round(attn_ms, 4), "algorithmic_bytes": int(b_attn)},
         "gpu_launches": int(K * launches_per_step),
         "clocks": clocks,

@@ -152,9 +152,9 @@ int pa_decode_partition_tokens(int num_seqs, int num_kv_heads, int max_context_l
  * dev_error_word  device, may be NULL: PA_ERRBIT_BLOCK_OOB (the block is
  *               skipped), PA_ERRBIT_CONTEXT_LEN (the sequence gets a zero
  *               row), PA_ERRBIT_TIMEOUT
- * Enqueues two to three kernels (plan, attention, merge when some sequence
- * may span more than one partition), chained with programmatic dependent
- * launch.
+ * Enqueues two or three kernels, chained with programmatic dependent launch:
+ * a plan kernel (the work list), the attention kernel, and a merge kernel
+ * when a sequence may span more than one context partition.
  */
 pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, const void *query,
                                 const void *k_cache, const void *v_cache,

@@ -130,7 +130,7 @@ struct Layout {
     static constexpr size_t meta_off = (l_off + (size_t)kNCW * GM * 4 + 15) / 16 * 16;
     static constexpr size_t bar_off = meta_off + (size_t)R * sizeof(StageMeta);  // full[R], empty[R]
     static constexpr size_t cbar_off = bar_off + (size_t)2 * R * 8;  // consumer item barriers [2]
-    static constexpr size_t flag_off = cbar_off + 2 * 8;
+    static constexpr size_t flag_off = cbar_off + 2 * 8;       // abort flag
     static constexpr size_t bytes = flag_off + 16;
 };
 
@@ -138,7 +138,7 @@ struct Layout {
 // 16-token K+V stages as fit the shared-memory share of one CTA.
 template <int D, int GM>
 struct Tuning {
-    static constexpr int kMinBlocks = GM <= 2 ? 3 : 2;
+    static constexpr int kMinBlocks = GM <= 2 ? 4 : 2;
     static constexpr size_t kBudget = 233472 / kMinBlocks - 1024 - 512;
     static constexpr size_t kStage = (size_t)2 * kBlock * D * 2 + (size_t)GM * D * 2 + 32 + 16;
     static constexpr size_t kFixed = (size_t)kNCW * GM * (D + 2) * 4 + 64;
@@ -285,11 +285,12 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &P, const T *sk,
     const int c = lane % LPR, rg = lane / LPR;
     const int G = P.G;
     const int tid = cw * 32 + lane;
-    uint32_t item_par = 0;  // phase parity of the consumer item barriers
+    uint32_t bar_par[2] = {0u, 0u};  // phase parity of the two consumer barriers
     // Bounded barrier over the 128 consumer threads; false if it gave up.
-    auto consumer_sync = [&](uint64_t *bar) -> bool {
-        mbar_arrive(bar);
-        const bool ok = mbar_wait(bar, item_par, abort_flag);
+    auto consumer_sync = [&](int b) -> bool {
+        mbar_arrive(&cbar[b]);
+        const bool ok = mbar_wait(&cbar[b], bar_par[b], abort_flag);
+        bar_par[b] ^= 1u;
         if (__all_sync(0xffffffffu, ok)) return true;
         if (lane == 0) {
             *abort_flag = 1;
@@ -440,7 +441,7 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &P, const T *sk,
                 }
             }
         }
-        if (!consumer_sync(&cbar[0])) return;
+        if (!consumer_sync(0)) return;
         const int H = P.num_heads;
         for (int idx = tid; idx < G * D; idx += kNCW * 32) {
             const int g = idx / D, d = idx - g * D;
@@ -468,8 +469,7 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &P, const T *sk,
                 }
             }
         }
-        if (!consumer_sync(&cbar[1])) return;  // merge buffer free for the next item
-        item_par ^= 1u;
+        if (!consumer_sync(1)) return;  // merge buffers free for the next item
     }
 }
 
@@ -508,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, MINB) paged_decode_kernel(const __gr
                                   abort_flag, warp - 1, lane);
 }
 
+// Merge of the partitions of multi-partition sequences (pa_decode_api.cu).
 // Host-side launcher for one head_dim (defined in pa_decode_d{64,128,256}.cu).
 pa_status_t launch_decode_d64(const DecodeParams &P, pa_dtype_t dtype, int grid_cap,
                               cudaStream_t stream);

@@ -1,10 +1,11 @@
-// pa_decode_api.cu -- pa_decode_attention / pa_decode_workspace_size: the plan
-// kernel, the partition merge kernel and the host-side checks and launches.
+// pa_decode_api.cu -- pa_decode_attention / pa_decode_workspace_size /
+// pa_decode_partition_tokens: the plan kernel, the partition merge kernel and
+// the host-side checks and launches.
 //
 // Context split: a sequence longer than part_tokens is cut into partitions of
 // part_tokens tokens; every (sequence, partition, KV head) is an independent
 // work item whose partial softmax state (max m, sum l, weighted values acc)
-// is merged exactly afterwards:
+// is merged exactly afterwards by the merge kernel:
 //     M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  o = sum_p acc_p 2^(m_p - M) / L
 // [vLLM Internals ..., "The kernel pays for the indirection": a grid axis over
 // partitions; Paged Attention: Managing the KV Cache Like Virtual Memory,
@@ -17,6 +18,7 @@
 #include <climits>
 
 #include "pa_decode.cuh"
+#include "pa_launch.cuh"
 
 namespace pa {
 
@@ -75,6 +77,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ 
                                                     int4 *__restrict__ items, WsHeader *hdr,
                                                     void *out, int out_dtype, unsigned int *err) {
     pdl_trigger();  // the attention CTAs may start their set-up now
+    pdl_wait();     // inputs written by earlier work on the stream are ready
     __shared__ int hist[kMaxPartTokens / kBlock + 1];
     __shared__ int offs[kMaxPartTokens / kBlock + 1];
     const int PB = part_tokens / kBlock;
@@ -246,10 +249,10 @@ extern "C" pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, cons
     P.err = dev_error_word;
     cudaStream_t st = (cudaStream_t)stream;
 
-    plan_kernel<<<1, 1024, 0, st>>>(context_lens, num_seqs, max_context_len, w.part_tokens,
-                                    num_kv_heads, num_heads, head_dim, P.items, P.hdr, out,
-                                    (int)out_dtype, dev_error_word);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, (const int32_t *)context_lens,
+                   num_seqs, max_context_len, w.part_tokens, num_kv_heads, num_heads, head_dim,
+                   P.items, P.hdr, out, (int)out_dtype, dev_error_word) != cudaSuccess)
+        return PA_ERR_CUDA;
 
     long long cap = (long long)num_seqs * w.max_parts * num_kv_heads;
     if (cap > INT_MAX) cap = INT_MAX;
@@ -262,23 +265,17 @@ extern "C" pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, cons
         st_launch = launch_decode_d256(P, dtype, (int)cap, st);
     if (st_launch != PA_OK) return st_launch;
 
+    if (st_launch != PA_OK) return st_launch;
+
     if (w.max_parts > 1) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)num_seqs, (unsigned)((num_heads + 3) / 4));
-        cfg.blockDim = dim3(128);
-        cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        const dim3 grid((unsigned)num_seqs, (unsigned)((num_heads + 3) / 4));
         cudaError_t e;
         if (head_dim == 64)
-            e = cudaLaunchKernelEx(&cfg, merge_kernel<64>, P);
+            e = launch_pdl(merge_kernel<64>, grid, dim3(128), 0, st, P);
         else if (head_dim == 128)
-            e = cudaLaunchKernelEx(&cfg, merge_kernel<128>, P);
+            e = launch_pdl(merge_kernel<128>, grid, dim3(128), 0, st, P);
         else
-            e = cudaLaunchKernelEx(&cfg, merge_kernel<256>, P);
+            e = launch_pdl(merge_kernel<256>, grid, dim3(128), 0, st, P);
         if (e != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;

@@ -7,6 +7,7 @@
 #include <atomic>
 
 #include "pa_decode.cuh"
+#include "pa_launch.cuh"
 
 namespace pa {
 
@@ -37,17 +38,8 @@ pa_status_t launch_one(const DecodeParams &P, int grid_cap, cudaStream_t stream)
     if (grid > grid_cap) grid = grid_cap;
     if (grid < 1) grid = 1;
 
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = L::bytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, P) != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), L::bytes, stream, P) != cudaSuccess)
+        return PA_ERR_CUDA;
     return PA_OK;
 }
 

@@ -1,8 +1,9 @@
 // pa_small_ops.cu -- pa_cache_write, pa_copy_blocks, pa_status_string.
 //
 // Both kernels move bytes unchanged with 16-byte vector loads and stores:
-//   - cache write: one CTA per new token; the token's Hkv rows of K and of V
-//     (Hkv * head_dim * 2 bytes each) go to block slot/16, offset slot%16
+//   - cache write: a grid over (new token, 16-byte chunk group); the token's
+//     Hkv rows of K and of V (Hkv * head_dim * 2 bytes each) go to block
+//     slot/16, offset slot%16
 //     [Efficient Memory Management for Large Language Model Serving with
 //     PagedAttention, "Kernel-Level Optimizations", 1. fused reshape and
 //     block write].
@@ -14,33 +15,41 @@
 #include <cstdint>
 
 #include "pa.h"
+#include "pa_launch.cuh"
+#include "pa_ptx.cuh"
 
 namespace {
 
 constexpr int kBlock = PA_BLOCK_SIZE;
 
-__global__ void __launch_bounds__(128) cache_write_kernel(
+constexpr int kWriteThreads = 256;
+
+// grid (token, chunk group): every thread moves one 16-byte chunk of the
+// token's K rows and the same chunk of its V rows.
+__global__ void __launch_bounds__(kWriteThreads) cache_write_kernel(
     const uint4 *__restrict__ key, const uint4 *__restrict__ value, uint4 *__restrict__ k_cache,
     uint4 *__restrict__ v_cache, const int64_t *__restrict__ slot_mapping, long long num_slots,
     int num_kv_heads, int chunks_per_row, unsigned int *err) {
+    pa::pdl_trigger();
+    pa::pdl_wait();  // earlier kernels on the stream may still read or write the pools
     const int t = blockIdx.x;
+    const int i = blockIdx.y * kWriteThreads + threadIdx.x;
+    const int total = num_kv_heads * chunks_per_row;
     const int64_t slot = slot_mapping[t];
     if (slot < 0) return;                                  // padding token
     if (slot >= num_slots) {
-        if (threadIdx.x == 0 && err) atomicOr(err, PA_ERRBIT_SLOT_OOB);
+        if (i == 0 && err) atomicOr(err, PA_ERRBIT_SLOT_OOB);
         return;
     }
+    if (i >= total) return;
     const int64_t blk = slot / kBlock, off = slot % kBlock;
-    const int total = num_kv_heads * chunks_per_row;
-    const size_t src_base = (size_t)t * total;
-    for (int i = threadIdx.x; i < total; i += blockDim.x) {
-        const int h = i / chunks_per_row, c = i - h * chunks_per_row;
-        const size_t dst = (((size_t)blk * num_kv_heads + h) * kBlock + off) * chunks_per_row + c;
-        const uint4 kv = __ldg(key + src_base + i);
-        const uint4 vv = __ldg(value + src_base + i);
-        k_cache[dst] = kv;
-        v_cache[dst] = vv;
-    }
+    const int h = i / chunks_per_row, c = i - h * chunks_per_row;
+    const size_t src = (size_t)t * total + i;
+    const size_t dst = (((size_t)blk * num_kv_heads + h) * kBlock + off) * chunks_per_row + c;
+    const uint4 kv = __ldcs(key + src);
+    const uint4 vv = __ldcs(value + src);
+    k_cache[dst] = kv;
+    v_cache[dst] = vv;
 }
 
 struct LayerPools {
@@ -54,6 +63,8 @@ constexpr int kCopyUnroll = 4;
 __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
     const LayerPools pools, const int64_t *__restrict__ pairs, int num_blocks,
     long long chunks_per_block, long long chunks_per_cta, unsigned int *err) {
+    pa::pdl_trigger();
+    pa::pdl_wait();  // earlier kernels on the stream may still read or write the pools
     const int pair = blockIdx.x;
     const int layer = blockIdx.y >> 1;
     const int which = blockIdx.y & 1;
@@ -100,11 +111,14 @@ extern "C" pa_status_t pa_cache_write(const void *key, const void *value, void *
     if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_INVALID_ARG;
     const int chunks_per_row = head_dim * 2 / 16;
-    cache_write_kernel<<<num_tokens, 128, 0, (cudaStream_t)stream>>>(
-        (const uint4 *)key, (const uint4 *)value, (uint4 *)k_cache, (uint4 *)v_cache,
-        slot_mapping, (long long)num_blocks * kBlock, num_kv_heads, chunks_per_row,
-        dev_error_word);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    const int groups = (num_kv_heads * chunks_per_row + kWriteThreads - 1) / kWriteThreads;
+    if (groups > 65535) return PA_ERR_UNSUPPORTED;
+    const cudaError_t e = pa::launch_pdl(
+        cache_write_kernel, dim3((unsigned)num_tokens, (unsigned)groups), dim3(kWriteThreads), 0,
+        (cudaStream_t)stream, (const uint4 *)key, (const uint4 *)value, (uint4 *)k_cache,
+        (uint4 *)v_cache, slot_mapping, (long long)num_blocks * kBlock, num_kv_heads,
+        chunks_per_row, dev_error_word);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 extern "C" pa_status_t pa_copy_blocks(void *const *k_caches, void *const *v_caches,
@@ -130,11 +144,13 @@ extern "C" pa_status_t pa_copy_blocks(void *const *k_caches, void *const *v_cach
     // about 32 KiB per CTA: enough bytes in flight per CTA, enough CTAs per copy
     const long long chunks_per_cta = 2048;
     const long long splits = (chunks_per_block + chunks_per_cta - 1) / chunks_per_cta;
-    if (num_pairs > 2147483647 || splits > 65535) return PA_ERR_UNSUPPORTED;
-    dim3 grid((unsigned)num_pairs, (unsigned)(2 * num_layers), (unsigned)splits);
-    copy_blocks_kernel<<<grid, kCopyThreads, 0, (cudaStream_t)stream>>>(
-        pools, block_pairs, num_blocks, chunks_per_block, chunks_per_cta, dev_error_word);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    if (splits > 65535) return PA_ERR_UNSUPPORTED;
+    const dim3 grid((unsigned)num_pairs, (unsigned)(2 * num_layers), (unsigned)splits);
+    const cudaError_t e =
+        pa::launch_pdl(copy_blocks_kernel, grid, dim3(kCopyThreads), 0, (cudaStream_t)stream,
+                       pools, block_pairs, num_blocks, chunks_per_block, chunks_per_cta,
+                       dev_error_word);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 extern "C" const char *pa_status_string(pa_status_t s) {
