@@ -48,6 +48,17 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and sequences/sec per layer"
+WORKLOADS = {
+    "opt13b": "opt13b-shaped decode step: S=256, H=Hkv=40, D=128, fp16, block 16, lognormal "
+              "prompt 220 + output 204, <=2048 tokens, scattered blocks, one layer",
+    "gqa": "Qwen2.5-1.5B-shaped GQA decode step: S=64, H=12, Hkv=2, D=128, bf16, block 16, "
+           "lengths U[512,4096], scattered blocks, one layer",
+    "long": "long-context decode step: S=8, H=Hkv=40, D=128, fp16, block 16, lengths "
+            "U[16384,32768], blocks drawn from a 60 GiB pool, one layer",
+    "beams": "shared-prefix beam step: 32 prompts x 6 beams, H=Hkv=40, D=128, fp16, 512-token "
+             "shared prompt, copy-on-write copies + cache write + attention, one layer",
+    "tiny": "tiny decode step: S=4, H=Hkv=8, D=64, fp16, lengths U[1,128], 64-block pool",
+}
 UNIT = "GB/s"
 
 
@@ -405,14 +416,14 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic",
-        "config": {"workload": "opt13b-shaped decode step: S=256, H=Hkv=40, D=128, fp16, "
-                               "block 16, lognormal prompt 220 + output 204, <=2048 tokens, "
-                               "scattered blocks, one layer",
+        "config": {"workload": WORKLOADS.get(args.config, args.config) +
+                               (f" (cut to {S} sequences)" if args.seqs else ""),
                    "mean_context": round(float(wl.context_lens.mean()), 1),
                    "kv_bytes_per_step": int(wl.kv_bytes()),
-                   "l2": "inputs larger than L2 (K/V read per step >> 126 MB L2)",
+                   "l2": ("inputs larger than L2 (K/V read per step >> 126 MB L2)"
+                          if wl.kv_bytes() > (256 << 20) else "K/V per step near or below L2 size"),
                    "parallelism": f"replicas x{world}"},
         "seqs_per_s_per_layer": round(world * S / (ms_per_step * 1e-3), 1),
         "pct_of_peak": {"measured_copy": round(100 * value / world / peak, 2),

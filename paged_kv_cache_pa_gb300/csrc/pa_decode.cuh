@@ -34,6 +34,7 @@
 // exponentials are single ex2 instructions.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -63,6 +64,9 @@ struct WsHeader {
 };
 
 struct DecodeParams {
+    // Tensor maps of the query and the pools (tensor-core kernel only):
+    // 2-D views [rows][head_dim], 64-element boxes, 128-byte swizzle.
+    CUtensorMap tmap_q, tmap_k, tmap_v;
     void *out;
     int out_dtype;  // PA_F16, PA_BF16 or PA_F32
     const void *q;
@@ -508,7 +512,10 @@ __global__ void __launch_bounds__(kThreads, MINB) paged_decode_kernel(const __gr
                                   abort_flag, warp - 1, lane);
 }
 
-// Merge of the partitions of multi-partition sequences (pa_decode_api.cu).
+// Query groups of 2..8 heads with head_dim <= 128 run on the tensor cores
+// (pa_decode_mma.cuh); single-head groups and head_dim 256 on the CUDA cores.
+inline bool uses_tensor_cores(int G, int head_dim) { return G >= 2 && head_dim <= 128; }
+
 // Host-side launcher for one head_dim (defined in pa_decode_d{64,128,256}.cu).
 pa_status_t launch_decode_d64(const DecodeParams &P, pa_dtype_t dtype, int grid_cap,
                               cudaStream_t stream);

@@ -16,6 +16,7 @@
 
 #include <atomic>
 #include <climits>
+#include <cstring>
 
 #include "pa_decode.cuh"
 #include "pa_launch.cuh"
@@ -161,6 +162,46 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Deco
 
 std::atomic<int> g_sm_count[64];
 
+// cuTensorMapEncodeTiled, looked up once through the runtime's driver entry
+// point (no link against the driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tensor_map_encoder() {
+    static std::atomic<void *> fn{nullptr};
+    void *f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !f)
+            return nullptr;
+        fn.store(f, std::memory_order_release);
+    }
+    return reinterpret_cast<EncodeTiledFn>(f);
+}
+
+// 2-D view [rows][head_dim] of a row-major 16-bit tensor; boxes of 64
+// elements x box_rows rows with the 128-byte swizzle; reads past the last
+// row return zeros.
+bool encode_rows(CUtensorMap *map, const void *base, pa_dtype_t dtype, unsigned long long rows,
+                 int head_dim, int box_rows) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    const cuuint32_t elem_strides[2] = {1u, 1u};
+    return enc(map,
+               dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+               2, const_cast<void *>(base), dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
@@ -223,6 +264,16 @@ extern "C" pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, cons
 
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     DecodeParams P;
+    memset(&P, 0, sizeof(P));
+    if (uses_tensor_cores(num_heads / num_kv_heads, head_dim)) {
+        const unsigned long long pool_rows =
+            (unsigned long long)num_blocks * num_kv_heads * PA_BLOCK_SIZE;
+        if (!encode_rows(&P.tmap_q, query, dtype, (unsigned long long)num_seqs * num_heads,
+                         head_dim, 8) ||
+            !encode_rows(&P.tmap_k, k_cache, dtype, pool_rows, head_dim, PA_BLOCK_SIZE) ||
+            !encode_rows(&P.tmap_v, v_cache, dtype, pool_rows, head_dim, PA_BLOCK_SIZE))
+            return PA_ERR_CUDA;
+    }
     P.out = out;
     P.out_dtype = (int)out_dtype;
     P.q = query;

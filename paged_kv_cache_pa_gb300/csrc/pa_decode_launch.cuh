@@ -7,6 +7,7 @@
 #include <atomic>
 
 #include "pa_decode.cuh"
+#include "pa_decode_mma.cuh"
 #include "pa_launch.cuh"
 
 namespace pa {
@@ -44,13 +45,47 @@ pa_status_t launch_one(const DecodeParams &P, int grid_cap, cudaStream_t stream)
 }
 
 template <int D, typename T>
+pa_status_t launch_one_mma(const DecodeParams &P, int grid_cap, cudaStream_t stream) {
+    using Tn = TuningMma<D>;
+    constexpr int R = Tn::kStages;
+    constexpr int MINB = Tn::kMinBlocks;
+    using L = LayoutMma<D, R>;
+    auto kern = paged_decode_mma_kernel<D, T, R, MINB>;
+    static std::atomic<int> occ_cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+    int occ = occ_cache[dev].load(std::memory_order_relaxed);
+    if (occ == 0) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)L::bytes) != cudaSuccess)
+            return PA_ERR_CUDA;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, L::bytes) !=
+            cudaSuccess)
+            return PA_ERR_CUDA;
+        if (occ < 1) return PA_ERR_UNSUPPORTED;
+        occ_cache[dev].store(occ, std::memory_order_relaxed);
+    }
+    long long grid = (long long)current_sm_count() * occ;
+    if (grid > grid_cap) grid = grid_cap;
+    if (grid < 1) grid = 1;
+    if (launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), L::bytes, stream, P) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+template <int D, typename T>
 pa_status_t dispatch_group(const DecodeParams &P, int grid_cap, cudaStream_t stream) {
     const int G = P.G;
-    if (G == 1) return launch_one<D, 1, T>(P, grid_cap, stream);
-    if (G == 2) return launch_one<D, 2, T>(P, grid_cap, stream);
-    if (G <= 4) return launch_one<D, 4, T>(P, grid_cap, stream);
-    if (G <= 6) return launch_one<D, 6, T>(P, grid_cap, stream);
-    if (G <= 8) return launch_one<D, 8, T>(P, grid_cap, stream);
+    if constexpr (D <= 128) {
+        if (G == 1) return launch_one<D, 1, T>(P, grid_cap, stream);
+        if (G <= 8) return launch_one_mma<D, T>(P, grid_cap, stream);
+    } else {
+        if (G == 1) return launch_one<D, 1, T>(P, grid_cap, stream);
+        if (G == 2) return launch_one<D, 2, T>(P, grid_cap, stream);
+        if (G <= 4) return launch_one<D, 4, T>(P, grid_cap, stream);
+        if (G <= 6) return launch_one<D, 6, T>(P, grid_cap, stream);
+        if (G <= 8) return launch_one<D, 8, T>(P, grid_cap, stream);
+    }
     return PA_ERR_UNSUPPORTED;
 }
 

@@ -1,0 +1,476 @@
+// pa_decode_mma.cuh -- paged decode attention on the tensor cores, for query
+// groups of 2..8 heads per KV head (grouped-query attention), head_dim 64 or
+// 128.
+//
+// With G query heads sharing a KV head, each 16-token block is a small dense
+// contraction: S = Q K^T is [G x D] x [D x 16] and O += P V is
+// [G x 16] x [16 x D].  Both run as m16n8k16 MMAs (fp16 or bf16 operands,
+// fp32 accumulation) with the G query rows padded to 16
+// [Paged Attention: Managing the KV Cache Like Virtual Memory, "Attention
+// over scattered blocks": the query heads that share a KV head all use each
+// K/V read; Efficient Memory Management for Large Language Model Serving with
+// PagedAttention, "PagedAttention Algorithm": block-wise attention].
+//
+// Data movement: the producer warp fetches up to four blocks per stage (one
+// per consumer warp) with 2-D tiled bulk copies (TMA) through tensor maps of
+// the pools viewed as [blocks * KV heads * 16 rows][head_dim], 64-element
+// boxes with the 128-byte swizzle, so the ldmatrix reads of the consumers are
+// free of bank conflicts.  The item's query rows (8-row box) ride with its
+// first stage.  A block's box always has 16 rows; rows past the sequence's
+// length are masked out of the scores and zeroed in the V tile before P V,
+// so stale or poisoned data never reaches the output.
+//
+// Precision: P is rounded to the operand type in two parts, P = P_hi + P_lo,
+// and both are multiplied with V, so the weights carry ~16 significant bits
+// (bf16 alone would carry 8).  Scores, the running softmax and the output
+// accumulate in fp32.
+#pragma once
+
+#include "pa_decode.cuh"
+
+namespace pa {
+
+constexpr int kBPS = kNCW;            // blocks per stage: one per consumer warp
+constexpr size_t kBoxBytes = 16 * 128;  // one block's 64-element box: 16 rows x 128 B
+constexpr size_t kQBoxBytes = 8 * 128;  // the query box: 8 rows x 128 B
+
+template <int D, int R>
+struct LayoutMma {
+    static constexpr int kBoxes = D / 64;
+    static constexpr size_t k_off = 0;  // [R][BPS][boxes] boxes, 1 KiB aligned
+    static constexpr size_t v_off = k_off + (size_t)R * kBPS * kBoxes * kBoxBytes;
+    static constexpr size_t q_off = v_off + (size_t)R * kBPS * kBoxes * kBoxBytes;
+    static constexpr size_t acc_off = q_off + (size_t)R * kBoxes * kQBoxBytes;  // f32 [NCW][8][D]
+    static constexpr size_t m_off = acc_off + (size_t)kNCW * 8 * D * 4;
+    static constexpr size_t l_off = m_off + (size_t)kNCW * 8 * 4;
+    static constexpr size_t meta_off = (l_off + (size_t)kNCW * 8 * 4 + 15) / 16 * 16;
+    static constexpr size_t bar_off = meta_off + (size_t)R * sizeof(StageMeta);
+    static constexpr size_t cbar_off = bar_off + (size_t)2 * R * 8;
+    static constexpr size_t flag_off = cbar_off + 2 * 8;
+    static constexpr size_t used = flag_off + 16;
+    static constexpr size_t bytes = used + 1024;  // slack to align the base to 1 KiB
+};
+
+template <int D>
+struct TuningMma {
+    static constexpr int kMinBlocks = 2;
+    static constexpr size_t kBudget = 233472 / kMinBlocks - 1024 - 512;
+    static constexpr size_t kStage =
+        (size_t)2 * kBPS * (D / 64) * kBoxBytes + (D / 64) * kQBoxBytes + 32 + 16;
+    static constexpr size_t kFixed = (size_t)kNCW * 8 * (D + 2) * 4 + 64 + 1024;
+    static constexpr int kRaw = (int)((kBudget - kFixed) / kStage);
+    static constexpr int kStages = kRaw > 8 ? 8 : kRaw;
+    static_assert(kStages >= 2, "ring too shallow");
+};
+
+template <typename T>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1);
+template <>
+__device__ __forceinline__ void mma16816<__half>(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                 uint32_t a2, uint32_t a3, uint32_t b0,
+                                                 uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                        uint32_t a2, uint32_t a3, uint32_t b0,
+                                                        uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// (lo, hi) fp32 -> packed pair of T (lo in the low half); also returns the
+// rounding residuals.
+template <typename T>
+__device__ __forceinline__ uint32_t pack_split(float lo, float hi, float &rlo, float &rhi);
+template <>
+__device__ __forceinline__ uint32_t pack_split<__half>(float lo, float hi, float &rlo, float &rhi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    const float2 b = __half22float2(h);
+    rlo = lo - b.x;
+    rhi = hi - b.y;
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack_split<__nv_bfloat16>(float lo, float hi, float &rlo,
+                                                              float &rhi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    const float2 b = __bfloat1622float2(h);
+    rlo = lo - b.x;
+    rhi = hi - b.y;
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Byte offset of 16-byte chunk `chunk` (of the full head_dim row) of row
+// `row` inside a block's [boxes] of 128-byte-swizzled rows.
+__device__ __forceinline__ uint32_t swz(int chunk, int row, size_t box_bytes) {
+    return (uint32_t)((chunk >> 3) * box_bytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+// ---------------------------------------------------------------------------
+// producer warp: same item pipeline as the CUDA-core kernel, four blocks per
+// stage, tiled TMA
+// ---------------------------------------------------------------------------
+template <int D, typename T, int R>
+__device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned char *sk,
+                                                 unsigned char *sv, unsigned char *sq,
+                                                 StageMeta *meta, uint64_t *full, uint64_t *empty,
+                                                 volatile int *abort_flag, int lane) {
+    constexpr int KB = D / 64;
+    if (lane == 0) {
+        prefetch_tmap(&P.tmap_k);
+        prefetch_tmap(&P.tmap_v);
+        prefetch_tmap(&P.tmap_q);
+    }
+    pdl_wait();  // the plan kernel's items and counter are ready
+    const unsigned n_items = P.hdr->n_items;
+    const unsigned Hkv = (unsigned)P.num_kv_heads;
+    const int G = P.G;
+    const int PB = P.part_tokens / kBlock;
+    const uint64_t policy = l2_evict_first_policy();
+
+    auto claim = [&]() -> unsigned { return lane == 0 ? atomicAdd(&P.hdr->counter, 1u) : 0u; };
+    auto bcast = [&](unsigned v) -> unsigned { return __shfl_sync(0xffffffffu, v, 0); };
+    auto load_entry = [&](unsigned c) -> int4 {
+        return c < n_items ? P.items[c / Hkv] : make_int4(0, 0, 0, 0);
+    };
+    auto load_tab = [&](unsigned c, int4 e) -> int {
+        const int nblk = (e.z + kBlock - 1) / kBlock;
+        if (c < n_items && lane < nblk)
+            return __ldg(&P.block_tables[(size_t)e.x * P.max_blocks_per_seq + (size_t)e.y * PB +
+                                         lane]);
+        return -1;
+    };
+
+    unsigned cA = bcast(claim());
+    int4 eA = load_entry(cA);
+    int tA = load_tab(cA, eA);
+    unsigned cB = bcast(claim());
+    int4 eB = load_entry(cB);
+    unsigned raw = claim();
+
+    uint32_t k = 0;
+    bool aborted = false;
+    while (cA < n_items) {
+        const int tB = load_tab(cB, eB);
+        const unsigned cC = bcast(raw);
+        const int4 eC = load_entry(cC);
+        raw = claim();
+
+        const int s = eA.x, part = eA.y, ntok = eA.z, nparts = eA.w;
+        const int hk = (int)(cA % Hkv);
+        const int nblk = (ntok + kBlock - 1) / kBlock;
+        const int nst = (nblk + kBPS - 1) / kBPS;
+        for (int st = 0; st < nst; ++st, ++k) {
+            const int slot = (int)(k % R);
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(&empty[slot], ((k / R) & 1u) ^ 1u, abort_flag);
+            if (!__shfl_sync(0xffffffffu, (int)ok, 0)) {
+                aborted = true;
+                break;
+            }
+            const int j0 = st * kBPS;
+            int phys[kBPS];
+#pragma unroll
+            for (int b = 0; b < kBPS; ++b) phys[b] = __shfl_sync(0xffffffffu, tA, min(j0 + b, 31));
+            if (lane == 0) {
+                const int nb = min(kBPS, nblk - j0);
+                unsigned bad = 0;
+                uint32_t bytes = st == 0 ? (uint32_t)(KB * kQBoxBytes) : 0u;
+#pragma unroll
+                for (int b = 0; b < kBPS; ++b) {
+                    if (b >= nb) continue;
+                    if (phys[b] < 0 || phys[b] >= P.num_blocks) {
+                        if (P.err) atomicOr(P.err, PA_ERRBIT_BLOCK_OOB);
+                        bad |= 1u << b;  // skip the block
+                    } else {
+                        bytes += (uint32_t)(2 * KB * kBoxBytes);
+                    }
+                }
+                StageMeta m;
+                m.s = s; m.hk = hk; m.p = part; m.nparts = nparts;
+                m.j = st; m.nblk = nst; m.nvalid = ntok - j0 * kBlock; m.flags = (int)(bad << 8);
+                meta[slot] = m;
+                mbar_arrive_expect_tx(&full[slot], bytes);
+#pragma unroll
+                for (int b = 0; b < kBPS; ++b) {
+                    if (b >= nb || (bad >> b) & 1u) continue;
+                    const int y = (phys[b] * P.num_kv_heads + hk) * kBlock;
+#pragma unroll
+                    for (int h = 0; h < KB; ++h) {
+                        const size_t off = ((size_t)(slot * kBPS + b) * KB + h) * kBoxBytes;
+                        tma_load_2d(sk + off, &P.tmap_k, h * 64, y, &full[slot], policy);
+                        tma_load_2d(sv + off, &P.tmap_v, h * 64, y, &full[slot], policy);
+                    }
+                }
+                if (st == 0) {
+#pragma unroll
+                    for (int h = 0; h < KB; ++h)
+                        tma_load_2d(sq + ((size_t)slot * KB + h) * kQBoxBytes, &P.tmap_q, h * 64,
+                                    s * P.num_heads + hk * G, &full[slot], policy);
+                }
+            }
+            __syncwarp();
+        }
+        if (aborted) break;
+        cA = cB; eA = eB; tA = tB;
+        cB = cC; eB = eC;
+    }
+    if (!aborted) {
+        const int slot = (int)(k % R);
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&empty[slot], ((k / R) & 1u) ^ 1u, abort_flag);
+        if (__shfl_sync(0xffffffffu, (int)ok, 0)) {
+            if (lane == 0) {
+                StageMeta m = {};
+                m.flags = kEndFlag;
+                meta[slot] = m;
+                mbar_arrive(&full[slot]);
+            }
+        } else {
+            aborted = true;
+        }
+    }
+    if (aborted) {
+        if (lane == 0) {
+            *abort_flag = 1;
+            if (P.err) atomicOr(P.err, PA_ERRBIT_TIMEOUT);
+            volatile int never = 0;
+            const uint32_t first = k > (uint32_t)R ? k - R : 0u;
+            for (uint32_t kk = first; kk < k; ++kk) mbar_wait(&full[kk % R], (kk / R) & 1u, &never);
+        }
+        __syncwarp();
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------
+// consumer warps: warp w takes block w of every stage
+// ---------------------------------------------------------------------------
+template <int D, typename T, int R>
+__device__ __forceinline__ void run_consumer_mma(const DecodeParams &P, unsigned char *sk,
+                                                 unsigned char *sv, const unsigned char *sq,
+                                                 const StageMeta *meta, uint64_t *full,
+                                                 uint64_t *empty, uint64_t *cbar, float *s_acc,
+                                                 float *s_m, float *s_l,
+                                                 volatile int *abort_flag, int cw, int lane) {
+    constexpr int KB = D / 64;
+    constexpr int NK = D / 16;  // k-steps of Q K^T
+    constexpr int NT = D / 8;   // n-tiles of P V
+    const int g = lane >> 2, t = lane & 3;
+    const int G = P.G;
+    const int tid = cw * 32 + lane;
+    const float sc = P.scale_log2;
+
+    uint32_t bar_par[2] = {0u, 0u};
+    auto consumer_sync = [&](int b) -> bool {
+        mbar_arrive(&cbar[b]);
+        const bool ok = mbar_wait(&cbar[b], bar_par[b], abort_flag);
+        bar_par[b] ^= 1u;
+        if (__all_sync(0xffffffffu, ok)) return true;
+        if (lane == 0) {
+            *abort_flag = 1;
+            if (P.err) atomicOr(P.err, PA_ERRBIT_TIMEOUT);
+        }
+        return false;
+    };
+
+    uint32_t qa[NK][2];
+    float o[NT][4];
+    float m_run = -INFINITY, l_run = 0.f;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < NK; ++kk) qa[kk][0] = qa[kk][1] = 0u;
+
+    for (uint32_t k = 0;; ++k) {
+        const int slot = (int)(k % R);
+        const bool okw = mbar_wait(&full[slot], (k / R) & 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, okw)) {
+            if (lane == 0) {
+                *abort_flag = 1;
+                if (P.err) atomicOr(P.err, PA_ERRBIT_TIMEOUT);
+            }
+            return;
+        }
+        const StageMeta mt = meta[slot];
+        if (mt.flags & kEndFlag) return;
+
+        if (mt.j == 0) {  // new item: query fragments (rows 0..7; rows 8..15 are zero)
+            const uint32_t qbase = smem_u32(sq + (size_t)slot * KB * kQBoxBytes);
+#pragma unroll
+            for (int kk = 0; kk < NK; kk += 2) {
+                const int r = lane & 7, chunk = 2 * kk + (lane >> 3);
+                ldsm_x4(qa[kk][0], qa[kk][1], qa[kk + 1][0], qa[kk + 1][1],
+                        qbase + swz(chunk, r, kQBoxBytes));
+            }
+            m_run = -INFINITY;
+            l_run = 0.f;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        }
+
+        const int vb = min(kBlock, max(0, mt.nvalid - cw * kBlock));  // my block's tokens
+        const bool mine = vb > 0 && !(((unsigned)mt.flags >> (8 + cw)) & 1u);
+        if (mine) {
+            unsigned char *kt = sk + (size_t)(slot * kBPS + cw) * KB * kBoxBytes;
+            unsigned char *vt = sv + (size_t)(slot * kBPS + cw) * KB * kBoxBytes;
+            if (vb < kBlock) {  // zero the V rows past the sequence's end
+                for (int i = lane; i < (kBlock - vb) * KB * 8; i += 32) {
+                    const int row = vb + i / (KB * 8), rest = i % (KB * 8);
+                    *reinterpret_cast<uint4 *>(vt + (rest >> 3) * kBoxBytes + row * 128 +
+                                               (rest & 7) * 16) = make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+            const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+            // S = Q K^T for the block's 16 tokens (two n-tiles of 8)
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < NK; ++kk) {
+                const int mi = lane >> 3;
+                const int tok = 8 * (mi >> 1) + (lane & 7), chunk = 2 * kk + (mi & 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(b0, b1, b2, b3, kbase + swz(chunk, tok, kBoxBytes));
+                mma16816<T>(s0, qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+                mma16816<T>(s1, qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+            }
+            // running softmax for row g (query head g); the quad t = 0..3 shares it
+            float x[4] = {s0[0] * sc, s0[1] * sc, s1[0] * sc, s1[1] * sc};
+            if (2 * t >= vb) x[0] = -INFINITY;
+            if (2 * t + 1 >= vb) x[1] = -INFINITY;
+            if (8 + 2 * t >= vb) x[2] = -INFINITY;
+            if (9 + 2 * t >= vb) x[3] = -INFINITY;
+            float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float mnew = fmaxf(m_run, mx);
+            const float ms = mnew == -INFINITY ? 0.f : mnew;
+            const float alpha = ex2(m_run - ms);
+            float p[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) p[i] = ex2(x[i] - ms);
+            l_run = l_run * alpha + (p[0] + p[1]) + (p[2] + p[3]);
+            m_run = mnew;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                o[n][0] *= alpha;
+                o[n][1] *= alpha;
+            }
+            // O += P V with P = P_hi + P_lo (rows 8..15 of P are zero)
+            float r0, r1, r2, r3;
+            const uint32_t ph01 = pack_split<T>(p[0], p[1], r0, r1);
+            const uint32_t ph23 = pack_split<T>(p[2], p[3], r2, r3);
+            float d0, d1, d2, d3;
+            const uint32_t pl01 = pack_split<T>(r0, r1, d0, d1);
+            const uint32_t pl23 = pack_split<T>(r2, r3, d2, d3);
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+                const int mi = lane >> 3;
+                const int tok = 8 * (mi & 1) + (lane & 7), chunk = 2 * np + (mi >> 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_trans(b0, b1, b2, b3, vbase + swz(chunk, tok, kBoxBytes));
+                mma16816<T>(o[2 * np], ph01, 0u, ph23, 0u, b0, b1);
+                mma16816<T>(o[2 * np], pl01, 0u, pl23, 0u, b0, b1);
+                mma16816<T>(o[2 * np + 1], ph01, 0u, ph23, 0u, b2, b3);
+                mma16816<T>(o[2 * np + 1], pl01, 0u, pl23, 0u, b2, b3);
+            }
+            if (vb < kBlock) fence_proxy_async_smem();  // zeroed rows before the next TMA here
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);  // stage consumed by this warp
+
+        if (mt.j != mt.nblk - 1) continue;
+
+        // ---- item complete: warp state -> shared memory, then merge warps ----
+        float lq = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
+        lq += __shfl_xor_sync(0xffffffffu, lq, 2);
+        if (g < G) {
+            float *dst = s_acc + ((size_t)cw * 8 + g) * D + 2 * t;
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+                *reinterpret_cast<float2 *>(dst + 8 * n) = make_float2(o[n][0], o[n][1]);
+            if (t == 0) {
+                s_m[cw * 8 + g] = m_run;
+                s_l[cw * 8 + g] = lq;
+            }
+        }
+        if (!consumer_sync(0)) return;
+        const int H = P.num_heads;
+        for (int idx = tid; idx < G * D; idx += kNCW * 32) {
+            const int gg = idx / D, d = idx - gg * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kNCW; ++w) M = fmaxf(M, s_m[w * 8 + gg]);
+            const float Ms = M == -INFINITY ? 0.f : M;
+            float Lsum = 0.f, ov = 0.f;
+#pragma unroll
+            for (int w = 0; w < kNCW; ++w) {
+                const float cf = ex2(s_m[w * 8 + gg] - Ms);
+                Lsum += s_l[w * 8 + gg] * cf;
+                ov += s_acc[((size_t)w * 8 + gg) * D + d] * cf;
+            }
+            const int h = mt.hk * G + gg;
+            if (mt.nparts == 1) {
+                store_out(P.out, P.out_dtype, ((size_t)mt.s * H + h) * D + d,
+                          Lsum > 0.f ? ov / Lsum : 0.f);
+            } else {
+                const size_t pi = ((size_t)mt.s * H + h) * P.max_parts + mt.p;
+                P.part_acc[pi * D + d] = ov;
+                if (d == 0) {
+                    P.part_m[pi] = M;
+                    P.part_l[pi] = Lsum;
+                }
+            }
+        }
+        if (!consumer_sync(1)) return;  // merge buffers free for the next item
+    }
+}
+
+template <int D, typename T, int R, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
+    paged_decode_mma_kernel(const __grid_constant__ DecodeParams P) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    using L = LayoutMma<D, R>;
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    unsigned char *sk = smem + L::k_off;
+    unsigned char *sv = smem + L::v_off;
+    unsigned char *sq = smem + L::q_off;
+    float *s_acc = reinterpret_cast<float *>(smem + L::acc_off);
+    float *s_m = reinterpret_cast<float *>(smem + L::m_off);
+    float *s_l = reinterpret_cast<float *>(smem + L::l_off);
+    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + L::meta_off);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bar_off);
+    uint64_t *empty = full + R;
+    uint64_t *cbar = reinterpret_cast<uint64_t *>(smem + L::cbar_off);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::flag_off);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int r = 0; r < R; ++r) {
+            mbar_init(&full[r], 1);
+            mbar_init(&empty[r], kNCW);
+        }
+        mbar_init(&cbar[0], kNCW * 32);
+        mbar_init(&cbar[1], kNCW * 32);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0)
+        run_producer_mma<D, T, R>(P, sk, sv, sq, meta, full, empty, abort_flag, lane);
+    else
+        run_consumer_mma<D, T, R>(P, sk, sv, sq, meta, full, empty, cbar, s_acc, s_m, s_l,
+                                  abort_flag, warp - 1, lane);
+}
+
+}  // namespace pa
