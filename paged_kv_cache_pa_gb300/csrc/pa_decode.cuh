@@ -13,7 +13,8 @@
 // How (one persistent CTA family per SM, warp-specialised):
 //   * A work item is (sequence, context partition of <= part_tokens tokens,
 //     KV head).  A plan kernel lists the (sequence, partition) pairs longest
-//     first; CTAs claim items with one atomic each, so the tail is short.
+//     first; CTA b starts with item b and then claims items with one atomic
+//     each, so the tail is short.
 //   * Warp 0 (producer) resolves the item's block-table slice once (one
 //     coalesced load for up to 32 blocks) and streams each block's K and V
 //     tiles -- 16 rows x head_dim contiguous, only the valid rows -- with 1-D
@@ -59,13 +60,13 @@ struct alignas(16) StageMeta {
 };
 
 struct WsHeader {
-    unsigned int counter;   // next item to claim
+    unsigned int counter;   // items claimed beyond the first one of each CTA
     unsigned int n_items;   // (sequence, partition, kv head) items in the plan
 };
 
 struct DecodeParams {
     // Tensor maps of the query and the pools (tensor-core kernel only):
-    // 2-D views [rows][head_dim], 64-element boxes, 128-byte swizzle.
+    // 3-D views [head_dim/64][rows][64], whole-row boxes, 128-byte swizzle.
     CUtensorMap tmap_q, tmap_k, tmap_v;
     void *out;
     int out_dtype;  // PA_F16, PA_BF16 or PA_F32
@@ -169,7 +170,9 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
     const T *qg = static_cast<const T *>(P.q);
     constexpr size_t kTile = (size_t)kBlock * D;
 
-    auto claim = [&]() -> unsigned { return lane == 0 ? atomicAdd(&P.hdr->counter, 1u) : 0u; };
+    auto claim = [&]() -> unsigned {
+        return lane == 0 ? gridDim.x + atomicAdd(&P.hdr->counter, 1u) : 0u;
+    };
     auto bcast = [&](unsigned v) -> unsigned { return __shfl_sync(0xffffffffu, v, 0); };
     auto load_entry = [&](unsigned c) -> int4 {
         return c < n_items ? P.items[c / Hkv] : make_int4(0, 0, 0, 0);
@@ -185,7 +188,8 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
     // Software pipeline over items: claim (atomic) -> entry load -> table
     // load -> copy issue, each stage one item ahead of the next, so the
     // latencies of the dependent loads overlap the previous item's copies.
-    unsigned cA = bcast(claim());
+    // CTA b's first item is item b (no atomic).
+    unsigned cA = blockIdx.x;
     int4 eA = load_entry(cA);
     int tA = load_tab(cA, eA);
     unsigned cB = bcast(claim());
@@ -212,29 +216,29 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
                 break;
             }
             const int phys = __shfl_sync(0xffffffffu, tA, j);
+            const bool bad = phys < 0 || phys >= P.num_blocks;
+            const int nvalid = bad ? 0 : min(kBlock, ntok - j * kBlock);  // bad: skip the block
+            const uint32_t kv_bytes = (uint32_t)nvalid * D * (uint32_t)sizeof(T);
+            const uint32_t q_bytes = j == 0 ? (uint32_t)(G * D * sizeof(T)) : 0u;
             if (lane == 0) {
-                int nvalid = min(kBlock, ntok - j * kBlock);
-                if (phys < 0 || phys >= P.num_blocks) {
-                    if (P.err) atomicOr(P.err, PA_ERRBIT_BLOCK_OOB);
-                    nvalid = 0;  // skip the block
-                }
+                if (bad && P.err) atomicOr(P.err, PA_ERRBIT_BLOCK_OOB);
                 StageMeta m;
                 m.s = s; m.hk = hk; m.p = part; m.nparts = nparts;
                 m.j = j; m.nblk = nblk; m.nvalid = nvalid; m.flags = 0;
                 meta[slot] = m;
-                const uint32_t kv_bytes = (uint32_t)nvalid * D * (uint32_t)sizeof(T);
-                const uint32_t q_bytes = j == 0 ? (uint32_t)(G * D * sizeof(T)) : 0u;
                 mbar_arrive_expect_tx(&full[slot], 2 * kv_bytes + q_bytes);
-                if (kv_bytes) {
-                    const size_t off = ((size_t)phys * Hkv + hk) * kTile;
-                    bulk_g2s(sk + slot * kTile, kc + off, kv_bytes, &full[slot], policy);
-                    bulk_g2s(sv + slot * kTile, vc + off, kv_bytes, &full[slot], policy);
-                }
-                if (q_bytes)
-                    bulk_g2s_nohint(sq + (size_t)slot * GM * D,
-                                    qg + ((size_t)s * P.num_heads + (size_t)hk * G) * D, q_bytes,
-                                    &full[slot]);
             }
+            __syncwarp();
+            // one copy per lane: K rows (lane 0), V rows (lane 1), query (lane 2)
+            if (lane < 2 && kv_bytes) {
+                const size_t off = ((size_t)phys * Hkv + hk) * kTile;
+                bulk_g2s((lane ? sv : sk) + slot * kTile, (lane ? vc : kc) + off, kv_bytes,
+                         &full[slot], policy);
+            }
+            if (lane == 2 && q_bytes)
+                bulk_g2s_nohint(sq + (size_t)slot * GM * D,
+                                qg + ((size_t)s * P.num_heads + (size_t)hk * G) * D, q_bytes,
+                                &full[slot]);
             __syncwarp();
         }
         if (aborted) break;

@@ -71,93 +71,178 @@ WsLayout ws_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
 
 // One CTA: count (sequence, partition) pairs by size, lay them out longest
 // first (a counting sort on the number of blocks), reset the claim counter,
-// and zero the output rows of empty sequences.
-__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *__restrict__ lens, int num_seqs,
-                                                    int max_context_len, int part_tokens,
-                                                    int num_kv_heads, int num_heads, int head_dim,
-                                                    int4 *__restrict__ items, WsHeader *hdr,
-                                                    void *out, int out_dtype, unsigned int *err) {
+// and zero the output rows of empty sequences.  Sequences are taken 1024 at
+// a time, one per thread; shared-memory counters are bumped once per warp
+// and size (warp-aggregated), so threads do not queue on one address.
+constexpr int kPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(
+    const int32_t *__restrict__ lens, int num_seqs, int max_context_len, int part_tokens,
+    int num_kv_heads, int num_heads, int head_dim, int4 *__restrict__ items, WsHeader *hdr,
+    void *out, int out_dtype, unsigned int *err) {
     pdl_trigger();  // the attention CTAs may start their set-up now
     pdl_wait();     // inputs written by earlier work on the stream are ready
-    __shared__ int hist[kMaxPartTokens / kBlock + 1];
-    __shared__ int offs[kMaxPartTokens / kBlock + 1];
+    constexpr int kKeys = kMaxPartTokens / kBlock + 1;
+    __shared__ int hist[kKeys];
+    __shared__ int offs[kKeys];
     const int PB = part_tokens / kBlock;
-    for (int i = threadIdx.x; i <= PB; i += blockDim.x) hist[i] = 0;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    if (tid < kKeys) hist[tid] = 0;
     __syncthreads();
-    for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
-        int L = lens[s];
-        if (L < 0 || L > max_context_len) {
-            if (err) atomicOr(err, PA_ERRBIT_CONTEXT_LEN);
-            L = 0;
-        }
-        if (L == 0) continue;
-        const int np = (L + part_tokens - 1) / part_tokens;
-        if (np > 1) atomicAdd(&hist[PB], np - 1);
-        const int last = L - (np - 1) * part_tokens;
-        atomicAdd(&hist[(last + kBlock - 1) / kBlock], 1);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int key = PB; key >= 1; --key) {
-            offs[key] = run;
-            run += hist[key];
-        }
-        hdr->counter = 0u;
-        hdr->n_items = (unsigned)run * (unsigned)num_kv_heads;
-    }
-    __syncthreads();
-    for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
-        const int L = lens[s];
-        if (L <= 0 || L > max_context_len) continue;
-        const int np = (L + part_tokens - 1) / part_tokens;
-        for (int p = 0; p < np; ++p) {
-            const int ntok = min(part_tokens, L - p * part_tokens);
-            const int pos = atomicAdd(&offs[(ntok + kBlock - 1) / kBlock], 1);
-            items[pos] = make_int4(s, p, ntok, np);
+    // pass 1: histogram of partition sizes (in blocks); zero empty rows
+    for (int s0 = 0; s0 < num_seqs; s0 += kPlanThreads) {
+        const int s = s0 + tid;
+        int L = s < num_seqs ? lens[s] : 1;
+        const bool bad = L < 0 || L > max_context_len;
+        if (bad && s < num_seqs && err) atomicOr(err, PA_ERRBIT_CONTEXT_LEN);
+        if (bad) L = 0;
+        const bool live = s < num_seqs && L > 0;
+        const int np = live ? (L + part_tokens - 1) / part_tokens : 0;
+        // full partitions: one add per warp
+        int full = np > 1 ? np - 1 : 0;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) full += __shfl_xor_sync(0xffffffffu, full, off);
+        if (lane == 0 && full) atomicAdd(&hist[PB], full);
+        // last partitions: one add per distinct size in the warp
+        const int key = live ? (L - (np - 1) * part_tokens + kBlock - 1) / kBlock : 0;
+        const unsigned same = __match_any_sync(0xffffffffu, key);
+        if (live && (same & lt_mask) == 0) atomicAdd(&hist[key], __popc(same));
+        // the warp zeroes the output rows of its empty sequences together
+        unsigned empty = __ballot_sync(0xffffffffu, s < num_seqs && L == 0);
+        while (empty) {
+            const int src = __ffs(empty) - 1;
+            empty &= empty - 1;
+            const size_t base = (size_t)(s0 + (tid & ~31) + src) * num_heads * head_dim;
+            for (int i = lane; i < num_heads * head_dim; i += 32)
+                store_out(out, out_dtype, base + i, 0.f);
         }
     }
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nw = blockDim.x / 32;
-    for (int s = warp; s < num_seqs; s += nw) {
-        const int L = lens[s];
-        if (L > 0 && L <= max_context_len) continue;
-        const size_t base = (size_t)s * num_heads * head_dim;
-        for (int i = lane; i < num_heads * head_dim; i += 32) store_out(out, out_dtype, base + i, 0.f);
+    __syncthreads();
+    if (tid < 32) {  // exclusive scan over sizes, largest first
+        const int key = PB - tid;
+        const int v = (tid < PB) ? hist[key] : 0;
+        int incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, off);
+            if (tid >= off) incl += u;
+        }
+        if (tid < PB) offs[key] = incl - v;
+        if (tid == 31) {
+            hdr->counter = 0u;
+            hdr->n_items = (unsigned)incl * (unsigned)num_kv_heads;
+        }
+    }
+    __syncthreads();
+    // pass 2: place every (sequence, partition)
+    for (int s0 = 0; s0 < num_seqs; s0 += kPlanThreads) {
+        const int s = s0 + tid;
+        const int L0 = s < num_seqs ? lens[s] : 0;
+        const bool live = s < num_seqs && L0 > 0 && L0 <= max_context_len;
+        const int L = live ? L0 : 0;
+        const int np = live ? (L + part_tokens - 1) / part_tokens : 0;
+        // full partitions of the warp: contiguous range from one add
+        const int full = np > 1 ? np - 1 : 0;
+        int incl = full;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += u;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        int base = 0;
+        if (lane == 31 && total) base = atomicAdd(&offs[PB], total);
+        base = __shfl_sync(0xffffffffu, base, 31) + incl - full;
+        for (int p = 0; p < full; ++p)
+            items[base + p] = make_int4(s, p, part_tokens, np);
+        // last partition: rank among the warp's lanes with the same size
+        const int ntok = live ? L - (np - 1) * part_tokens : 0;
+        const int key = live ? (ntok + kBlock - 1) / kBlock : 0;
+        const unsigned same = __match_any_sync(0xffffffffu, key);
+        const int leader = __ffs(same) - 1;
+        int slot = 0;
+        if (live && lane == leader) slot = atomicAdd(&offs[key], __popc(same));
+        slot = __shfl_sync(0xffffffffu, slot, leader) + __popc(same & lt_mask);
+        if (live) items[slot] = make_int4(s, np - 1, ntok, np);
     }
 }
 
-// One warp per (sequence, query head) of a multi-partition sequence.
+// One CTA per (sequence, query head) of a multi-partition sequence:
+//   M = max_p m_p,  c_p = 2^(m_p - M),  L = sum_p l_p c_p,
+//   o = sum_p acc_p c_p / L.
+// The partition weights go to shared memory once; the weighted-value loads
+// are spread over all threads (head_dim/4 float4 columns x partition groups)
+// and reduced in shared memory.
+constexpr int kMergeThreads = 128;
+constexpr int kMergeParts = 2048;  // weights kept in shared memory up to this many partitions
+
 template <int D>
-__global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ DecodeParams P) {
-    pdl_wait();  // partials from the attention kernel
-    constexpr int E = D / 32;
-    const int s = blockIdx.x;
-    const int h = blockIdx.y * 4 + threadIdx.x / 32;
-    const int lane = threadIdx.x % 32;
-    if (h >= P.num_heads) return;
-    const int L = P.context_lens[s];
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ DecodeParams P) {
+    constexpr int C = D / 4;                   // float4 columns
+    constexpr int NG = kMergeThreads / C;      // partition groups
+    __shared__ float s_c[kMergeParts];
+    __shared__ float s_red[kMergeThreads / 32];
+    __shared__ float4 s_acc[NG][C];
+    const int s = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
+    const int L = P.context_lens[s];  // an input: complete before this grid launched
     if (L <= P.part_tokens || L > P.max_context_len) return;  // one partition, or invalid
     const int np = (L + P.part_tokens - 1) / P.part_tokens;
+    pdl_wait();  // partials from the attention kernel
     const size_t base = ((size_t)s * P.num_heads + h) * P.max_parts;
+
     float M = -INFINITY;
-    for (int p = lane; p < np; p += 32) M = fmaxf(M, P.part_m[base + p]);
+    for (int p = tid; p < np; p += kMergeThreads) M = fmaxf(M, P.part_m[base + p]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (lane == 0) s_red[tid / 32] = M;
+    __syncthreads();
+    M = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, s_red[w]);
     const float Ms = M == -INFINITY ? 0.f : M;
-    float o[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) o[e] = 0.f;
-    float Lsum = 0.f;
-    for (int p = 0; p < np; ++p) {
-        const float cf = ex2(P.part_m[base + p] - Ms);
-        Lsum += P.part_l[base + p] * cf;
-        const float *a = P.part_acc + (base + p) * D + lane * E;
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[e] = fmaf(a[e], cf, o[e]);
+    __syncthreads();
+
+    float lsum = 0.f;
+    for (int p = tid; p < np; p += kMergeThreads) {
+        const float c = ex2(P.part_m[base + p] - Ms);
+        if (p < kMergeParts) s_c[p] = c;
+        lsum = fmaf(P.part_l[base + p], c, lsum);
     }
-    const size_t ob = ((size_t)s * P.num_heads + h) * D + lane * E;
 #pragma unroll
-    for (int e = 0; e < E; ++e) store_out(P.out, P.out_dtype, ob + e, Lsum > 0.f ? o[e] / Lsum : 0.f);
+    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    if (lane == 0) s_red[tid / 32] = lsum;
+    __syncthreads();
+    float Lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeThreads / 32; ++w) Lsum += s_red[w];
+
+    const int col = tid % C, grp = tid / C;
+    const float4 *acc = reinterpret_cast<const float4 *>(P.part_acc + base * D) + col;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int p = grp; p < np; p += NG) {
+        const float c = p < kMergeParts ? s_c[p] : ex2(P.part_m[base + p] - Ms);
+        const float4 a = acc[(size_t)p * C];
+        o.x = fmaf(a.x, c, o.x);
+        o.y = fmaf(a.y, c, o.y);
+        o.z = fmaf(a.z, c, o.z);
+        o.w = fmaf(a.w, c, o.w);
+    }
+    s_acc[grp][col] = o;
+    __syncthreads();
+    if (grp == 0) {
+#pragma unroll
+        for (int g = 1; g < NG; ++g) {
+            const float4 b = s_acc[g][col];
+            o.x += b.x; o.y += b.y; o.z += b.z; o.w += b.w;
+        }
+        const size_t ob = ((size_t)s * P.num_heads + h) * D + col * 4;
+        store_out(P.out, P.out_dtype, ob + 0, Lsum > 0.f ? o.x / Lsum : 0.f);
+        store_out(P.out, P.out_dtype, ob + 1, Lsum > 0.f ? o.y / Lsum : 0.f);
+        store_out(P.out, P.out_dtype, ob + 2, Lsum > 0.f ? o.z / Lsum : 0.f);
+        store_out(P.out, P.out_dtype, ob + 3, Lsum > 0.f ? o.w / Lsum : 0.f);
+    }
 }
 
 std::atomic<int> g_sm_count[64];
@@ -183,20 +268,21 @@ EncodeTiledFn tensor_map_encoder() {
     return reinterpret_cast<EncodeTiledFn>(f);
 }
 
-// 2-D view [rows][head_dim] of a row-major 16-bit tensor; boxes of 64
-// elements x box_rows rows with the 128-byte swizzle; reads past the last
-// row return zeros.
+// 3-D view [head_dim / 64][rows][64] of a row-major [rows][head_dim] 16-bit
+// tensor (strides: a row is head_dim * 2 bytes, a 64-element half 128 bytes);
+// one box is box_rows rows with all halves, 128-byte swizzle; reads past the
+// last row return zeros.
 bool encode_rows(CUtensorMap *map, const void *base, pa_dtype_t dtype, unsigned long long rows,
                  int head_dim, int box_rows) {
     EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-    const cuuint32_t elem_strides[2] = {1u, 1u};
+    const cuuint64_t dims[3] = {64u, (cuuint64_t)rows, (cuuint64_t)(head_dim / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, 128u};
+    const cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, (cuuint32_t)(head_dim / 64)};
+    const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
     return enc(map,
                dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-               2, const_cast<void *>(base), dims, strides, box, elem_strides,
+               3, const_cast<void *>(base), dims, strides, box, elem_strides,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -300,7 +386,7 @@ extern "C" pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, cons
     P.err = dev_error_word;
     cudaStream_t st = (cudaStream_t)stream;
 
-    if (launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, (const int32_t *)context_lens,
+    if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, (const int32_t *)context_lens,
                    num_seqs, max_context_len, w.part_tokens, num_kv_heads, num_heads, head_dim,
                    P.items, P.hdr, out, (int)out_dtype, dev_error_word) != cudaSuccess)
         return PA_ERR_CUDA;
@@ -319,14 +405,15 @@ extern "C" pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, cons
     if (st_launch != PA_OK) return st_launch;
 
     if (w.max_parts > 1) {
-        const dim3 grid((unsigned)num_seqs, (unsigned)((num_heads + 3) / 4));
+        if (num_heads > 65535) return PA_ERR_UNSUPPORTED;
+        const dim3 grid((unsigned)num_seqs, (unsigned)num_heads);
         cudaError_t e;
         if (head_dim == 64)
-            e = launch_pdl(merge_kernel<64>, grid, dim3(128), 0, st, P);
+            e = launch_pdl(merge_kernel<64>, grid, dim3(kMergeThreads), 0, st, P);
         else if (head_dim == 128)
-            e = launch_pdl(merge_kernel<128>, grid, dim3(128), 0, st, P);
+            e = launch_pdl(merge_kernel<128>, grid, dim3(kMergeThreads), 0, st, P);
         else
-            e = launch_pdl(merge_kernel<256>, grid, dim3(128), 0, st, P);
+            e = launch_pdl(merge_kernel<256>, grid, dim3(kMergeThreads), 0, st, P);
         if (e != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;

@@ -59,7 +59,7 @@ pa_status_t launch_one_mma(const DecodeParams &P, int grid_cap, cudaStream_t str
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)L::bytes) != cudaSuccess)
             return PA_ERR_CUDA;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, L::bytes) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreadsMma, L::bytes) !=
             cudaSuccess)
             return PA_ERR_CUDA;
         if (occ < 1) return PA_ERR_UNSUPPORTED;
@@ -68,7 +68,8 @@ pa_status_t launch_one_mma(const DecodeParams &P, int grid_cap, cudaStream_t str
     long long grid = (long long)current_sm_count() * occ;
     if (grid > grid_cap) grid = grid_cap;
     if (grid < 1) grid = 1;
-    if (launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), L::bytes, stream, P) != cudaSuccess)
+    if (launch_pdl(kern, dim3((unsigned)grid), dim3(kThreadsMma), L::bytes, stream, P) !=
+        cudaSuccess)
         return PA_ERR_CUDA;
     return PA_OK;
 }

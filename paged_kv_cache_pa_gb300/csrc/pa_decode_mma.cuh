@@ -12,13 +12,20 @@
 // PagedAttention, "PagedAttention Algorithm": block-wise attention].
 //
 // Data movement: the producer warp fetches up to four blocks per stage (one
-// per consumer warp) with 2-D tiled bulk copies (TMA) through tensor maps of
-// the pools viewed as [blocks * KV heads * 16 rows][head_dim], 64-element
-// boxes with the 128-byte swizzle, so the ldmatrix reads of the consumers are
-// free of bank conflicts.  The item's query rows (8-row box) ride with its
+// per consumer warp) with tiled bulk copies (TMA) through 3-D tensor maps of
+// the pools viewed as [head_dim / 64 halves][blocks * KV heads * 16 rows][64],
+// with the 128-byte swizzle: one copy brings a block's whole K (or V) tile as
+// [half][token][64], and the ldmatrix reads of the consumers are free of bank
+// conflicts.  The copies of a stage are issued by separate lanes in one warp
+// instruction.  The item's query rows (8-row box) ride with its
 // first stage.  A block's box always has 16 rows; rows past the sequence's
 // length are masked out of the scores and zeroed in the V tile before P V,
 // so stale or poisoned data never reaches the output.
+//
+// Item ends: each consumer warp hands its running state for the item to a
+// dedicated epilogue warp through one of two shared-memory buffers and goes
+// straight on to the next stage; the epilogue warp merges the four states and
+// writes the output row or the partition's partial state.
 //
 // Precision: P is rounded to the operand type in two parts, P = P_hi + P_lo,
 // and both are multiplied with V, so the weights carry ~16 significant bits
@@ -34,19 +41,29 @@ constexpr int kBPS = kNCW;            // blocks per stage: one per consumer warp
 constexpr size_t kBoxBytes = 16 * 128;  // one block's 64-element box: 16 rows x 128 B
 constexpr size_t kQBoxBytes = 8 * 128;  // the query box: 8 rows x 128 B
 
+// Per-item hand-off from the consumer warps to the epilogue warp.
+struct alignas(16) ItemInfo {
+    int s, hk, p, nparts;
+    int flags, pad0, pad1, pad2;
+};
+
+constexpr int kThreadsMma = 32 * (kNCW + 2);  // producer, 4 consumers, epilogue
+
 template <int D, int R>
 struct LayoutMma {
     static constexpr int kBoxes = D / 64;
     static constexpr size_t k_off = 0;  // [R][BPS][boxes] boxes, 1 KiB aligned
     static constexpr size_t v_off = k_off + (size_t)R * kBPS * kBoxes * kBoxBytes;
     static constexpr size_t q_off = v_off + (size_t)R * kBPS * kBoxes * kBoxBytes;
-    static constexpr size_t acc_off = q_off + (size_t)R * kBoxes * kQBoxBytes;  // f32 [NCW][8][D]
-    static constexpr size_t m_off = acc_off + (size_t)kNCW * 8 * D * 4;
-    static constexpr size_t l_off = m_off + (size_t)kNCW * 8 * 4;
-    static constexpr size_t meta_off = (l_off + (size_t)kNCW * 8 * 4 + 15) / 16 * 16;
+    // two hand-off buffers: f32 acc [2][NCW][8][D], m and l [2][NCW][8]
+    static constexpr size_t acc_off = q_off + (size_t)R * kBoxes * kQBoxBytes;
+    static constexpr size_t m_off = acc_off + (size_t)2 * kNCW * 8 * D * 4;
+    static constexpr size_t l_off = m_off + (size_t)2 * kNCW * 8 * 4;
+    static constexpr size_t info_off = (l_off + (size_t)2 * kNCW * 8 * 4 + 15) / 16 * 16;
+    static constexpr size_t meta_off = info_off + 2 * sizeof(ItemInfo);
     static constexpr size_t bar_off = meta_off + (size_t)R * sizeof(StageMeta);
-    static constexpr size_t cbar_off = bar_off + (size_t)2 * R * 8;
-    static constexpr size_t flag_off = cbar_off + 2 * 8;
+    // full[R], empty[R], acc_full[2], acc_empty[2]
+    static constexpr size_t flag_off = bar_off + (size_t)(2 * R + 4) * 8;
     static constexpr size_t used = flag_off + 16;
     static constexpr size_t bytes = used + 1024;  // slack to align the base to 1 KiB
 };
@@ -57,7 +74,7 @@ struct TuningMma {
     static constexpr size_t kBudget = 233472 / kMinBlocks - 1024 - 512;
     static constexpr size_t kStage =
         (size_t)2 * kBPS * (D / 64) * kBoxBytes + (D / 64) * kQBoxBytes + 32 + 16;
-    static constexpr size_t kFixed = (size_t)kNCW * 8 * (D + 2) * 4 + 64 + 1024;
+    static constexpr size_t kFixed = (size_t)2 * kNCW * 8 * (D + 2) * 4 + 2 * 32 + 96 + 1024;
     static constexpr int kRaw = (int)((kBudget - kFixed) / kStage);
     static constexpr int kStages = kRaw > 8 ? 8 : kRaw;
     static_assert(kStages >= 2, "ring too shallow");
@@ -137,7 +154,9 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
     const int PB = P.part_tokens / kBlock;
     const uint64_t policy = l2_evict_first_policy();
 
-    auto claim = [&]() -> unsigned { return lane == 0 ? atomicAdd(&P.hdr->counter, 1u) : 0u; };
+    auto claim = [&]() -> unsigned {
+        return lane == 0 ? gridDim.x + atomicAdd(&P.hdr->counter, 1u) : 0u;
+    };
     auto bcast = [&](unsigned v) -> unsigned { return __shfl_sync(0xffffffffu, v, 0); };
     auto load_entry = [&](unsigned c) -> int4 {
         return c < n_items ? P.items[c / Hkv] : make_int4(0, 0, 0, 0);
@@ -150,7 +169,11 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
         return -1;
     };
 
-    unsigned cA = bcast(claim());
+    // Software pipeline over items: claim (atomic) -> entry load -> table
+    // load -> copy issue, each stage one item ahead of the next, so the
+    // latencies of the dependent loads overlap the previous item's copies.
+    // CTA b's first item is item b (no atomic).
+    unsigned cA = blockIdx.x;
     int4 eA = load_entry(cA);
     int tA = load_tab(cA, eA);
     unsigned cB = bcast(claim());
@@ -178,46 +201,40 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
                 break;
             }
             const int j0 = st * kBPS;
+            const int nb = min(kBPS, nblk - j0);
             int phys[kBPS];
+            unsigned bad = 0;  // blocks with an out-of-range id are skipped
 #pragma unroll
-            for (int b = 0; b < kBPS; ++b) phys[b] = __shfl_sync(0xffffffffu, tA, min(j0 + b, 31));
+            for (int b = 0; b < kBPS; ++b) {
+                phys[b] = __shfl_sync(0xffffffffu, tA, min(j0 + b, 31));
+                if (b < nb && (phys[b] < 0 || phys[b] >= P.num_blocks)) bad |= 1u << b;
+            }
             if (lane == 0) {
-                const int nb = min(kBPS, nblk - j0);
-                unsigned bad = 0;
-                uint32_t bytes = st == 0 ? (uint32_t)(KB * kQBoxBytes) : 0u;
-#pragma unroll
-                for (int b = 0; b < kBPS; ++b) {
-                    if (b >= nb) continue;
-                    if (phys[b] < 0 || phys[b] >= P.num_blocks) {
-                        if (P.err) atomicOr(P.err, PA_ERRBIT_BLOCK_OOB);
-                        bad |= 1u << b;  // skip the block
-                    } else {
-                        bytes += (uint32_t)(2 * KB * kBoxBytes);
-                    }
-                }
+                if (bad && P.err) atomicOr(P.err, PA_ERRBIT_BLOCK_OOB);
+                const uint32_t bytes = (uint32_t)(2 * (nb - __popc(bad)) * KB * kBoxBytes) +
+                                       (st == 0 ? (uint32_t)(KB * kQBoxBytes) : 0u);
                 StageMeta m;
                 m.s = s; m.hk = hk; m.p = part; m.nparts = nparts;
                 m.j = st; m.nblk = nst; m.nvalid = ntok - j0 * kBlock; m.flags = (int)(bad << 8);
                 meta[slot] = m;
                 mbar_arrive_expect_tx(&full[slot], bytes);
-#pragma unroll
-                for (int b = 0; b < kBPS; ++b) {
-                    if (b >= nb || (bad >> b) & 1u) continue;
-                    const int y = (phys[b] * P.num_kv_heads + hk) * kBlock;
-#pragma unroll
-                    for (int h = 0; h < KB; ++h) {
-                        const size_t off = ((size_t)(slot * kBPS + b) * KB + h) * kBoxBytes;
-                        tma_load_2d(sk + off, &P.tmap_k, h * 64, y, &full[slot], policy);
-                        tma_load_2d(sv + off, &P.tmap_v, h * 64, y, &full[slot], policy);
-                    }
-                }
-                if (st == 0) {
-#pragma unroll
-                    for (int h = 0; h < KB; ++h)
-                        tma_load_2d(sq + ((size_t)slot * KB + h) * kQBoxBytes, &P.tmap_q, h * 64,
-                                    s * P.num_heads + hk * G, &full[slot], policy);
-                }
             }
+            __syncwarp();
+            // one copy per lane: lane 2b fetches block b's K tile, lane 2b+1 its
+            // V tile (both 64-element halves in one 3-D box); lane 2*kBPS the
+            // item's query rows
+            if (lane < 2 * nb && !((bad >> (lane >> 1)) & 1u)) {
+                const int b = lane >> 1;
+                const size_t off = (size_t)(slot * kBPS + b) * KB * kBoxBytes;
+                const int y = (phys[b] * P.num_kv_heads + hk) * kBlock;
+                if (lane & 1)
+                    tma_load_3d(sv + off, &P.tmap_v, 0, y, 0, &full[slot], policy);
+                else
+                    tma_load_3d(sk + off, &P.tmap_k, 0, y, 0, &full[slot], policy);
+            }
+            if (st == 0 && lane == 2 * kBPS)
+                tma_load_3d(sq + (size_t)slot * KB * kQBoxBytes, &P.tmap_q, 0,
+                            s * P.num_heads + hk * G, 0, &full[slot], policy);
             __syncwarp();
         }
         if (aborted) break;
@@ -259,27 +276,29 @@ template <int D, typename T, int R>
 __device__ __forceinline__ void run_consumer_mma(const DecodeParams &P, unsigned char *sk,
                                                  unsigned char *sv, const unsigned char *sq,
                                                  const StageMeta *meta, uint64_t *full,
-                                                 uint64_t *empty, uint64_t *cbar, float *s_acc,
-                                                 float *s_m, float *s_l,
+                                                 uint64_t *empty, uint64_t *acc_full,
+                                                 uint64_t *acc_empty, float *s_acc, float *s_m,
+                                                 float *s_l, ItemInfo *info,
                                                  volatile int *abort_flag, int cw, int lane) {
     constexpr int KB = D / 64;
     constexpr int NK = D / 16;  // k-steps of Q K^T
     constexpr int NT = D / 8;   // n-tiles of P V
     const int g = lane >> 2, t = lane & 3;
     const int G = P.G;
-    const int tid = cw * 32 + lane;
     const float sc = P.scale_log2;
-
-    uint32_t bar_par[2] = {0u, 0u};
-    auto consumer_sync = [&](int b) -> bool {
-        mbar_arrive(&cbar[b]);
-        const bool ok = mbar_wait(&cbar[b], bar_par[b], abort_flag);
-        bar_par[b] ^= 1u;
-        if (__all_sync(0xffffffffu, ok)) return true;
+    uint32_t handoffs = 0;  // items handed to the epilogue warp so far
+    auto fail = [&]() {
         if (lane == 0) {
             *abort_flag = 1;
             if (P.err) atomicOr(P.err, PA_ERRBIT_TIMEOUT);
         }
+    };
+    // Take the next hand-off buffer (waits only if the epilogue is two items behind).
+    auto take_buffer = [&](int &buf) -> bool {
+        buf = (int)(handoffs & 1u);
+        const bool ok = mbar_wait(&acc_empty[buf], ((handoffs >> 1) & 1u) ^ 1u, abort_flag);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        fail();
         return false;
     };
 
@@ -295,14 +314,17 @@ __device__ __forceinline__ void run_consumer_mma(const DecodeParams &P, unsigned
         const int slot = (int)(k % R);
         const bool okw = mbar_wait(&full[slot], (k / R) & 1u, abort_flag);
         if (!__all_sync(0xffffffffu, okw)) {
-            if (lane == 0) {
-                *abort_flag = 1;
-                if (P.err) atomicOr(P.err, PA_ERRBIT_TIMEOUT);
-            }
+            fail();
             return;
         }
         const StageMeta mt = meta[slot];
-        if (mt.flags & kEndFlag) return;
+        if (mt.flags & kEndFlag) {  // tell the epilogue warp there is no more work
+            int buf;
+            if (!take_buffer(buf)) return;
+            if (cw == 0 && lane == 0) info[buf].flags = kEndFlag;
+            mbar_arrive(&acc_full[buf]);
+            return;
+        }
 
         if (mt.j == 0) {  // new item: query fragments (rows 0..7; rows 8..15 are zero)
             const uint32_t qbase = smem_u32(sq + (size_t)slot * KB * kQBoxBytes);
@@ -390,53 +412,93 @@ __device__ __forceinline__ void run_consumer_mma(const DecodeParams &P, unsigned
 
         if (mt.j != mt.nblk - 1) continue;
 
-        // ---- item complete: warp state -> shared memory, then merge warps ----
+        // ---- item complete: hand the warp's state to the epilogue warp ----
         float lq = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
         lq += __shfl_xor_sync(0xffffffffu, lq, 2);
+        int buf;
+        if (!take_buffer(buf)) return;
+        float *acc_b = s_acc + (size_t)buf * kNCW * 8 * D;
         if (g < G) {
-            float *dst = s_acc + ((size_t)cw * 8 + g) * D + 2 * t;
+            float *dst = acc_b + ((size_t)cw * 8 + g) * D + 2 * t;
 #pragma unroll
             for (int n = 0; n < NT; ++n)
                 *reinterpret_cast<float2 *>(dst + 8 * n) = make_float2(o[n][0], o[n][1]);
             if (t == 0) {
-                s_m[cw * 8 + g] = m_run;
-                s_l[cw * 8 + g] = lq;
+                s_m[(buf * kNCW + cw) * 8 + g] = m_run;
+                s_l[(buf * kNCW + cw) * 8 + g] = lq;
             }
         }
-        if (!consumer_sync(0)) return;
-        const int H = P.num_heads;
-        for (int idx = tid; idx < G * D; idx += kNCW * 32) {
-            const int gg = idx / D, d = idx - gg * D;
+        if (cw == 0 && lane == 0) {
+            ItemInfo it;
+            it.s = mt.s; it.hk = mt.hk; it.p = mt.p; it.nparts = mt.nparts;
+            it.flags = 0; it.pad0 = it.pad1 = it.pad2 = 0;
+            info[buf] = it;
+        }
+        mbar_arrive(&acc_full[buf]);  // every consumer thread: its writes are released
+        ++handoffs;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// epilogue warp: merge the four consumer warps' states of each item and write
+// the output row (one partition) or the partition's partial state
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void run_epilogue_mma(const DecodeParams &P, uint64_t *acc_full,
+                                                 uint64_t *acc_empty, const float *s_acc,
+                                                 const float *s_m, const float *s_l,
+                                                 const ItemInfo *info, volatile int *abort_flag,
+                                                 int lane) {
+    const int G = P.G, H = P.num_heads;
+    for (uint32_t n = 0;; ++n) {
+        const int buf = (int)(n & 1u);
+        const bool ok = mbar_wait(&acc_full[buf], (n >> 1) & 1u, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) {
+                *abort_flag = 1;
+                if (P.err) atomicOr(P.err, PA_ERRBIT_TIMEOUT);
+            }
+            return;
+        }
+        const ItemInfo it = info[buf];
+        if (it.flags & kEndFlag) return;
+        const float *acc_b = s_acc + (size_t)buf * kNCW * 8 * D;
+        const float *m_b = s_m + buf * kNCW * 8, *l_b = s_l + buf * kNCW * 8;
+        for (int gg = 0; gg < G; ++gg) {
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kNCW; ++w) M = fmaxf(M, s_m[w * 8 + gg]);
+            for (int w = 0; w < kNCW; ++w) M = fmaxf(M, m_b[w * 8 + gg]);
             const float Ms = M == -INFINITY ? 0.f : M;
-            float Lsum = 0.f, ov = 0.f;
+            float cf[kNCW], Lsum = 0.f;
 #pragma unroll
             for (int w = 0; w < kNCW; ++w) {
-                const float cf = ex2(s_m[w * 8 + gg] - Ms);
-                Lsum += s_l[w * 8 + gg] * cf;
-                ov += s_acc[((size_t)w * 8 + gg) * D + d] * cf;
+                cf[w] = ex2(m_b[w * 8 + gg] - Ms);
+                Lsum += l_b[w * 8 + gg] * cf[w];
             }
-            const int h = mt.hk * G + gg;
-            if (mt.nparts == 1) {
-                store_out(P.out, P.out_dtype, ((size_t)mt.s * H + h) * D + d,
-                          Lsum > 0.f ? ov / Lsum : 0.f);
-            } else {
-                const size_t pi = ((size_t)mt.s * H + h) * P.max_parts + mt.p;
-                P.part_acc[pi * D + d] = ov;
-                if (d == 0) {
-                    P.part_m[pi] = M;
-                    P.part_l[pi] = Lsum;
-                }
+            const int h = it.hk * G + gg;
+            const size_t pi = ((size_t)it.s * H + h) * P.max_parts + it.p;
+            for (int d = lane; d < D; d += 32) {
+                float ov = 0.f;
+#pragma unroll
+                for (int w = 0; w < kNCW; ++w) ov += acc_b[((size_t)w * 8 + gg) * D + d] * cf[w];
+                if (it.nparts == 1)
+                    store_out(P.out, P.out_dtype, ((size_t)it.s * H + h) * D + d,
+                              Lsum > 0.f ? ov / Lsum : 0.f);
+                else
+                    P.part_acc[pi * D + d] = ov;
+            }
+            if (it.nparts > 1 && lane == 0) {
+                P.part_m[pi] = M;
+                P.part_l[pi] = Lsum;
             }
         }
-        if (!consumer_sync(1)) return;  // merge buffers free for the next item
+        __syncwarp();
+        mbar_arrive(&acc_empty[buf]);  // every lane: buffer free
     }
 }
 
 template <int D, typename T, int R, int MINB>
-__global__ void __launch_bounds__(kThreads, MINB)
+__global__ void __launch_bounds__(kThreadsMma, MINB)
     paged_decode_mma_kernel(const __grid_constant__ DecodeParams P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     using L = LayoutMma<D, R>;
@@ -448,10 +510,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
     float *s_acc = reinterpret_cast<float *>(smem + L::acc_off);
     float *s_m = reinterpret_cast<float *>(smem + L::m_off);
     float *s_l = reinterpret_cast<float *>(smem + L::l_off);
+    ItemInfo *info = reinterpret_cast<ItemInfo *>(smem + L::info_off);
     StageMeta *meta = reinterpret_cast<StageMeta *>(smem + L::meta_off);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bar_off);
     uint64_t *empty = full + R;
-    uint64_t *cbar = reinterpret_cast<uint64_t *>(smem + L::cbar_off);
+    uint64_t *acc_full = empty + R;
+    uint64_t *acc_empty = acc_full + 2;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::flag_off);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -460,17 +524,21 @@ __global__ void __launch_bounds__(kThreads, MINB)
             mbar_init(&full[r], 1);
             mbar_init(&empty[r], kNCW);
         }
-        mbar_init(&cbar[0], kNCW * 32);
-        mbar_init(&cbar[1], kNCW * 32);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], kNCW * 32);
+            mbar_init(&acc_empty[b], 32);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
     if (warp == 0)
         run_producer_mma<D, T, R>(P, sk, sv, sq, meta, full, empty, abort_flag, lane);
+    else if (warp <= kNCW)
+        run_consumer_mma<D, T, R>(P, sk, sv, sq, meta, full, empty, acc_full, acc_empty, s_acc,
+                                  s_m, s_l, info, abort_flag, warp - 1, lane);
     else
-        run_consumer_mma<D, T, R>(P, sk, sv, sq, meta, full, empty, cbar, s_acc, s_m, s_l,
-                                  abort_flag, warp - 1, lane);
+        run_epilogue_mma<D>(P, acc_full, acc_empty, s_acc, s_m, s_l, info, abort_flag, lane);
 }
 
 }  // namespace pa

@@ -99,15 +99,14 @@ __device__ __forceinline__ void bulk_g2s_nohint(void *dst, const void *src, uint
         : "memory");
 }
 
-// 2-D tiled bulk copy (TMA) global -> this CTA's shared memory through a
-// tensor map; x (innermost, elements) and y are the box's start coordinates.
-// x * element size must be a multiple of 16 bytes.
-__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y,
+// 3-D tiled bulk copy (TMA) through a tensor map; x is the innermost
+// coordinate (elements) and must satisfy the same 16-byte rule.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, int y, int z,
                                             uint64_t *bar, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 
