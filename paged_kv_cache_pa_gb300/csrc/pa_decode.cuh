@@ -13,8 +13,8 @@
 // How (one persistent CTA family per SM, warp-specialised):
 //   * A work item is (sequence, context partition of <= part_tokens tokens,
 //     KV head).  A plan kernel lists the (sequence, partition) pairs longest
-//     first; CTA b starts with item b and then claims items with one atomic
-//     each, so the tail is short.
+//     first; CTAs take their first three items in a fixed order and claim
+//     the rest with one atomic each, so the tail is short.
 //   * Warp 0 (producer) resolves the item's block-table slice once (one
 //     coalesced load for up to 32 blocks) and streams each block's K and V
 //     tiles -- 16 rows x head_dim contiguous, only the valid rows -- with 1-D
@@ -60,7 +60,7 @@ struct alignas(16) StageMeta {
 };
 
 struct WsHeader {
-    unsigned int counter;   // items claimed beyond the first one of each CTA
+    unsigned int counter;   // items claimed beyond the first three rounds
     unsigned int n_items;   // (sequence, partition, kv head) items in the plan
 };
 
@@ -153,6 +153,64 @@ struct Tuning {
 };
 
 // ---------------------------------------------------------------------------
+// Item pipeline of one producer warp.  Rounds 0..2 are assigned statically
+// (CTA b takes items b, b + grid, b + 2 grid), later items are claimed with
+// one atomic each.  Four items are in flight: X (issuing), Y (block-table
+// slice loaded), Z (entry loaded, slice loading), and the claim of the item
+// after Z; every load is issued at least one item before its value is used,
+// so only the very first item waits for two dependent loads.
+// ---------------------------------------------------------------------------
+struct ItemPipe {
+    const DecodeParams *P;
+    unsigned n_items, Hkv;
+    int PB, lane;
+    unsigned cX, cY, cZ, raw;  // item indices; raw: lane 0's pending claim
+    int4 eX, eY, eZ;           // entries (s, p, ntok, nparts)
+    int tX, tY;                // this lane's block-table entry of X and Y
+
+    __device__ __forceinline__ int4 entry(unsigned c) const {
+        return c < n_items ? P->items[c / Hkv] : make_int4(0, 0, 0, 0);
+    }
+    __device__ __forceinline__ int table(unsigned c, int4 e) const {
+        const int nblk = (e.z + kBlock - 1) / kBlock;
+        if (c < n_items && lane < nblk)
+            return __ldg(&P->block_tables[(size_t)e.x * P->max_blocks_per_seq + (size_t)e.y * PB +
+                                          lane]);
+        return -1;
+    }
+    __device__ __forceinline__ unsigned claim() const {
+        return lane == 0 ? 3u * gridDim.x + atomicAdd(&P->hdr->counter, 1u) : 0u;
+    }
+    __device__ __forceinline__ void init(const DecodeParams &params, unsigned n, int lane_) {
+        P = &params;
+        n_items = n;
+        Hkv = (unsigned)params.num_kv_heads;
+        PB = params.part_tokens / kBlock;
+        lane = lane_;
+        cX = blockIdx.x;
+        cY = blockIdx.x + gridDim.x;
+        cZ = blockIdx.x + 2u * gridDim.x;
+        eX = entry(cX);
+        eY = entry(cY);
+        eZ = entry(cZ);
+        raw = claim();
+        tX = table(cX, eX);
+        tY = table(cY, eY);
+    }
+    __device__ __forceinline__ bool valid() const { return cX < n_items; }
+    // Move to the next item; called after the current item's copies are issued.
+    __device__ __forceinline__ void advance() {
+        const int tZ = table(cZ, eZ);
+        const unsigned cW = __shfl_sync(0xffffffffu, raw, 0);
+        const int4 eW = entry(cW);
+        raw = claim();
+        cX = cY; eX = eY; tX = tY;
+        cY = cZ; eY = eZ; tY = tZ;
+        cZ = cW; eZ = eW;
+    }
+};
+
+// ---------------------------------------------------------------------------
 // producer warp
 // ---------------------------------------------------------------------------
 template <int D, int GM, typename T, int R>
@@ -163,46 +221,21 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
     const unsigned n_items = P.hdr->n_items;
     const unsigned Hkv = (unsigned)P.num_kv_heads;
     const int G = P.G;
-    const int PB = P.part_tokens / kBlock;
     const uint64_t policy = l2_evict_first_policy();
     const T *kc = static_cast<const T *>(P.k_cache);
     const T *vc = static_cast<const T *>(P.v_cache);
     const T *qg = static_cast<const T *>(P.q);
     constexpr size_t kTile = (size_t)kBlock * D;
 
-    auto claim = [&]() -> unsigned {
-        return lane == 0 ? gridDim.x + atomicAdd(&P.hdr->counter, 1u) : 0u;
-    };
-    auto bcast = [&](unsigned v) -> unsigned { return __shfl_sync(0xffffffffu, v, 0); };
-    auto load_entry = [&](unsigned c) -> int4 {
-        return c < n_items ? P.items[c / Hkv] : make_int4(0, 0, 0, 0);
-    };
-    auto load_tab = [&](unsigned c, int4 e) -> int {
-        const int nblk = (e.z + kBlock - 1) / kBlock;
-        if (c < n_items && lane < nblk)
-            return __ldg(&P.block_tables[(size_t)e.x * P.max_blocks_per_seq + (size_t)e.y * PB +
-                                         lane]);
-        return -1;
-    };
-
-    // Software pipeline over items: claim (atomic) -> entry load -> table
-    // load -> copy issue, each stage one item ahead of the next, so the
-    // latencies of the dependent loads overlap the previous item's copies.
-    // CTA b's first item is item b (no atomic).
-    unsigned cA = blockIdx.x;
-    int4 eA = load_entry(cA);
-    int tA = load_tab(cA, eA);
-    unsigned cB = bcast(claim());
-    int4 eB = load_entry(cB);
-    unsigned raw = claim();
+    ItemPipe items;
+    items.init(P, n_items, lane);
 
     uint32_t k = 0;  // stages issued so far
     bool aborted = false;
-    while (cA < n_items) {
-        const int tB = load_tab(cB, eB);
-        const unsigned cC = bcast(raw);
-        const int4 eC = load_entry(cC);
-        raw = claim();
+    while (items.valid()) {
+        const unsigned cA = items.cX;
+        const int4 eA = items.eX;
+        const int tA = items.tX;
 
         const int s = eA.x, part = eA.y, ntok = eA.z, nparts = eA.w;
         const int hk = (int)(cA % Hkv);
@@ -242,8 +275,7 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
             __syncwarp();
         }
         if (aborted) break;
-        cA = cB; eA = eB; tA = tB;
-        cB = cC; eB = eC;
+        items.advance();
     }
     if (!aborted) {  // end-of-work marker for the consumers
         const int slot = (int)(k % R);

@@ -44,13 +44,16 @@ pa_status_t launch_one(const DecodeParams &P, int grid_cap, cudaStream_t stream)
     return PA_OK;
 }
 
-template <int D, typename T>
+// Consumer warps per CTA of the tensor-core kernel.
+constexpr int kMmaWarps = 4;
+
+template <int D, typename T, int W = kMmaWarps>
 pa_status_t launch_one_mma(const DecodeParams &P, int grid_cap, cudaStream_t stream) {
-    using Tn = TuningMma<D>;
+    using Tn = TuningMma<D, W>;
     constexpr int R = Tn::kStages;
     constexpr int MINB = Tn::kMinBlocks;
-    using L = LayoutMma<D, R>;
-    auto kern = paged_decode_mma_kernel<D, T, R, MINB>;
+    using L = LayoutMma<D, R, W>;
+    auto kern = paged_decode_mma_kernel<D, T, R, MINB, W>;
     static std::atomic<int> occ_cache[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
@@ -59,7 +62,7 @@ pa_status_t launch_one_mma(const DecodeParams &P, int grid_cap, cudaStream_t str
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)L::bytes) != cudaSuccess)
             return PA_ERR_CUDA;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreadsMma, L::bytes) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads_mma<W>(), L::bytes) !=
             cudaSuccess)
             return PA_ERR_CUDA;
         if (occ < 1) return PA_ERR_UNSUPPORTED;
@@ -68,7 +71,7 @@ pa_status_t launch_one_mma(const DecodeParams &P, int grid_cap, cudaStream_t str
     long long grid = (long long)current_sm_count() * occ;
     if (grid > grid_cap) grid = grid_cap;
     if (grid < 1) grid = 1;
-    if (launch_pdl(kern, dim3((unsigned)grid), dim3(kThreadsMma), L::bytes, stream, P) !=
+    if (launch_pdl(kern, dim3((unsigned)grid), dim3(threads_mma<W>()), L::bytes, stream, P) !=
         cudaSuccess)
         return PA_ERR_CUDA;
     return PA_OK;

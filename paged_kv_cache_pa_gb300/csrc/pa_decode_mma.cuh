@@ -11,7 +11,7 @@
 // K/V read; Efficient Memory Management for Large Language Model Serving with
 // PagedAttention, "PagedAttention Algorithm": block-wise attention].
 //
-// Data movement: the producer warp fetches up to four blocks per stage (one
+// Data movement: the producer warp fetches up to W blocks per stage (one
 // per consumer warp) with tiled bulk copies (TMA) through 3-D tensor maps of
 // the pools viewed as [head_dim / 64 halves][blocks * KV heads * 16 rows][64],
 // with the 128-byte swizzle: one copy brings a block's whole K (or V) tile as
@@ -37,7 +37,6 @@
 
 namespace pa {
 
-constexpr int kBPS = kNCW;            // blocks per stage: one per consumer warp
 constexpr size_t kBoxBytes = 16 * 128;  // one block's 64-element box: 16 rows x 128 B
 constexpr size_t kQBoxBytes = 8 * 128;  // the query box: 8 rows x 128 B
 
@@ -47,19 +46,21 @@ struct alignas(16) ItemInfo {
     int flags, pad0, pad1, pad2;
 };
 
-constexpr int kThreadsMma = 32 * (kNCW + 2);  // producer, 4 consumers, epilogue
+// threads of a CTA with W consumer warps: producer, W consumers, epilogue
+template <int W>
+constexpr int threads_mma() { return 32 * (W + 2); }
 
-template <int D, int R>
+template <int D, int R, int W>
 struct LayoutMma {
     static constexpr int kBoxes = D / 64;
     static constexpr size_t k_off = 0;  // [R][BPS][boxes] boxes, 1 KiB aligned
-    static constexpr size_t v_off = k_off + (size_t)R * kBPS * kBoxes * kBoxBytes;
-    static constexpr size_t q_off = v_off + (size_t)R * kBPS * kBoxes * kBoxBytes;
+    static constexpr size_t v_off = k_off + (size_t)R * W * kBoxes * kBoxBytes;
+    static constexpr size_t q_off = v_off + (size_t)R * W * kBoxes * kBoxBytes;
     // two hand-off buffers: f32 acc [2][NCW][8][D], m and l [2][NCW][8]
     static constexpr size_t acc_off = q_off + (size_t)R * kBoxes * kQBoxBytes;
-    static constexpr size_t m_off = acc_off + (size_t)2 * kNCW * 8 * D * 4;
-    static constexpr size_t l_off = m_off + (size_t)2 * kNCW * 8 * 4;
-    static constexpr size_t info_off = (l_off + (size_t)2 * kNCW * 8 * 4 + 15) / 16 * 16;
+    static constexpr size_t m_off = acc_off + (size_t)2 * W * 8 * D * 4;
+    static constexpr size_t l_off = m_off + (size_t)2 * W * 8 * 4;
+    static constexpr size_t info_off = (l_off + (size_t)2 * W * 8 * 4 + 15) / 16 * 16;
     static constexpr size_t meta_off = info_off + 2 * sizeof(ItemInfo);
     static constexpr size_t bar_off = meta_off + (size_t)R * sizeof(StageMeta);
     // full[R], empty[R], acc_full[2], acc_empty[2]
@@ -68,13 +69,13 @@ struct LayoutMma {
     static constexpr size_t bytes = used + 1024;  // slack to align the base to 1 KiB
 };
 
-template <int D>
+template <int D, int W>
 struct TuningMma {
-    static constexpr int kMinBlocks = 2;
+    static constexpr int kMinBlocks = W >= 4 ? 2 : (W == 2 ? 3 : 4);
     static constexpr size_t kBudget = 233472 / kMinBlocks - 1024 - 512;
     static constexpr size_t kStage =
-        (size_t)2 * kBPS * (D / 64) * kBoxBytes + (D / 64) * kQBoxBytes + 32 + 16;
-    static constexpr size_t kFixed = (size_t)2 * kNCW * 8 * (D + 2) * 4 + 2 * 32 + 96 + 1024;
+        (size_t)2 * W * (D / 64) * kBoxBytes + (D / 64) * kQBoxBytes + 32 + 16;
+    static constexpr size_t kFixed = (size_t)2 * W * 8 * (D + 2) * 4 + 2 * 32 + 96 + 1024;
     static constexpr int kRaw = (int)((kBudget - kFixed) / kStage);
     static constexpr int kStages = kRaw > 8 ? 8 : kRaw;
     static_assert(kStages >= 2, "ring too shallow");
@@ -136,7 +137,7 @@ __device__ __forceinline__ uint32_t swz(int chunk, int row, size_t box_bytes) {
 // producer warp: same item pipeline as the CUDA-core kernel, four blocks per
 // stage, tiled TMA
 // ---------------------------------------------------------------------------
-template <int D, typename T, int R>
+template <int D, typename T, int R, int W>
 __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned char *sk,
                                                  unsigned char *sv, unsigned char *sq,
                                                  StageMeta *meta, uint64_t *full, uint64_t *empty,
@@ -151,47 +152,22 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
     const unsigned n_items = P.hdr->n_items;
     const unsigned Hkv = (unsigned)P.num_kv_heads;
     const int G = P.G;
-    const int PB = P.part_tokens / kBlock;
     const uint64_t policy = l2_evict_first_policy();
 
-    auto claim = [&]() -> unsigned {
-        return lane == 0 ? gridDim.x + atomicAdd(&P.hdr->counter, 1u) : 0u;
-    };
-    auto bcast = [&](unsigned v) -> unsigned { return __shfl_sync(0xffffffffu, v, 0); };
-    auto load_entry = [&](unsigned c) -> int4 {
-        return c < n_items ? P.items[c / Hkv] : make_int4(0, 0, 0, 0);
-    };
-    auto load_tab = [&](unsigned c, int4 e) -> int {
-        const int nblk = (e.z + kBlock - 1) / kBlock;
-        if (c < n_items && lane < nblk)
-            return __ldg(&P.block_tables[(size_t)e.x * P.max_blocks_per_seq + (size_t)e.y * PB +
-                                         lane]);
-        return -1;
-    };
-
-    // Software pipeline over items: claim (atomic) -> entry load -> table
-    // load -> copy issue, each stage one item ahead of the next, so the
-    // latencies of the dependent loads overlap the previous item's copies.
-    // CTA b's first item is item b (no atomic).
-    unsigned cA = blockIdx.x;
-    int4 eA = load_entry(cA);
-    int tA = load_tab(cA, eA);
-    unsigned cB = bcast(claim());
-    int4 eB = load_entry(cB);
-    unsigned raw = claim();
+    ItemPipe items;
+    items.init(P, n_items, lane);
 
     uint32_t k = 0;
     bool aborted = false;
-    while (cA < n_items) {
-        const int tB = load_tab(cB, eB);
-        const unsigned cC = bcast(raw);
-        const int4 eC = load_entry(cC);
-        raw = claim();
+    while (items.valid()) {
+        const unsigned cA = items.cX;
+        const int4 eA = items.eX;
+        const int tA = items.tX;
 
         const int s = eA.x, part = eA.y, ntok = eA.z, nparts = eA.w;
         const int hk = (int)(cA % Hkv);
         const int nblk = (ntok + kBlock - 1) / kBlock;
-        const int nst = (nblk + kBPS - 1) / kBPS;
+        const int nst = (nblk + W - 1) / W;
         for (int st = 0; st < nst; ++st, ++k) {
             const int slot = (int)(k % R);
             bool ok = true;
@@ -200,12 +176,12 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
                 aborted = true;
                 break;
             }
-            const int j0 = st * kBPS;
-            const int nb = min(kBPS, nblk - j0);
-            int phys[kBPS];
+            const int j0 = st * W;
+            const int nb = min(W, nblk - j0);
+            int phys[W];
             unsigned bad = 0;  // blocks with an out-of-range id are skipped
 #pragma unroll
-            for (int b = 0; b < kBPS; ++b) {
+            for (int b = 0; b < W; ++b) {
                 phys[b] = __shfl_sync(0xffffffffu, tA, min(j0 + b, 31));
                 if (b < nb && (phys[b] < 0 || phys[b] >= P.num_blocks)) bad |= 1u << b;
             }
@@ -221,25 +197,24 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
             }
             __syncwarp();
             // one copy per lane: lane 2b fetches block b's K tile, lane 2b+1 its
-            // V tile (both 64-element halves in one 3-D box); lane 2*kBPS the
+            // V tile (both 64-element halves in one 3-D box); lane 2*W the
             // item's query rows
             if (lane < 2 * nb && !((bad >> (lane >> 1)) & 1u)) {
                 const int b = lane >> 1;
-                const size_t off = (size_t)(slot * kBPS + b) * KB * kBoxBytes;
+                const size_t off = (size_t)(slot * W + b) * KB * kBoxBytes;
                 const int y = (phys[b] * P.num_kv_heads + hk) * kBlock;
                 if (lane & 1)
                     tma_load_3d(sv + off, &P.tmap_v, 0, y, 0, &full[slot], policy);
                 else
                     tma_load_3d(sk + off, &P.tmap_k, 0, y, 0, &full[slot], policy);
             }
-            if (st == 0 && lane == 2 * kBPS)
+            if (st == 0 && lane == 2 * W)
                 tma_load_3d(sq + (size_t)slot * KB * kQBoxBytes, &P.tmap_q, 0,
                             s * P.num_heads + hk * G, 0, &full[slot], policy);
             __syncwarp();
         }
         if (aborted) break;
-        cA = cB; eA = eB; tA = tB;
-        cB = cC; eB = eC;
+        items.advance();
     }
     if (!aborted) {
         const int slot = (int)(k % R);
@@ -272,7 +247,7 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
 // ---------------------------------------------------------------------------
 // consumer warps: warp w takes block w of every stage
 // ---------------------------------------------------------------------------
-template <int D, typename T, int R>
+template <int D, typename T, int R, int W>
 __device__ __forceinline__ void run_consumer_mma(const DecodeParams &P, unsigned char *sk,
                                                  unsigned char *sv, const unsigned char *sq,
                                                  const StageMeta *meta, uint64_t *full,
@@ -343,8 +318,8 @@ __device__ __forceinline__ void run_consumer_mma(const DecodeParams &P, unsigned
         const int vb = min(kBlock, max(0, mt.nvalid - cw * kBlock));  // my block's tokens
         const bool mine = vb > 0 && !(((unsigned)mt.flags >> (8 + cw)) & 1u);
         if (mine) {
-            unsigned char *kt = sk + (size_t)(slot * kBPS + cw) * KB * kBoxBytes;
-            unsigned char *vt = sv + (size_t)(slot * kBPS + cw) * KB * kBoxBytes;
+            unsigned char *kt = sk + (size_t)(slot * W + cw) * KB * kBoxBytes;
+            unsigned char *vt = sv + (size_t)(slot * W + cw) * KB * kBoxBytes;
             if (vb < kBlock) {  // zero the V rows past the sequence's end
                 for (int i = lane; i < (kBlock - vb) * KB * 8; i += 32) {
                     const int row = vb + i / (KB * 8), rest = i % (KB * 8);
@@ -417,15 +392,15 @@ __device__ __forceinline__ void run_consumer_mma(const DecodeParams &P, unsigned
         lq += __shfl_xor_sync(0xffffffffu, lq, 2);
         int buf;
         if (!take_buffer(buf)) return;
-        float *acc_b = s_acc + (size_t)buf * kNCW * 8 * D;
+        float *acc_b = s_acc + (size_t)buf * W * 8 * D;
         if (g < G) {
             float *dst = acc_b + ((size_t)cw * 8 + g) * D + 2 * t;
 #pragma unroll
             for (int n = 0; n < NT; ++n)
                 *reinterpret_cast<float2 *>(dst + 8 * n) = make_float2(o[n][0], o[n][1]);
             if (t == 0) {
-                s_m[(buf * kNCW + cw) * 8 + g] = m_run;
-                s_l[(buf * kNCW + cw) * 8 + g] = lq;
+                s_m[(buf * W + cw) * 8 + g] = m_run;
+                s_l[(buf * W + cw) * 8 + g] = lq;
             }
         }
         if (cw == 0 && lane == 0) {
@@ -443,7 +418,7 @@ __device__ __forceinline__ void run_consumer_mma(const DecodeParams &P, unsigned
 // epilogue warp: merge the four consumer warps' states of each item and write
 // the output row (one partition) or the partition's partial state
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, int W>
 __device__ __forceinline__ void run_epilogue_mma(const DecodeParams &P, uint64_t *acc_full,
                                                  uint64_t *acc_empty, const float *s_acc,
                                                  const float *s_m, const float *s_l,
@@ -462,16 +437,16 @@ __device__ __forceinline__ void run_epilogue_mma(const DecodeParams &P, uint64_t
         }
         const ItemInfo it = info[buf];
         if (it.flags & kEndFlag) return;
-        const float *acc_b = s_acc + (size_t)buf * kNCW * 8 * D;
-        const float *m_b = s_m + buf * kNCW * 8, *l_b = s_l + buf * kNCW * 8;
+        const float *acc_b = s_acc + (size_t)buf * W * 8 * D;
+        const float *m_b = s_m + buf * W * 8, *l_b = s_l + buf * W * 8;
         for (int gg = 0; gg < G; ++gg) {
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kNCW; ++w) M = fmaxf(M, m_b[w * 8 + gg]);
+            for (int w = 0; w < W; ++w) M = fmaxf(M, m_b[w * 8 + gg]);
             const float Ms = M == -INFINITY ? 0.f : M;
-            float cf[kNCW], Lsum = 0.f;
+            float cf[W], Lsum = 0.f;
 #pragma unroll
-            for (int w = 0; w < kNCW; ++w) {
+            for (int w = 0; w < W; ++w) {
                 cf[w] = ex2(m_b[w * 8 + gg] - Ms);
                 Lsum += l_b[w * 8 + gg] * cf[w];
             }
@@ -480,7 +455,7 @@ __device__ __forceinline__ void run_epilogue_mma(const DecodeParams &P, uint64_t
             for (int d = lane; d < D; d += 32) {
                 float ov = 0.f;
 #pragma unroll
-                for (int w = 0; w < kNCW; ++w) ov += acc_b[((size_t)w * 8 + gg) * D + d] * cf[w];
+                for (int w = 0; w < W; ++w) ov += acc_b[((size_t)w * 8 + gg) * D + d] * cf[w];
                 if (it.nparts == 1)
                     store_out(P.out, P.out_dtype, ((size_t)it.s * H + h) * D + d,
                               Lsum > 0.f ? ov / Lsum : 0.f);
@@ -497,11 +472,11 @@ __device__ __forceinline__ void run_epilogue_mma(const DecodeParams &P, uint64_t
     }
 }
 
-template <int D, typename T, int R, int MINB>
-__global__ void __launch_bounds__(kThreadsMma, MINB)
+template <int D, typename T, int R, int MINB, int W>
+__global__ void __launch_bounds__(threads_mma<W>(), MINB)
     paged_decode_mma_kernel(const __grid_constant__ DecodeParams P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    using L = LayoutMma<D, R>;
+    using L = LayoutMma<D, R, W>;
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     unsigned char *sk = smem + L::k_off;
@@ -522,10 +497,10 @@ __global__ void __launch_bounds__(kThreadsMma, MINB)
     if (threadIdx.x == 0) {
         for (int r = 0; r < R; ++r) {
             mbar_init(&full[r], 1);
-            mbar_init(&empty[r], kNCW);
+            mbar_init(&empty[r], W);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], kNCW * 32);
+            mbar_init(&acc_full[b], W * 32);
             mbar_init(&acc_empty[b], 32);
         }
         *abort_flag = 0;
@@ -533,12 +508,12 @@ __global__ void __launch_bounds__(kThreadsMma, MINB)
     }
     __syncthreads();
     if (warp == 0)
-        run_producer_mma<D, T, R>(P, sk, sv, sq, meta, full, empty, abort_flag, lane);
-    else if (warp <= kNCW)
-        run_consumer_mma<D, T, R>(P, sk, sv, sq, meta, full, empty, acc_full, acc_empty, s_acc,
+        run_producer_mma<D, T, R, W>(P, sk, sv, sq, meta, full, empty, abort_flag, lane);
+    else if (warp <= W)
+        run_consumer_mma<D, T, R, W>(P, sk, sv, sq, meta, full, empty, acc_full, acc_empty, s_acc,
                                   s_m, s_l, info, abort_flag, warp - 1, lane);
     else
-        run_epilogue_mma<D>(P, acc_full, acc_empty, s_acc, s_m, s_l, info, abort_flag, lane);
+        run_epilogue_mma<D, W>(P, acc_full, acc_empty, s_acc, s_m, s_l, info, abort_flag, lane);
 }
 
 }  // namespace pa
