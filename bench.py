@@ -247,6 +247,60 @@ def run_reference(args, wl, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def layout_sweep(args, wl, dev):
+    """Attention-call time on one workload in three layouts: the paged pool
+    with scattered blocks, the paged pool with each sequence's blocks in
+    order, and a contiguous cache [S][Hkv][rows][D] read without a table."""
+    import torch
+    import paged_kv_cache_pa_gb300 as pa
+    from paged_kv_cache_pa_gb300 import synthetic
+    S, H, Hkv, D = wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim
+    b_attn = algorithmic_bytes(wl)[0]
+    out = torch.empty(S, H, D, dtype=torch.float32, device=dev)
+    ws = torch.empty(pa.decode_workspace_size(S, H, Hkv, D, wl.max_context_len),
+                     dtype=torch.uint8, device=dev)
+    lens = torch.as_tensor(wl.context_lens, device=dev)
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / args.steps
+
+    res = {}
+    for name, w in (("paged_scattered", wl), ("paged_in_order", synthetic.in_order(wl))):
+        vals = synthetic.make_values(w, device=dev)
+        tables = torch.as_tensor(w.block_tables, device=dev)
+        ms = timed(lambda: pa.decode_attention(vals["q"], vals["k_cache"], vals["v_cache"], tables,
+                                               lens, w.max_context_len, w.scale, out=out,
+                                               workspace=ws))
+        res[name] = {"ms_per_call": round(ms, 4), "GBps": round(b_attn / (ms * 1e-3) / 1e9, 1)}
+        del vals
+        torch.cuda.empty_cache()
+    rows = int(-(-wl.max_context_len // 16) * 16)
+    dt = synthetic._torch_dtype(wl.dtype)
+    g = torch.Generator(device=dev).manual_seed(wl.seed)
+    q = torch.randn(S, H, D, generator=g, device=dev).to(dt)
+    kc = torch.randn(S, Hkv, rows, D, generator=g, device=dev).to(dt)
+    vc = torch.randn(S, Hkv, rows, D, generator=g, device=dev).to(dt)
+    ms = timed(lambda: pa.decode_attention_contiguous(q, kc, vc, lens, wl.max_context_len,
+                                                      wl.scale, out=out, workspace=ws))
+    res["contiguous"] = {"ms_per_call": round(ms, 4), "GBps": round(b_attn / (ms * 1e-3) / 1e9, 1)}
+    base = res["contiguous"]["ms_per_call"]
+    for v in res.values():
+        v["time_vs_contiguous"] = round(v["ms_per_call"] / base, 4)
+    print(json.dumps({"layout_sweep": args.config, "workload": WORKLOADS.get(args.config),
+                      "steps": args.steps, "algorithmic_bytes": int(b_attn), "results": res}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -259,6 +313,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layout-sweep", action="store_true",
+                    help="time the attention call with blocks scattered, blocks in order, and "
+                         "on a contiguous (unpaged) cache; prints its own JSON line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -285,6 +342,10 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
+
+    if args.layout_sweep:
+        layout_sweep(args, wl, dev)
+        return
 
     vals = synthetic.make_values(wl, device=dev)
     S, H, Hkv, D = wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim

@@ -165,6 +165,31 @@ pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, const void *que
                                 void *workspace, size_t workspace_bytes,
                                 unsigned int *dev_error_word, pa_stream_t stream);
 
+/*
+ * pa_decode_attention_contiguous -- the same decode attention over a
+ * contiguous (unpaged) KV cache: sequence s's tokens for KV head hk are rows
+ * 0 .. context_lens[s]-1 of k_cache[s][hk] and v_cache[s][hk]; no block
+ * table.  This is the layout a paged cache replaces; the entry point exists
+ * to measure what the table indirection costs on this GPU
+ * [Efficient Memory Management ..., "Kernel-Level Optimizations" (the paged
+ * kernel against FasterTransformer's contiguous one); Paged Attention:
+ * Managing the KV Cache ..., "Attention over scattered blocks" (the same
+ * kernel with and without the table)].
+ *
+ * k_cache, v_cache  device [num_seqs][num_kv_heads][max_rows][head_dim], dtype
+ * max_rows      rows per (sequence, KV head): a multiple of 16, >= max_context_len
+ * Every other argument, the workspace (pa_decode_workspace_size) and the
+ * error behaviour are those of pa_decode_attention.
+ */
+pa_status_t pa_decode_attention_contiguous(void *out, pa_dtype_t out_dtype, const void *query,
+                                           const void *k_cache, const void *v_cache,
+                                           int max_rows, const int32_t *context_lens,
+                                           int max_context_len, int num_seqs, int num_heads,
+                                           int num_kv_heads, int head_dim, float scale,
+                                           pa_dtype_t dtype, void *workspace,
+                                           size_t workspace_bytes,
+                                           unsigned int *dev_error_word, pa_stream_t stream);
+
 /* Size of the workspace array built into the library for
  * pa_decode_attention_noalloc (32 MiB on every GPU that loads the library). */
 #define PA_NOALLOC_WORKSPACE_BYTES (32u << 20)

@@ -21,7 +21,8 @@ import os
 import threading
 from typing import Optional, Sequence
 
-__all__ = ["cache_write", "decode_attention", "decode_workspace_size", "decode_partition_tokens", "copy_blocks",
+__all__ = ["cache_write", "decode_attention", "decode_attention_contiguous",
+           "decode_workspace_size", "decode_partition_tokens", "copy_blocks",
            "status_string", "PaError", "library_path", "load_library", "BLOCK_SIZE",
            "ERRBIT_BLOCK_OOB", "ERRBIT_SLOT_OOB", "ERRBIT_CONTEXT_LEN", "ERRBIT_TIMEOUT",
            "MAX_LAYERS"]
@@ -44,6 +45,8 @@ _SIGNATURES = {
     "pa_decode_partition_tokens": (_I, [_I, _I, _I]),
     "pa_decode_attention": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I,
                                  ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P]),
+    "pa_decode_attention_contiguous": (_I, [_P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
+                                            ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P]),
     "pa_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -177,6 +180,34 @@ def decode_attention(query, k_cache, v_cache, block_tables, context_lens,
         workspace.numel() * workspace.element_size(), _opt_ptr(error_word, "error_word"),
         _stream_ptr(stream, query.device))
     _check(st, "pa_decode_attention")
+    return out
+
+
+def decode_attention_contiguous(query, k_cache, v_cache, context_lens, max_context_len: int,
+                                scale: float, out=None, out_dtype=None, workspace=None,
+                                error_word=None, stream=None):
+    """Decode attention over a contiguous (unpaged) cache
+    k_cache / v_cache [S][Hkv][max_rows][D] (max_rows a multiple of 16); the
+    baseline that measures what the block table costs."""
+    import torch
+    S, H, D = query.shape
+    s2, hkv, rows, d2 = k_cache.shape
+    if s2 != S or d2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("cache shape mismatch")
+    if context_lens.dtype != torch.int32 or context_lens.shape != (S,):
+        raise TypeError("context_lens must be int32 [S]")
+    if out is None:
+        out = torch.empty(S, H, D, dtype=out_dtype or torch.float32, device=query.device)
+    if workspace is None:
+        nbytes = decode_workspace_size(S, H, hkv, D, int(max_context_len))
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=query.device)
+    st = load_library().pa_decode_attention_contiguous(
+        _dev(out, "out"), _dtype_code(out.dtype), _dev(query, "query"), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), rows, _dev(context_lens, "context_lens"), int(max_context_len),
+        S, H, hkv, D, float(scale), _dtype_code(query.dtype), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _opt_ptr(error_word, "error_word"),
+        _stream_ptr(stream, query.device))
+    _check(st, "pa_decode_attention_contiguous")
     return out
 
 

@@ -75,6 +75,9 @@ struct DecodeParams {
     const void *v_cache;
     const int32_t *block_tables;
     int max_blocks_per_seq;
+    // 0: paged pools reached through block_tables.  > 0: contiguous caches
+    // [num_seqs][num_kv_heads][contig_rows][head_dim], no table.
+    int contig_rows;
     const int32_t *context_lens;
     int max_context_len;
     int num_seqs, num_heads, num_kv_heads, G, head_dim, num_blocks;
@@ -173,6 +176,7 @@ struct ItemPipe {
     }
     __device__ __forceinline__ int table(unsigned c, int4 e) const {
         const int nblk = (e.z + kBlock - 1) / kBlock;
+        if (P->contig_rows) return 0;  // contiguous cache: no table
         if (c < n_items && lane < nblk)
             return __ldg(&P->block_tables[(size_t)e.x * P->max_blocks_per_seq + (size_t)e.y * PB +
                                           lane]);
@@ -249,7 +253,7 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
                 break;
             }
             const int phys = __shfl_sync(0xffffffffu, tA, j);
-            const bool bad = phys < 0 || phys >= P.num_blocks;
+            const bool bad = !P.contig_rows && (phys < 0 || phys >= P.num_blocks);
             const int nvalid = bad ? 0 : min(kBlock, ntok - j * kBlock);  // bad: skip the block
             const uint32_t kv_bytes = (uint32_t)nvalid * D * (uint32_t)sizeof(T);
             const uint32_t q_bytes = j == 0 ? (uint32_t)(G * D * sizeof(T)) : 0u;
@@ -264,7 +268,11 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
             __syncwarp();
             // one copy per lane: K rows (lane 0), V rows (lane 1), query (lane 2)
             if (lane < 2 && kv_bytes) {
-                const size_t off = ((size_t)phys * Hkv + hk) * kTile;
+                const size_t off =
+                    P.contig_rows
+                        ? (((size_t)s * Hkv + hk) * P.contig_rows +
+                           (size_t)(part * (P.part_tokens / kBlock) + j) * kBlock) * D
+                        : ((size_t)phys * Hkv + hk) * kTile;
                 bulk_g2s((lane ? sv : sk) + slot * kTile, (lane ? vc : kc) + off, kv_bytes,
                          &full[slot], policy);
             }

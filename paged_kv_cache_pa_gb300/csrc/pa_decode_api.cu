@@ -320,28 +320,41 @@ extern "C" int pa_decode_partition_tokens(int num_seqs, int num_kv_heads, int ma
     return choose_part_tokens(num_seqs, num_kv_heads, max_context_len);
 }
 
-extern "C" pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, const void *query,
-                                           const void *k_cache, const void *v_cache,
-                                           const int32_t *block_tables, int max_blocks_per_seq,
-                                           const int32_t *context_lens, int max_context_len,
-                                           int num_seqs, int num_heads, int num_kv_heads,
-                                           int head_dim, int num_blocks, float scale,
-                                           pa_dtype_t dtype, void *workspace,
-                                           size_t workspace_bytes, unsigned int *dev_error_word,
-                                           pa_stream_t stream) {
-    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
-        max_blocks_per_seq <= 0 || max_context_len < 0)
+namespace {
+
+// Shared implementation of the paged (contig_rows == 0) and contiguous
+// (contig_rows > 0) entry points.
+pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, const void *k_cache,
+                        const void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                        int contig_rows, const int32_t *context_lens, int max_context_len,
+                        int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                        int num_blocks, float scale, pa_dtype_t dtype, void *workspace,
+                        size_t workspace_bytes, unsigned int *dev_error_word,
+                        pa_stream_t stream) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0)
         return PA_ERR_INVALID_ARG;
     if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
     if (out_dtype != PA_F32 && out_dtype != dtype) return PA_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
     if (num_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
-    if ((long long)max_context_len > (long long)PA_BLOCK_SIZE * max_blocks_per_seq)
-        return PA_ERR_INVALID_ARG;
+    // rows of the pool viewed as [rows][head_dim] (row coordinates are 32-bit)
+    unsigned long long pool_rows;
+    if (contig_rows == 0) {
+        if (num_blocks <= 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+        if ((long long)max_context_len > (long long)PA_BLOCK_SIZE * max_blocks_per_seq)
+            return PA_ERR_INVALID_ARG;
+        pool_rows = (unsigned long long)num_blocks * num_kv_heads * PA_BLOCK_SIZE;
+    } else {
+        if (contig_rows < 0 || contig_rows % PA_BLOCK_SIZE != 0 || max_context_len > contig_rows)
+            return PA_ERR_INVALID_ARG;
+        pool_rows = (unsigned long long)num_seqs * num_kv_heads * contig_rows;
+    }
+    if (pool_rows >= (1ull << 31)) return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PA_OK;
-    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+    if (!out || !query || !k_cache || !v_cache || !context_lens || !workspace)
         return PA_ERR_INVALID_ARG;
+    if (contig_rows == 0 && !block_tables) return PA_ERR_INVALID_ARG;
     if (!aligned(out, 16) || !aligned(query, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
         return PA_ERR_INVALID_ARG;
     if (!aligned(workspace, 256)) return PA_ERR_WORKSPACE;
@@ -352,8 +365,6 @@ extern "C" pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, cons
     DecodeParams P;
     memset(&P, 0, sizeof(P));
     if (uses_tensor_cores(num_heads / num_kv_heads, head_dim)) {
-        const unsigned long long pool_rows =
-            (unsigned long long)num_blocks * num_kv_heads * PA_BLOCK_SIZE;
         if (!encode_rows(&P.tmap_q, query, dtype, (unsigned long long)num_seqs * num_heads,
                          head_dim, 8) ||
             !encode_rows(&P.tmap_k, k_cache, dtype, pool_rows, head_dim, PA_BLOCK_SIZE) ||
@@ -367,6 +378,7 @@ extern "C" pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, cons
     P.v_cache = v_cache;
     P.block_tables = block_tables;
     P.max_blocks_per_seq = max_blocks_per_seq;
+    P.contig_rows = contig_rows;
     P.context_lens = context_lens;
     P.max_context_len = max_context_len;
     P.num_seqs = num_seqs;
@@ -417,4 +429,33 @@ extern "C" pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, cons
         if (e != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, const void *query,
+                                           const void *k_cache, const void *v_cache,
+                                           const int32_t *block_tables, int max_blocks_per_seq,
+                                           const int32_t *context_lens, int max_context_len,
+                                           int num_seqs, int num_heads, int num_kv_heads,
+                                           int head_dim, int num_blocks, float scale,
+                                           pa_dtype_t dtype, void *workspace,
+                                           size_t workspace_bytes, unsigned int *dev_error_word,
+                                           pa_stream_t stream) {
+    return decode_impl(out, out_dtype, query, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                       0, context_lens, max_context_len, num_seqs, num_heads, num_kv_heads,
+                       head_dim, num_blocks, scale, dtype, workspace, workspace_bytes,
+                       dev_error_word, stream);
+}
+
+extern "C" pa_status_t pa_decode_attention_contiguous(
+    void *out, pa_dtype_t out_dtype, const void *query, const void *k_cache, const void *v_cache,
+    int max_rows, const int32_t *context_lens, int max_context_len, int num_seqs, int num_heads,
+    int num_kv_heads, int head_dim, float scale, pa_dtype_t dtype, void *workspace,
+    size_t workspace_bytes, unsigned int *dev_error_word, pa_stream_t stream) {
+    if (max_rows <= 0) return PA_ERR_INVALID_ARG;
+    return decode_impl(out, out_dtype, query, k_cache, v_cache, nullptr, 0, max_rows,
+                       context_lens, max_context_len, num_seqs, num_heads, num_kv_heads,
+                       head_dim, 0, scale, dtype, workspace, workspace_bytes, dev_error_word,
+                       stream);
 }

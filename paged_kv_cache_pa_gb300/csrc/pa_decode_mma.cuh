@@ -183,7 +183,8 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
 #pragma unroll
             for (int b = 0; b < W; ++b) {
                 phys[b] = __shfl_sync(0xffffffffu, tA, min(j0 + b, 31));
-                if (b < nb && (phys[b] < 0 || phys[b] >= P.num_blocks)) bad |= 1u << b;
+                if (b < nb && !P.contig_rows && (phys[b] < 0 || phys[b] >= P.num_blocks))
+                    bad |= 1u << b;
             }
             if (lane == 0) {
                 if (bad && P.err) atomicOr(P.err, PA_ERRBIT_BLOCK_OOB);
@@ -202,7 +203,10 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
             if (lane < 2 * nb && !((bad >> (lane >> 1)) & 1u)) {
                 const int b = lane >> 1;
                 const size_t off = (size_t)(slot * W + b) * KB * kBoxBytes;
-                const int y = (phys[b] * P.num_kv_heads + hk) * kBlock;
+                const int y = P.contig_rows
+                                  ? (s * P.num_kv_heads + hk) * P.contig_rows +
+                                        (part * (P.part_tokens / kBlock) + j0 + b) * kBlock
+                                  : (phys[b] * P.num_kv_heads + hk) * kBlock;
                 if (lane & 1)
                     tma_load_3d(sv + off, &P.tmap_v, 0, y, 0, &full[slot], policy);
                 else

@@ -226,6 +226,20 @@ def make_beams(seed: Optional[int] = None, groups: int = 32, beams: int = 6,
                           "logical_blocks": float(logical), "cow_pairs": float(len(pairs))})
 
 
+def in_order(wl: Workload) -> Workload:
+    """The same workload with every sequence's blocks laid out consecutively
+    in the pool (sequence 0's blocks first), for comparing placements."""
+    lens = wl.context_lens.astype(np.int64)
+    need = int(sum(blocks_for(int(L)) for L in lens))
+    ids = np.arange(need, dtype=np.int64)
+    tables = _deal_tables(lens, ids, wl.max_blocks_per_seq)
+    return Workload(name=wl.name + "-inorder", num_seqs=wl.num_seqs, num_heads=wl.num_heads,
+                    num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim, dtype=wl.dtype,
+                    num_blocks=max(need, 1), context_lens=wl.context_lens.copy(),
+                    block_tables=tables, slot_mapping=_slots_of_last(tables, lens),
+                    seed=wl.seed, scale=wl.scale, used_blocks=ids, info=dict(wl.info))
+
+
 MAKERS = {"tiny": make_tiny, "opt13b": make_opt13b, "gqa": make_gqa, "beams": make_beams,
           "long": make_long}
 

@@ -261,3 +261,49 @@ def test_host_detected_errors():
     with pytest.raises(pa.PaError) as ei:
         pa.decode_attention(q96, k96, k96, t, ln, 16, 0.1)
     assert ei.value.status == 2
+
+
+# ---------------------------------------------------------------------------
+# contiguous (unpaged) cache: the layout the block table replaces
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("H,Hkv,D,dtype", [(8, 8, 128, "f16"), (12, 2, 128, "bf16"),
+                                           (8, 2, 64, "f16"), (4, 4, 256, "bf16")])
+def test_contiguous_cache_matches_oracle(H, Hkv, D, dtype):
+    import oracle
+    lens = np.array([1, 15, 16, 17, 100, 513, 1000, 1025], np.int32)
+    S = len(lens)
+    rows = int(-(-lens.max() // 16) * 16) + 16
+    tdt = torch.float16 if dtype == "f16" else torch.bfloat16
+    g = torch.Generator(device=DEV).manual_seed(H * 31 + D)
+    q = torch.randn(S, H, D, generator=g, device=DEV).to(tdt)
+    kc = torch.randn(S, Hkv, rows, D, generator=g, device=DEV).to(tdt)
+    vc = torch.randn(S, Hkv, rows, D, generator=g, device=DEV).to(tdt)
+    pos = torch.arange(rows, device=DEV)
+    live = pos[None, :] < torch.as_tensor(lens, device=DEV)[:, None]          # [S][rows]
+    nan = torch.tensor(float("nan"), dtype=tdt, device=DEV)
+    kc = torch.where(live[:, None, :, None], kc, nan).contiguous()            # poison past L
+    vc = torch.where(live[:, None, :, None], vc, nan).contiguous()
+    err = _err_word()
+    out = pa.decode_attention_contiguous(q, kc, vc, torch.as_tensor(lens, device=DEV),
+                                         int(lens.max()), 1.0 / np.sqrt(D), error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    # host: the same rows as a paged pool (sequence s's block j -> block s*nb + j)
+    nb = rows // 16
+
+    def pool(c):
+        return codes(c).reshape(S, Hkv, nb, 16, D).transpose(0, 2, 1, 3, 4).reshape(
+            S * nb, Hkv, 16, D).copy()
+    tables = (np.arange(S)[:, None] * nb + np.arange(nb)[None, :]).astype(np.int32)
+    want = oracle.decode_attention(codes(q), pool(kc), pool(vc), tables, lens, 1.0 / np.sqrt(D),
+                                   dtype)
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    assert max_abs(got, want) <= ATOL
+
+
+def test_in_order_placement_gives_the_same_output():
+    wl = synthetic.in_order(synthetic.make("gqa"))
+    got, want = _run_and_check(wl)
+    assert max_abs(got, want) <= ATOL
