@@ -12,7 +12,8 @@ header of ``pa_oracle.c``.  In short:
 * ``half_to_double`` / ``double_to_half``: IEEE binary16 and bfloat16 from
   their bit layouts, round-to-nearest-even on encode.
 * ``cache_write``: byte copy of every new token's K/V rows into the pool slot
-  named by ``slot_mapping`` (block ``slot // 16``, offset ``slot % 16``).
+  named by ``slot_mapping`` (block ``slot // B``, offset ``slot % B``, with B
+  the pool's block size, its third dimension).
 * ``copy_blocks``: byte copy of block ``src`` onto block ``dst`` in every
   layer's K and V pool.
 * ``decode_attention``: softmax(scale * q.K^T) V over the sequence's
@@ -41,7 +42,6 @@ _lock = threading.Lock()
 _lib = None
 
 DTYPES = {"f16": 0, "bf16": 1}
-BLOCK = 16
 
 
 def build(force: bool = False) -> str:
@@ -73,17 +73,17 @@ def _load():
             lib.pa_oracle_decode_halves.argtypes = [P, P, ctypes.c_int64, I]
             lib.pa_oracle_encode_halves.argtypes = [P, P, ctypes.c_int64, I]
             lib.pa_oracle_cache_write.restype = I
-            lib.pa_oracle_cache_write.argtypes = [P, P, P, P, P, I, I, I, I]
+            lib.pa_oracle_cache_write.argtypes = [P, P, P, P, P, I, I, I, I, I]
             lib.pa_oracle_copy_blocks.restype = I
-            lib.pa_oracle_copy_blocks.argtypes = [P, P, I, P, I, I, I, I]
-            attn = [P, P, P, P, P, I, P, I, I, I, I, I, ctypes.c_double, I, I]
+            lib.pa_oracle_copy_blocks.argtypes = [P, P, I, P, I, I, I, I, I]
+            attn = [P, P, P, P, P, I, P, I, I, I, I, I, I, ctypes.c_double, I, I]
             lib.pa_oracle_decode_attention.restype = I
             lib.pa_oracle_decode_attention.argtypes = attn
             lib.pa_oracle_decode_attention_blockwise.restype = I
             lib.pa_oracle_decode_attention_blockwise.argtypes = attn
             lib.pa_oracle_attention_weights.restype = I
             lib.pa_oracle_attention_weights.argtypes = [P, P, P, P, P, P, I, P, I, I, I, I, I,
-                                                        ctypes.c_double, I]
+                                                        I, ctypes.c_double, I]
             _lib = lib
     return _lib
 
@@ -137,7 +137,7 @@ def double_to_half(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def cache_write(key, value, k_cache, v_cache, slot_mapping) -> None:
-    """In place on k_cache / v_cache ([num_blocks][Hkv][16][D] 16-bit codes).
+    """In place on k_cache / v_cache ([num_blocks][Hkv][B][D] 16-bit codes).
     key / value: [num_tokens][Hkv][D]."""
     key, value = _u16(key), _u16(value)
     kc, vc = _u16(k_cache), _u16(v_cache)
@@ -145,9 +145,9 @@ def cache_write(key, value, k_cache, v_cache, slot_mapping) -> None:
         raise ValueError("pools must be contiguous 16-bit arrays (written in place)")
     slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     nb, hkv, bs, d = kc.shape
-    assert bs == BLOCK and key.shape[1:] == (hkv, d)
+    assert key.shape[1:] == (hkv, d) and vc.shape == kc.shape
     _check(_load().pa_oracle_cache_write(_ptr(key), _ptr(value), _ptr(kc), _ptr(vc),
-                                         _ptr(slots), key.shape[0], nb, hkv, d))
+                                         _ptr(slots), key.shape[0], nb, hkv, d, bs))
 
 
 def copy_blocks(k_caches, v_caches, block_pairs) -> None:
@@ -163,7 +163,7 @@ def copy_blocks(k_caches, v_caches, block_pairs) -> None:
     vp = (ctypes.c_void_p * len(vs))(*[_ptr(v) for v in vs])
     _check(_load().pa_oracle_copy_blocks(ctypes.cast(kp, ctypes.c_void_p),
                                          ctypes.cast(vp, ctypes.c_void_p), len(ks),
-                                         _ptr(pairs), pairs.shape[0], nb, hkv, d))
+                                         _ptr(pairs), pairs.shape[0], nb, hkv, d, bs))
 
 
 def _attn_args(q, k_cache, v_cache, block_tables, context_lens):
@@ -172,20 +172,20 @@ def _attn_args(q, k_cache, v_cache, block_tables, context_lens):
     cl = np.ascontiguousarray(context_lens, dtype=np.int32)
     s, h, d = q.shape
     nb, hkv, bs, d2 = kc.shape
-    assert bs == BLOCK and d2 == d and vc.shape == kc.shape
+    assert d2 == d and vc.shape == kc.shape
     assert bt.ndim == 2 and bt.shape[0] == s and cl.shape == (s,)
-    return q, kc, vc, bt, cl, s, h, d, nb, hkv
+    return q, kc, vc, bt, cl, s, h, d, nb, hkv, bs
 
 
 def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float,
                      dtype: str, nthreads: int | None = None) -> np.ndarray:
     """float64 [S][H][D] output of paged decode attention (token-wise, two-pass)."""
-    q, kc, vc, bt, cl, s, h, d, nb, hkv = _attn_args(q, k_cache, v_cache, block_tables,
+    q, kc, vc, bt, cl, s, h, d, nb, hkv, bs = _attn_args(q, k_cache, v_cache, block_tables,
                                                        context_lens)
     out = np.zeros((s, h, d), np.float64)
     _check(_load().pa_oracle_decode_attention(
         _ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cl), s, h, hkv,
-        d, nb, float(scale), DTYPES[dtype], nthreads or default_threads()))
+        d, nb, bs, float(scale), DTYPES[dtype], nthreads or default_threads()))
     return out
 
 
@@ -193,24 +193,24 @@ def decode_attention_blockwise(q, k_cache, v_cache, block_tables, context_lens,
                                scale: float, dtype: str,
                                nthreads: int | None = None) -> np.ndarray:
     """float64 [S][H][D] output through per-block partial states and a merge."""
-    q, kc, vc, bt, cl, s, h, d, nb, hkv = _attn_args(q, k_cache, v_cache, block_tables,
+    q, kc, vc, bt, cl, s, h, d, nb, hkv, bs = _attn_args(q, k_cache, v_cache, block_tables,
                                                        context_lens)
     out = np.zeros((s, h, d), np.float64)
     _check(_load().pa_oracle_decode_attention_blockwise(
         _ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cl), s, h, hkv,
-        d, nb, float(scale), DTYPES[dtype], nthreads or default_threads()))
+        d, nb, bs, float(scale), DTYPES[dtype], nthreads or default_threads()))
     return out
 
 
 def attention_weights(q, k_cache, v_cache, block_tables, context_lens, scale: float,
                       dtype: str):
     """(out [S][H][D], weights [S][H][max_ctx]) -- weights a_t = w_t / Z, zero past L."""
-    q, kc, vc, bt, cl, s, h, d, nb, hkv = _attn_args(q, k_cache, v_cache, block_tables,
+    q, kc, vc, bt, cl, s, h, d, nb, hkv, bs = _attn_args(q, k_cache, v_cache, block_tables,
                                                        context_lens)
     max_ctx = int(cl.max()) if s else 0
     out = np.zeros((s, h, d), np.float64)
     w = np.zeros((s, h, max(max_ctx, 1)), np.float64)
     _check(_load().pa_oracle_attention_weights(
         _ptr(out), _ptr(w), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cl), s,
-        h, hkv, d, nb, float(scale), DTYPES[dtype]))
+        h, hkv, d, nb, bs, float(scale), DTYPES[dtype]))
     return out, w[:, :, :max_ctx]

@@ -14,7 +14,8 @@
  *
  *   - cache write: for every new token t whose slot s = slot_mapping[t] is
  *     non-negative, the key row of every KV head is copied byte for byte to
- *     pool position (block s/16, head h, offset s%16); same for the value.
+ *     pool position (block s/B, head h, offset s%B) for block size B; same
+ *     for the value.
  *     [Paged Attention: Managing the KV Cache Like Virtual Memory, "A paged KV
  *     cache, in code" (PagedLayer.update writes through blocks/offsets, and the
  *     closing note on the slot mapping that says where each token's keys and
@@ -29,7 +30,7 @@
  *
  *   - decode attention: for sequence s and query head h (KV head h / G with
  *     G = num_heads / num_kv_heads, consecutive grouping), token t of the
- *     context lives at block_tables[s][t/16], offset t%16.  With
+ *     context lives at block_tables[s][t/B], offset t%B.  With
  *     x_t = scale * sum_d q[d] k_t[d], the output is
  *        o = sum_t exp(x_t - m) v_t / sum_t exp(x_t - m),   m = max_t x_t,
  *     i.e. the standard attention equation (a_ij, o_i) with the caller's scale,
@@ -49,7 +50,13 @@
  *
  * Layouts (all row-major, all caller-owned host memory):
  *   q           [num_seqs][num_heads][head_dim]                  16-bit codes
- *   k/v pools   [num_blocks][num_kv_heads][16][head_dim]          16-bit codes
+ *   k/v pools   [num_blocks][num_kv_heads][B][head_dim]           16-bit codes
+ *
+ * B (block_size) is the number of tokens per block, any positive value: the
+ * method fixes it per cache, not per kernel [Efficient Memory Management ...,
+ * "PagedAttention Algorithm": the KV cache is partitioned into blocks of B
+ * tokens; Paged Attention: Managing the KV Cache ..., benchmark section: the
+ * same attention swept over block sizes].
  *   block_tables[num_seqs][max_blocks_per_seq]                    int32
  *   context_lens[num_seqs]                                        int32
  *   out         [num_seqs][num_heads][head_dim]                   double
@@ -62,8 +69,6 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
-
-#define ORACLE_BLOCK 16
 
 enum { ORACLE_F16 = 0, ORACLE_BF16 = 1 };
 
@@ -149,18 +154,20 @@ void pa_oracle_encode_halves(const double *in, uint16_t *out, int64_t n, int dty
 int pa_oracle_cache_write(const uint16_t *key, const uint16_t *value,
                           uint16_t *k_cache, uint16_t *v_cache,
                           const int64_t *slot_mapping, int num_tokens,
-                          int num_blocks, int num_kv_heads, int head_dim) {
-    if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 1;
+                          int num_blocks, int num_kv_heads, int head_dim, int block_size) {
+    if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0)
+        return 1;
     int rc = 0;
     for (int t = 0; t < num_tokens; ++t) {
         int64_t slot = slot_mapping[t];
         if (slot < 0) continue;                              /* padding token: no slot */
-        if (slot >= (int64_t)num_blocks * ORACLE_BLOCK) { rc = 3; continue; }
-        int64_t blk = slot / ORACLE_BLOCK;
-        int64_t off = slot % ORACLE_BLOCK;
+        if (slot >= (int64_t)num_blocks * block_size) { rc = 3; continue; }
+        int64_t blk = slot / block_size;
+        int64_t off = slot % block_size;
         for (int h = 0; h < num_kv_heads; ++h) {
             size_t src = ((size_t)t * num_kv_heads + h) * head_dim;
-            size_t dst = (((size_t)blk * num_kv_heads + h) * ORACLE_BLOCK + off) * head_dim;
+            size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * head_dim;
             memcpy(k_cache + dst, key + src, sizeof(uint16_t) * head_dim);
             memcpy(v_cache + dst, value + src, sizeof(uint16_t) * head_dim);
         }
@@ -174,9 +181,9 @@ int pa_oracle_cache_write(const uint16_t *key, const uint16_t *value,
 /* ------------------------------------------------------------------------ */
 int pa_oracle_copy_blocks(uint16_t *const *k_caches, uint16_t *const *v_caches, int num_layers,
                           const int64_t *block_pairs, int num_pairs,
-                          int num_blocks, int num_kv_heads, int head_dim) {
-    if (num_layers < 0 || num_pairs < 0 || num_blocks <= 0) return 1;
-    size_t block_elems = (size_t)num_kv_heads * ORACLE_BLOCK * head_dim;
+                          int num_blocks, int num_kv_heads, int head_dim, int block_size) {
+    if (num_layers < 0 || num_pairs < 0 || num_blocks <= 0 || block_size <= 0) return 1;
+    size_t block_elems = (size_t)num_kv_heads * block_size * head_dim;
     int rc = 0;
     for (int l = 0; l < num_layers; ++l) {
         for (int i = 0; i < num_pairs; ++i) {
@@ -199,7 +206,7 @@ typedef struct {
     double *weights;                 /* optional [num_seqs][num_heads][max_ctx] */
     const uint16_t *q, *k_cache, *v_cache;
     const int32_t *block_tables, *context_lens;
-    int max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks;
+    int max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks, block_size;
     int max_ctx, dtype, blockwise;
     double scale;
     int nthreads, tid;
@@ -209,10 +216,11 @@ typedef struct {
 /* Address of token t's row (K or V) of KV head hk in sequence s, or NULL if
  * the table entry is out of range. */
 static const uint16_t *token_row(const attn_job *J, const uint16_t *pool, int s, int hk, int t) {
-    int32_t blk = J->block_tables[(size_t)s * J->max_blocks_per_seq + t / ORACLE_BLOCK];
+    const int B = J->block_size;
+    int32_t blk = J->block_tables[(size_t)s * J->max_blocks_per_seq + t / B];
     if (blk < 0 || blk >= J->num_blocks) return NULL;
-    int off = t % ORACLE_BLOCK;
-    return pool + (((size_t)blk * J->num_kv_heads + hk) * ORACLE_BLOCK + off) * J->head_dim;
+    int off = t % B;
+    return pool + (((size_t)blk * J->num_kv_heads + hk) * B + off) * J->head_dim;
 }
 
 /* Token-wise form: two passes, scores first, then max, exp, sums. */
@@ -262,9 +270,10 @@ static int attend_blockwise(const attn_job *J, int s, int h, double *x, double *
     for (int d = 0; d < D; ++d) qd[d] = pa_oracle_half_to_double(qrow[d], J->dtype);
     for (int d = 0; d < D; ++d) o[d] = 0.0;
     if (L <= 0) return 0;
-    const int nb = (L + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
+    const int B = J->block_size;
+    const int nb = (L + B - 1) / B;
     for (int j = 0; j < nb; ++j) {
-        int t0 = j * ORACLE_BLOCK, t1 = t0 + ORACLE_BLOCK < L ? t0 + ORACLE_BLOCK : L;
+        int t0 = j * B, t1 = t0 + B < L ? t0 + B : L;
         double mj = -INFINITY;
         for (int t = t0; t < t1; ++t) {
             const uint16_t *krow = token_row(J, J->k_cache, s, hk, t);
@@ -302,8 +311,9 @@ static int attend_blockwise(const attn_job *J, int s, int h, double *x, double *
 static void *attn_worker(void *arg) {
     attn_job *J = (attn_job *)arg;
     const int D = J->head_dim;
-    const int maxnb = (J->max_ctx + ORACLE_BLOCK - 1) / ORACLE_BLOCK + 1;
-    double *x = (double *)malloc(sizeof(double) * (size_t)(J->max_ctx > ORACLE_BLOCK ? J->max_ctx : ORACLE_BLOCK));
+    const int B = J->block_size;
+    const int maxnb = (J->max_ctx + B - 1) / B + 1;
+    double *x = (double *)malloc(sizeof(double) * (size_t)(J->max_ctx > B ? J->max_ctx : B));
     double *qd = (double *)malloc(sizeof(double) * (size_t)D);
     double *bm = (double *)malloc(sizeof(double) * (size_t)maxnb);
     double *bl = (double *)malloc(sizeof(double) * (size_t)maxnb);
@@ -328,15 +338,17 @@ static int run_attention(double *out, double *weights, const uint16_t *q,
                          const uint16_t *k_cache, const uint16_t *v_cache,
                          const int32_t *block_tables, int max_blocks_per_seq,
                          const int32_t *context_lens, int num_seqs, int num_heads,
-                         int num_kv_heads, int head_dim, int num_blocks, double scale,
-                         int dtype, int nthreads, int blockwise) {
+                         int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                         double scale, int dtype, int nthreads, int blockwise) {
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
-        num_heads % num_kv_heads != 0 || num_blocks <= 0 || max_blocks_per_seq < 0 ||
+        num_heads % num_kv_heads != 0 || num_blocks <= 0 || block_size <= 0 ||
+        max_blocks_per_seq < 0 ||
         (dtype != ORACLE_F16 && dtype != ORACLE_BF16))
         return 1;
     int max_ctx = 0;
     for (int s = 0; s < num_seqs; ++s) {
-        if (context_lens[s] < 0 || context_lens[s] > max_blocks_per_seq * ORACLE_BLOCK) return 1;
+        if (context_lens[s] < 0 || (int64_t)context_lens[s] > (int64_t)max_blocks_per_seq * block_size)
+            return 1;
         if (context_lens[s] > max_ctx) max_ctx = context_lens[s];
     }
     if (nthreads < 1) nthreads = 1;
@@ -347,7 +359,7 @@ static int run_attention(double *out, double *weights, const uint16_t *q,
     for (int i = 0; i < nthreads; ++i) {
         attn_job J = {out, weights, q, k_cache, v_cache, block_tables, context_lens,
                       max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks,
-                      max_ctx, dtype, blockwise, scale, nthreads, i, 0};
+                      block_size, max_ctx, dtype, blockwise, scale, nthreads, i, 0};
         jobs[i] = J;
     }
     for (int i = 1; i < nthreads; ++i) {
@@ -368,10 +380,10 @@ int pa_oracle_decode_attention(double *out, const uint16_t *q, const uint16_t *k
                                const uint16_t *v_cache, const int32_t *block_tables,
                                int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
                                int num_heads, int num_kv_heads, int head_dim, int num_blocks,
-                               double scale, int dtype, int nthreads) {
+                               int block_size, double scale, int dtype, int nthreads) {
     return run_attention(out, NULL, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                          context_lens, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks,
-                         scale, dtype, nthreads, 0);
+                         block_size, scale, dtype, nthreads, 0);
 }
 
 /* Same as above, also returning the normalised weights a_t = w_t / Z in
@@ -380,20 +392,20 @@ int pa_oracle_attention_weights(double *out, double *weights, const uint16_t *q,
                                 const uint16_t *k_cache, const uint16_t *v_cache,
                                 const int32_t *block_tables, int max_blocks_per_seq,
                                 const int32_t *context_lens, int num_seqs, int num_heads,
-                                int num_kv_heads, int head_dim, int num_blocks, double scale,
-                                int dtype) {
+                                int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                                double scale, int dtype) {
     return run_attention(out, weights, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                          context_lens, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks,
-                         scale, dtype, 1, 0);
+                         block_size, scale, dtype, 1, 0);
 }
 
 int pa_oracle_decode_attention_blockwise(double *out, const uint16_t *q, const uint16_t *k_cache,
                                          const uint16_t *v_cache, const int32_t *block_tables,
                                          int max_blocks_per_seq, const int32_t *context_lens,
                                          int num_seqs, int num_heads, int num_kv_heads,
-                                         int head_dim, int num_blocks, double scale, int dtype,
-                                         int nthreads) {
+                                         int head_dim, int num_blocks, int block_size,
+                                         double scale, int dtype, int nthreads) {
     return run_attention(out, NULL, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                          context_lens, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks,
-                         scale, dtype, nthreads, 1);
+                         block_size, scale, dtype, nthreads, 1);
 }

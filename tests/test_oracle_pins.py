@@ -147,6 +147,95 @@ def test_paged_equals_contiguous_bitwise(oracle_mod):
     assert np.array_equal(a, b)
 
 
+def _relayout(rows_k, rows_v, lens, B, rng):
+    """Store per-sequence token rows ([Hkv][L][D] codes) into a pool of
+    B-token blocks at scattered places; returns (kc, vc, tables)."""
+    S = len(lens)
+    Hkv, D = rows_k[0].shape[0], rows_k[0].shape[2]
+    nbs = [-(-int(L) // B) for L in lens]
+    NB = sum(nbs) + 2
+    perm = rng.permutation(NB)
+    tables = np.full((S, max(max(nbs), 1)), -1, np.int32)
+    kc = rng.integers(0, 1 << 16, (NB, Hkv, B, D), dtype=np.uint16)   # junk outside contexts
+    vc = rng.integers(0, 1 << 16, (NB, Hkv, B, D), dtype=np.uint16)
+    pos = 0
+    for s in range(S):
+        tables[s, :nbs[s]] = perm[pos:pos + nbs[s]]
+        pos += nbs[s]
+        for t in range(int(lens[s])):
+            kc[tables[s, t // B], :, t % B, :] = rows_k[s][:, t, :]
+            vc[tables[s, t // B], :, t % B, :] = rows_v[s][:, t, :]
+    return kc, vc, tables
+
+
+def test_block_size_does_not_change_the_output(oracle_mod):
+    """The block size B is a storage parameter: the same tokens stored in
+    blocks of 1, 3, 8, 16, 32, 64 or 256 tokens give bit-identical outputs
+    (same tokens, same summation order), and match SDPA on the dense rows.
+    A block size hard-coded anywhere (t / 16) fails every B but 16; junk
+    outside the contexts makes a read past L visible."""
+    rng = np.random.default_rng(21)
+    H, Hkv, D, dtype = 6, 2, 16, "bf16"
+    lens = np.array([1, 7, 8, 9, 31, 64, 100, 257], np.int32)
+    q = _codes(rng.standard_normal((len(lens), H, D)), dtype)
+    rows_k = [_codes(rng.standard_normal((Hkv, int(L), D)), dtype) for L in lens]
+    rows_v = [_codes(rng.standard_normal((Hkv, int(L), D)), dtype) for L in lens]
+    outs = {}
+    for B in (1, 3, 8, 16, 32, 64, 256):
+        kc, vc, tables = _relayout(rows_k, rows_v, lens, B, np.random.default_rng(B))
+        outs[B] = oracle_mod.decode_attention(q, kc, vc, tables, lens, 0.3, dtype)
+        bw = oracle_mod.decode_attention_blockwise(q, kc, vc, tables, lens, 0.3, dtype)
+        np.testing.assert_allclose(bw, outs[B], rtol=0, atol=1e-12)
+    for B, o in outs.items():
+        assert np.array_equal(o, outs[16]), B
+    G = H // Hkv
+    for s in range(len(lens)):
+        K = torch.from_numpy(oracle_mod.half_to_double(rows_k[s], dtype)).repeat_interleave(G, 0)
+        V = torch.from_numpy(oracle_mod.half_to_double(rows_v[s], dtype)).repeat_interleave(G, 0)
+        Q = torch.from_numpy(oracle_mod.half_to_double(q[s], dtype))[:, None, :]
+        ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, scale=0.3)[:, 0, :]
+        np.testing.assert_allclose(outs[8][s], ref.numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("B", [8, 64])
+def test_cache_write_at_other_block_sizes(oracle_mod, B):
+    """slot -> (slot // B, slot % B): the written rows are found there, and
+    nothing else in the pool changes."""
+    rng = np.random.default_rng(B)
+    NB, Hkv, D, T = 7, 3, 8, 12
+    kc = rng.integers(0, 1 << 16, (NB, Hkv, B, D), dtype=np.uint16)
+    vc = rng.integers(0, 1 << 16, (NB, Hkv, B, D), dtype=np.uint16)
+    k0, v0 = kc.copy(), vc.copy()
+    key = rng.integers(0, 1 << 16, (T, Hkv, D), dtype=np.uint16)
+    val = rng.integers(0, 1 << 16, (T, Hkv, D), dtype=np.uint16)
+    slots = rng.choice(NB * B, T, replace=False).astype(np.int64)
+    slots[3] = -1
+    oracle_mod.cache_write(key, val, kc, vc, slots)
+    touched = np.zeros((NB, B), bool)
+    for t, sl in enumerate(slots):
+        if sl < 0:
+            continue
+        b, o = divmod(int(sl), B)
+        assert np.array_equal(kc[b, :, o], key[t]) and np.array_equal(vc[b, :, o], val[t])
+        touched[b, o] = True
+    keep = ~touched[:, None, :, None].repeat(Hkv, 1).repeat(D, 3)
+    assert np.array_equal(kc[keep], k0[keep]) and np.array_equal(vc[keep], v0[keep])
+
+
+def test_copy_blocks_at_block_size_32(oracle_mod):
+    rng = np.random.default_rng(32)
+    NB, Hkv, B, D = 9, 2, 32, 8
+    ks = [rng.integers(0, 1 << 16, (NB, Hkv, B, D), dtype=np.uint16) for _ in range(2)]
+    vs = [rng.integers(0, 1 << 16, (NB, Hkv, B, D), dtype=np.uint16) for _ in range(2)]
+    before = [x.copy() for x in ks + vs]
+    pairs = np.array([[1, 4], [2, 7]], np.int64)
+    oracle_mod.copy_blocks(ks, vs, pairs)
+    for x, x0 in zip(ks + vs, before):
+        want = x0.copy()
+        want[4], want[7] = x0[1], x0[2]
+        assert np.array_equal(x, want)
+
+
 def test_context_of_one_returns_v0(oracle_mod):
     rng = np.random.default_rng(3)
     q, kc, vc, tables, lens = _paged_problem(rng, [1, 1, 1], 6, 3, 32, "bf16")
