@@ -66,11 +66,12 @@ def algorithmic_bytes(wl, out_elt=4):
     """(attention bytes, cache-write bytes, copy bytes) of one step."""
     S, H, Hkv, D, elt = wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, 2
     L = wl.context_lens.astype(np.int64)
-    nb = (L + 15) // 16
+    B = wl.block_size
+    nb = (L + B - 1) // B
     attn = int(L.sum()) * Hkv * D * elt * 2 + S * H * D * elt + S * H * D * out_elt + \
         int(nb.sum()) * 4 + S * 4
     write = 2 * (S * Hkv * D * elt * 2) + S * 8
-    copy = 2 * len(wl.copy_pairs) * Hkv * 16 * D * elt * 2
+    copy = 2 * len(wl.copy_pairs) * Hkv * B * D * elt * 2
     return attn, write, copy
 
 
@@ -301,6 +302,61 @@ def layout_sweep(args, wl, dev):
           flush=True)
 
 
+def block_size_sweep(args, wl, dev):
+    """Attention-call time on one workload's sequences stored in blocks of
+    8 .. 256 tokens, each with the blocks scattered over the pool and in
+    order; the contiguous cache is the common baseline."""
+    import torch
+    import paged_kv_cache_pa_gb300 as pa
+    from paged_kv_cache_pa_gb300 import synthetic
+    S, H, Hkv, D = wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim
+    out = torch.empty(S, H, D, dtype=torch.float32, device=dev)
+    ws = torch.empty(pa.decode_workspace_size(S, H, Hkv, D, wl.max_context_len),
+                     dtype=torch.uint8, device=dev)
+    lens = torch.as_tensor(wl.context_lens, device=dev)
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / args.steps
+
+    rows = int(-(-wl.max_context_len // 16) * 16)
+    dt = synthetic._torch_dtype(wl.dtype)
+    g = torch.Generator(device=dev).manual_seed(wl.seed)
+    q = torch.randn(S, H, D, generator=g, device=dev).to(dt)
+    kc = torch.randn(S, Hkv, rows, D, generator=g, device=dev).to(dt)
+    vc = torch.randn(S, Hkv, rows, D, generator=g, device=dev).to(dt)
+    base = timed(lambda: pa.decode_attention_contiguous(q, kc, vc, lens, wl.max_context_len,
+                                                        wl.scale, out=out, workspace=ws))
+    del q, kc, vc
+    torch.cuda.empty_cache()
+    res = {"contiguous": {"ms_per_call": round(base, 4)}}
+    for B in pa.BLOCK_SIZES:
+        w0 = wl if B == wl.block_size else synthetic.relayout(wl, B)
+        for order, w in (("scattered", w0), ("in_order", synthetic.in_order(w0))):
+            vals = synthetic.make_values(w, device=dev)
+            tables = torch.as_tensor(w.block_tables, device=dev)
+            ms = timed(lambda: pa.decode_attention(vals["q"], vals["k_cache"], vals["v_cache"],
+                                                   tables, lens, w.max_context_len, w.scale,
+                                                   out=out, workspace=ws))
+            b_attn = algorithmic_bytes(w)[0]
+            res[f"b{B}_{order}"] = {"ms_per_call": round(ms, 4),
+                                    "GBps": round(b_attn / (ms * 1e-3) / 1e9, 1),
+                                    "time_vs_contiguous": round(ms / base, 4)}
+            del vals
+            torch.cuda.empty_cache()
+    print(json.dumps({"block_size_sweep": args.config, "workload": WORKLOADS.get(args.config),
+                      "steps": args.steps, "results": res}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -316,6 +372,10 @@ def main():
     ap.add_argument("--layout-sweep", action="store_true",
                     help="time the attention call with blocks scattered, blocks in order, and "
                          "on a contiguous (unpaged) cache; prints its own JSON line")
+    ap.add_argument("--block-size-sweep", action="store_true",
+                    help="time the attention call with the workload's sequences in blocks of "
+                         "8..256 tokens, scattered and in order, against a contiguous cache; "
+                         "prints its own JSON line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -345,6 +405,9 @@ def main():
 
     if args.layout_sweep:
         layout_sweep(args, wl, dev)
+        return
+    if args.block_size_sweep:
+        block_size_sweep(args, wl, dev)
         return
 
     vals = synthetic.make_values(wl, device=dev)

@@ -1,7 +1,8 @@
 /*
  * pa.h -- C ABI of the paged-KV-cache decode path for one GB300 (sm_103a).
  *
- * The KV cache of every layer is a pool of fixed-size blocks of 16 tokens;
+ * The KV cache of every layer is a pool of fixed-size blocks of 16 tokens
+ * (other block sizes through the *_ex entry points);
  * each sequence reaches its tokens through a block table of physical block
  * ids, and the kernels see nothing but those ids and the sequence lengths
  * [Efficient Memory Management for Large Language Model Serving with
@@ -66,9 +67,18 @@ typedef enum {
 
 #define PA_BLOCK_SIZE 16
 
+/* Block sizes the *_ex entry points accept: powers of two in this range.  A
+ * pool of block size B is [num_blocks][num_kv_heads][B][head_dim] and token t
+ * of a sequence lives at block block_tables[s][t / B], offset t % B
+ * [Efficient Memory Management ..., "PagedAttention Algorithm": the KV cache
+ * is split into blocks of B tokens; Paged Attention: Managing the KV Cache
+ * ..., benchmark section: the same kernel over a range of block sizes]. */
+#define PA_MIN_BLOCK_SIZE 8
+#define PA_MAX_BLOCK_SIZE 256
+
 /* Bits OR-ed into *dev_error_word by the kernels. */
 #define PA_ERRBIT_BLOCK_OOB   1u  /* a block id (table entry or copy pair) outside [0, num_blocks) */
-#define PA_ERRBIT_SLOT_OOB    2u  /* a slot >= num_blocks * 16 */
+#define PA_ERRBIT_SLOT_OOB    2u  /* a slot >= num_blocks * block size */
 #define PA_ERRBIT_CONTEXT_LEN 4u  /* context_lens[s] < 0 or > max_context_len */
 #define PA_ERRBIT_TIMEOUT     8u  /* a bounded wait inside a kernel gave up */
 
@@ -97,6 +107,19 @@ pa_status_t pa_cache_write(const void *key, const void *value, void *k_cache, vo
                            const int64_t *slot_mapping, int num_tokens, int num_blocks,
                            int num_kv_heads, int head_dim, pa_dtype_t dtype,
                            unsigned int *dev_error_word, pa_stream_t stream);
+
+/*
+ * pa_cache_write_ex -- pa_cache_write for pools of block_size tokens per
+ * block: k_cache[slot / block_size][h][slot % block_size][:] = key[t][h][:].
+ * block_size: a power of two in [PA_MIN_BLOCK_SIZE, PA_MAX_BLOCK_SIZE]
+ * (others: PA_ERR_UNSUPPORTED).  pa_cache_write(...) is
+ * pa_cache_write_ex(..., num_blocks, PA_BLOCK_SIZE, ...).
+ */
+pa_status_t pa_cache_write_ex(const void *key, const void *value, void *k_cache,
+                              void *v_cache, const int64_t *slot_mapping, int num_tokens,
+                              int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                              pa_dtype_t dtype, unsigned int *dev_error_word,
+                              pa_stream_t stream);
 
 /*
  * pa_decode_workspace_size -- bytes of device workspace pa_decode_attention
@@ -164,6 +187,25 @@ pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, const void *que
                                 int num_blocks, float scale, pa_dtype_t dtype,
                                 void *workspace, size_t workspace_bytes,
                                 unsigned int *dev_error_word, pa_stream_t stream);
+
+/*
+ * pa_decode_attention_ex -- pa_decode_attention over pools of block_size
+ * tokens per block: token t of sequence s is read at block
+ * block_tables[s][t / block_size], offset t % block_size; max_context_len
+ * <= block_size * max_blocks_per_seq.  block_size: a power of two in
+ * [PA_MIN_BLOCK_SIZE, PA_MAX_BLOCK_SIZE] (others: PA_ERR_UNSUPPORTED).
+ * Results do not depend on the block size.  Workspace, errors and kernels
+ * are those of pa_decode_attention, which is
+ * pa_decode_attention_ex(..., num_blocks, PA_BLOCK_SIZE, ...).
+ */
+pa_status_t pa_decode_attention_ex(void *out, pa_dtype_t out_dtype, const void *query,
+                                   const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *context_lens, int max_context_len,
+                                   int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                   int num_blocks, int block_size, float scale,
+                                   pa_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                                   unsigned int *dev_error_word, pa_stream_t stream);
 
 /*
  * pa_decode_attention_contiguous -- the same decode attention over a
@@ -258,6 +300,18 @@ pa_status_t pa_copy_blocks(void *const *k_caches, void *const *v_caches, int num
                            const int64_t *block_pairs, int num_pairs, int num_blocks,
                            int num_kv_heads, int head_dim, pa_dtype_t dtype,
                            unsigned int *dev_error_word, pa_stream_t stream);
+
+/*
+ * pa_copy_blocks_ex -- pa_copy_blocks for pools of block_size tokens per
+ * block (whole blocks of num_kv_heads * block_size * head_dim elements).
+ * block_size: a power of two in [PA_MIN_BLOCK_SIZE, PA_MAX_BLOCK_SIZE]
+ * (others: PA_ERR_UNSUPPORTED).  pa_copy_blocks(...) is
+ * pa_copy_blocks_ex(..., num_blocks, PA_BLOCK_SIZE, ...).
+ */
+pa_status_t pa_copy_blocks_ex(void *const *k_caches, void *const *v_caches, int num_layers,
+                              const int64_t *block_pairs, int num_pairs, int num_blocks,
+                              int block_size, int num_kv_heads, int head_dim, pa_dtype_t dtype,
+                              unsigned int *dev_error_word, pa_stream_t stream);
 
 /* Static, human-readable name of a status. */
 const char *pa_status_string(pa_status_t status);

@@ -12,6 +12,10 @@ device, raises.
                      max_context_len, scale, out=None, ...)
     copy_blocks(k_caches, v_caches, block_pairs)
 
+Pools are [num_blocks][num_kv_heads][block_size][head_dim]; the block size
+is read from their third dimension: 16 goes to the plain entry points, other
+supported sizes (powers of two from 8 to 256) to the ``*_ex`` ones.
+
 Build the library with ``python -m paged_kv_cache_pa_gb300.build``.
 """
 from __future__ import annotations
@@ -25,9 +29,10 @@ __all__ = ["cache_write", "decode_attention", "decode_attention_contiguous",
            "decode_workspace_size", "decode_partition_tokens", "copy_blocks",
            "status_string", "PaError", "library_path", "load_library", "BLOCK_SIZE",
            "ERRBIT_BLOCK_OOB", "ERRBIT_SLOT_OOB", "ERRBIT_CONTEXT_LEN", "ERRBIT_TIMEOUT",
-           "MAX_LAYERS"]
+           "MAX_LAYERS", "BLOCK_SIZES"]
 
 BLOCK_SIZE = 16
+BLOCK_SIZES = (8, 16, 32, 64, 128, 256)
 MAX_LAYERS = 128
 PA_F16, PA_BF16, PA_F32 = 0, 1, 2
 ERRBIT_BLOCK_OOB, ERRBIT_SLOT_OOB, ERRBIT_CONTEXT_LEN, ERRBIT_TIMEOUT = 1, 2, 4, 8
@@ -41,13 +46,17 @@ _lock = threading.Lock()
 _P, _I, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
 _SIGNATURES = {
     "pa_cache_write": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "pa_cache_write_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pa_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
     "pa_decode_partition_tokens": (_I, [_I, _I, _I]),
     "pa_decode_attention": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I,
                                  ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P]),
+    "pa_decode_attention_ex": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I,
+                                    _I, ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P]),
     "pa_decode_attention_contiguous": (_I, [_P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                             ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P]),
     "pa_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "pa_copy_blocks_ex": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -122,21 +131,24 @@ def _opt_ptr(t, name):
 def cache_write(key, value, k_cache, v_cache, slot_mapping, error_word=None,
                 stream=None) -> None:
     """Write key[t] / value[t] ([T][Hkv][D]) into pool slot slot_mapping[t]
-    (int64; < 0 skips).  Pools: [num_blocks][Hkv][16][D]."""
+    (int64; < 0 skips).  Pools: [num_blocks][Hkv][block_size][D]."""
     import torch
     if slot_mapping.dtype != torch.int64:
         raise TypeError("slot_mapping must be int64")
     nb, hkv, bs, d = k_cache.shape
-    if bs != BLOCK_SIZE or tuple(key.shape[1:]) != (hkv, d) or key.shape != value.shape:
+    if tuple(key.shape[1:]) != (hkv, d) or key.shape != value.shape:
         raise ValueError("shape mismatch between key/value and the pools")
     if v_cache.shape != k_cache.shape or k_cache.dtype != key.dtype or v_cache.dtype != key.dtype:
         raise ValueError("pools must match each other and the key dtype")
-    st = load_library().pa_cache_write(
-        _dev(key, "key"), _dev(value, "value"), _dev(k_cache, "k_cache"),
-        _dev(v_cache, "v_cache"), _dev(slot_mapping, "slot_mapping"), key.shape[0], nb, hkv, d,
-        _dtype_code(key.dtype), _opt_ptr(error_word, "error_word"),
-        _stream_ptr(stream, key.device))
-    _check(st, "pa_cache_write")
+    args = (_dev(key, "key"), _dev(value, "value"), _dev(k_cache, "k_cache"),
+            _dev(v_cache, "v_cache"), _dev(slot_mapping, "slot_mapping"), key.shape[0], nb)
+    tail = (hkv, d, _dtype_code(key.dtype), _opt_ptr(error_word, "error_word"),
+            _stream_ptr(stream, key.device))
+    lib = load_library()
+    if bs == BLOCK_SIZE:
+        _check(lib.pa_cache_write(*args, *tail), "pa_cache_write")
+    else:
+        _check(lib.pa_cache_write_ex(*args, bs, *tail), "pa_cache_write_ex")
 
 
 def decode_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
@@ -157,11 +169,12 @@ def decode_attention(query, k_cache, v_cache, block_tables, context_lens,
                      workspace=None, error_word=None, stream=None):
     """Paged decode attention; returns ``out`` [S][H][D] (fp32 unless
     ``out_dtype`` / ``out`` says the input dtype).  ``workspace`` (uint8, >=
-    decode_workspace_size bytes) is allocated here when not given."""
+    decode_workspace_size bytes) is allocated here when not given.  Pools
+    are [num_blocks][Hkv][block_size][D]."""
     import torch
     S, H, D = query.shape
     nb, hkv, bs, d2 = k_cache.shape
-    if bs != BLOCK_SIZE or d2 != D or v_cache.shape != k_cache.shape:
+    if d2 != D or v_cache.shape != k_cache.shape:
         raise ValueError("pool shape mismatch")
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise TypeError("block_tables and context_lens must be int32")
@@ -172,14 +185,18 @@ def decode_attention(query, k_cache, v_cache, block_tables, context_lens,
     if workspace is None:
         nbytes = decode_workspace_size(S, H, hkv, D, int(max_context_len))
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=query.device)
-    st = load_library().pa_decode_attention(
-        _dev(out, "out"), _dtype_code(out.dtype), _dev(query, "query"), _dev(k_cache, "k_cache"),
-        _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"), block_tables.shape[1],
-        _dev(context_lens, "context_lens"), int(max_context_len), S, H, hkv, D, nb,
-        float(scale), _dtype_code(query.dtype), _dev(workspace, "workspace"),
-        workspace.numel() * workspace.element_size(), _opt_ptr(error_word, "error_word"),
-        _stream_ptr(stream, query.device))
-    _check(st, "pa_decode_attention")
+    head = (_dev(out, "out"), _dtype_code(out.dtype), _dev(query, "query"),
+            _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+            _dev(block_tables, "block_tables"), block_tables.shape[1],
+            _dev(context_lens, "context_lens"), int(max_context_len), S, H, hkv, D, nb)
+    tail = (float(scale), _dtype_code(query.dtype), _dev(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(), _opt_ptr(error_word, "error_word"),
+            _stream_ptr(stream, query.device))
+    lib = load_library()
+    if bs == BLOCK_SIZE:
+        _check(lib.pa_decode_attention(*head, *tail), "pa_decode_attention")
+    else:
+        _check(lib.pa_decode_attention_ex(*head, bs, *tail), "pa_decode_attention_ex")
     return out
 
 
@@ -228,9 +245,12 @@ def copy_blocks(k_caches: Sequence, v_caches: Sequence, block_pairs, error_word=
     kp = (ctypes.c_void_p * L)(*[_dev(c, "k_caches") for c in k_caches])
     vp = (ctypes.c_void_p * L)(*[_dev(c, "v_caches") for c in v_caches])
     npairs = block_pairs.shape[0] if block_pairs.numel() else 0
-    st = load_library().pa_copy_blocks(
-        ctypes.cast(kp, ctypes.c_void_p), ctypes.cast(vp, ctypes.c_void_p), L,
-        _dev(block_pairs, "block_pairs") if npairs else None, npairs, nb, hkv, d,
-        _dtype_code(k_caches[0].dtype), _opt_ptr(error_word, "error_word"),
-        _stream_ptr(stream, k_caches[0].device))
-    _check(st, "pa_copy_blocks")
+    head = (ctypes.cast(kp, ctypes.c_void_p), ctypes.cast(vp, ctypes.c_void_p), L,
+            _dev(block_pairs, "block_pairs") if npairs else None, npairs, nb)
+    tail = (hkv, d, _dtype_code(k_caches[0].dtype), _opt_ptr(error_word, "error_word"),
+            _stream_ptr(stream, k_caches[0].device))
+    lib = load_library()
+    if bs == BLOCK_SIZE:
+        _check(lib.pa_copy_blocks(*head, *tail), "pa_copy_blocks")
+    else:
+        _check(lib.pa_copy_blocks_ex(*head, bs, *tail), "pa_copy_blocks_ex")

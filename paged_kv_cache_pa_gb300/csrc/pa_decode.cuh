@@ -16,11 +16,16 @@
 //     first; CTAs take their first three items in a fixed order and claim
 //     the rest with one atomic each, so the tail is short.
 //   * Warp 0 (producer) resolves the item's block-table slice once (one
-//     coalesced load for up to 32 blocks) and streams each block's K and V
-//     tiles -- 16 rows x head_dim contiguous, only the valid rows -- with 1-D
-//     bulk async copies (TMA) into an R-stage shared-memory ring guarded by
-//     mbarriers (full: transaction bytes; empty: one arrival per consumer
-//     warp).  The item's G query rows ride with its first block.
+//     coalesced load, one entry per 16-token chunk; two for 8-token blocks)
+//     and streams each chunk's K and V rows -- 16 rows x head_dim, only the
+//     valid rows, contiguous within a block -- with 1-D bulk async copies
+//     (TMA) into an R-stage shared-memory ring guarded by mbarriers (full:
+//     transaction bytes; empty: one arrival per consumer warp).  The item's
+//     G query rows ride with its first chunk.
+//   * Block size B (tokens per block) is 8..256, a power of two, and only
+//     changes where a chunk's rows come from: token t of a sequence is row
+//     t % B of block block_tables[s][t / B]; a chunk lies in one block for
+//     B >= 16 and spans two for B = 8.
 //   * Warps 1..4 (consumers) each own 4 of a tile's 16 rows.  A row is split
 //     over head_dim/8 lanes (16-byte chunks), so a warp reads 512 contiguous
 //     bytes per instruction (no bank conflicts).  Scores: per-lane partial
@@ -47,11 +52,11 @@
 
 namespace pa {
 
-constexpr int kBlock = PA_BLOCK_SIZE;  // tokens per KV block
+constexpr int kBlock = 16;             // tokens per ring stage (a chunk; one MMA n-extent)
 constexpr int kNCW = 4;                // consumer warps
 constexpr int kThreads = 32 * (kNCW + 1);
 constexpr int kRowsPerWarp = kBlock / kNCW;
-constexpr int kMaxPartTokens = 32 * kBlock;  // one producer lane per block of an item
+constexpr int kMaxPartTokens = 32 * kBlock;  // one producer lane per chunk of an item
 constexpr int kEndFlag = 1;
 
 struct alignas(16) StageMeta {
@@ -75,6 +80,7 @@ struct DecodeParams {
     const void *v_cache;
     const int32_t *block_tables;
     int max_blocks_per_seq;
+    int block_size, block_shift;  // tokens per pool block (8..256) and its log2
     // 0: paged pools reached through block_tables.  > 0: contiguous caches
     // [num_seqs][num_kv_heads][contig_rows][head_dim], no table.
     int contig_rows;
@@ -169,18 +175,26 @@ struct ItemPipe {
     int PB, lane;
     unsigned cX, cY, cZ, raw;  // item indices; raw: lane 0's pending claim
     int4 eX, eY, eZ;           // entries (s, p, ntok, nparts)
-    int tX, tY;                // this lane's block-table entry of X and Y
+    int2 tX, tY;               // block-table entries of this lane's chunk of X and Y
 
     __device__ __forceinline__ int4 entry(unsigned c) const {
         return c < n_items ? P->items[c / Hkv] : make_int4(0, 0, 0, 0);
     }
-    __device__ __forceinline__ int table(unsigned c, int4 e) const {
-        const int nblk = (e.z + kBlock - 1) / kBlock;
-        if (P->contig_rows) return 0;  // contiguous cache: no table
-        if (c < n_items && lane < nblk)
-            return __ldg(&P->block_tables[(size_t)e.x * P->max_blocks_per_seq + (size_t)e.y * PB +
-                                          lane]);
-        return -1;
+    // Lane j's chunk (tokens 16 j .. 16 j + 15 of the item): x = the block
+    // holding its first token; y = the next block, read only for 8-token
+    // blocks when the chunk has more than 8 tokens.
+    __device__ __forceinline__ int2 table(unsigned c, int4 e) const {
+        if (P->contig_rows) return make_int2(0, 0);  // contiguous cache: no table
+        const int nchunk = (e.z + kBlock - 1) / kBlock;
+        int2 r = make_int2(-1, -1);
+        if (c < n_items && lane < nchunk) {
+            const int32_t *row = P->block_tables + (size_t)e.x * P->max_blocks_per_seq;
+            const int i = (e.y * PB + lane) * kBlock >> P->block_shift;
+            r.x = __ldg(&row[i]);
+            if (P->block_size < kBlock && e.z - lane * kBlock > P->block_size)
+                r.y = __ldg(&row[i + 1]);
+        }
+        return r;
     }
     __device__ __forceinline__ unsigned claim() const {
         return lane == 0 ? 3u * gridDim.x + atomicAdd(&P->hdr->counter, 1u) : 0u;
@@ -204,7 +218,7 @@ struct ItemPipe {
     __device__ __forceinline__ bool valid() const { return cX < n_items; }
     // Move to the next item; called after the current item's copies are issued.
     __device__ __forceinline__ void advance() {
-        const int tZ = table(cZ, eZ);
+        const int2 tZ = table(cZ, eZ);
         const unsigned cW = __shfl_sync(0xffffffffu, raw, 0);
         const int4 eW = entry(cW);
         raw = claim();
@@ -234,53 +248,78 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
     ItemPipe items;
     items.init(P, n_items, lane);
 
-    uint32_t k = 0;  // stages issued so far
+    uint32_t k = 0;      // stages issued so far
+    int slot = 0;        // k % R
+    uint32_t phase = 0;  // (k / R) & 1
     bool aborted = false;
+    const bool split = !P.contig_rows && P.block_size < kBlock;  // 8-token blocks
+    const uint32_t q_bytes = (uint32_t)(G * D * sizeof(T));
     while (items.valid()) {
         const unsigned cA = items.cX;
         const int4 eA = items.eX;
-        const int tA = items.tX;
+        const int2 tA = items.tX;
 
         const int s = eA.x, part = eA.y, ntok = eA.z, nparts = eA.w;
         const int hk = (int)(cA % Hkv);
         const int nblk = (ntok + kBlock - 1) / kBlock;
+        // Lane j prepares chunk j's copies once per item (all chunks at once),
+        // so the per-chunk loop below only waits, arms the barrier and issues.
+        const int nv = lane < nblk ? min(kBlock, ntok - lane * kBlock) : 0;
+        // rows from the chunk's first block and (8-token blocks) its second
+        const int n0 = split ? min(nv, P.block_size) : nv, n1 = nv - n0;
+        const bool bad = nv > 0 && !P.contig_rows &&
+                         (tA.x < 0 || tA.x >= P.num_blocks ||
+                          (n1 > 0 && (tA.y < 0 || tA.y >= P.num_blocks)));
+        const unsigned badmask = __ballot_sync(0xffffffffu, bad);  // skipped chunks
+        if (lane == 0 && badmask && P.err) atomicOr(P.err, PA_ERRBIT_BLOCK_OOB);
+        size_t off0 = 0, off1 = 0;  // element offsets of the rows in either pool
+        if (nv > 0 && !bad) {
+            const int t0 = part * P.part_tokens + lane * kBlock;  // the chunk's first token
+            if (P.contig_rows) {
+                off0 = (((size_t)s * Hkv + hk) * P.contig_rows + (size_t)t0) * D;
+            } else {
+                off0 = ((((size_t)tA.x * Hkv + hk) << P.block_shift) +
+                        (size_t)(t0 & (P.block_size - 1))) * D;
+                off1 = (((size_t)tA.y * Hkv + hk) << P.block_shift) * D;
+            }
+        }
+        const uint32_t bytes0 = (uint32_t)n0 * D * (uint32_t)sizeof(T);
+        const uint32_t bytes1 = (uint32_t)n1 * D * (uint32_t)sizeof(T);
+        const T *qsrc = qg + ((size_t)s * P.num_heads + (size_t)hk * G) * D;
+
         for (int j = 0; j < nblk; ++j, ++k) {
-            const int slot = (int)(k % R);
             bool ok = true;
-            if (lane == 0) ok = mbar_wait(&empty[slot], ((k / R) & 1u) ^ 1u, abort_flag);
+            if (lane == 0) ok = mbar_wait(&empty[slot], phase ^ 1u, abort_flag);
             if (!__shfl_sync(0xffffffffu, (int)ok, 0)) {  // warp-uniform outcome
                 aborted = true;
                 break;
             }
-            const int phys = __shfl_sync(0xffffffffu, tA, j);
-            const bool bad = !P.contig_rows && (phys < 0 || phys >= P.num_blocks);
-            const int nvalid = bad ? 0 : min(kBlock, ntok - j * kBlock);  // bad: skip the block
-            const uint32_t kv_bytes = (uint32_t)nvalid * D * (uint32_t)sizeof(T);
-            const uint32_t q_bytes = j == 0 ? (uint32_t)(G * D * sizeof(T)) : 0u;
             if (lane == 0) {
-                if (bad && P.err) atomicOr(P.err, PA_ERRBIT_BLOCK_OOB);
+                const int nvalid = ((badmask >> j) & 1u) ? 0 : min(kBlock, ntok - j * kBlock);
                 StageMeta m;
                 m.s = s; m.hk = hk; m.p = part; m.nparts = nparts;
                 m.j = j; m.nblk = nblk; m.nvalid = nvalid; m.flags = 0;
                 meta[slot] = m;
-                mbar_arrive_expect_tx(&full[slot], 2 * kv_bytes + q_bytes);
+                mbar_arrive_expect_tx(&full[slot],
+                                      2u * (uint32_t)nvalid * D * (uint32_t)sizeof(T) +
+                                          (j == 0 ? q_bytes : 0u));
+                if (j == 0) bulk_g2s_nohint(sq + (size_t)slot * GM * D, qsrc, q_bytes, &full[slot]);
             }
             __syncwarp();
-            // one copy per lane: K rows (lane 0), V rows (lane 1), query (lane 2)
-            if (lane < 2 && kv_bytes) {
-                const size_t off =
-                    P.contig_rows
-                        ? (((size_t)s * Hkv + hk) * P.contig_rows +
-                           (size_t)(part * (P.part_tokens / kBlock) + j) * kBlock) * D
-                        : ((size_t)phys * Hkv + hk) * kTile;
-                bulk_g2s((lane ? sv : sk) + slot * kTile, (lane ? vc : kc) + off, kv_bytes,
-                         &full[slot], policy);
+            if (lane == j && nv > 0 && !bad) {
+                T *dk = sk + slot * kTile, *dv = sv + slot * kTile;
+                bulk_g2s(dk, kc + off0, bytes0, &full[slot], policy);
+                bulk_g2s(dv, vc + off0, bytes0, &full[slot], policy);
+                if (bytes1) {
+                    bulk_g2s(dk + (size_t)n0 * D, kc + off1, bytes1, &full[slot], policy);
+                    bulk_g2s(dv + (size_t)n0 * D, vc + off1, bytes1, &full[slot], policy);
+                }
             }
-            if (lane == 2 && q_bytes)
-                bulk_g2s_nohint(sq + (size_t)slot * GM * D,
-                                qg + ((size_t)s * P.num_heads + (size_t)hk * G) * D, q_bytes,
-                                &full[slot]);
             __syncwarp();
+            if (++slot == R) {
+                slot = 0;
+                phase ^= 1u;
+            }
         }
         if (aborted) break;
         items.advance();
@@ -356,9 +395,12 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &P, const T *sk,
         for (int e = 0; e < 8; ++e) q[g][e] = acc[g][e] = 0.f;
     }
 
-    for (uint32_t k = 0;; ++k) {
-        const int slot = (int)(k % R);
-        const bool ok = mbar_wait(&full[slot], (k / R) & 1u, abort_flag);
+    int slot = -1;       // ring stage of this iteration
+    uint32_t phase = 1;  // its phase parity
+    for (;;) {
+        if (++slot == R) slot = 0;
+        if (slot == 0) phase ^= 1u;
+        const bool ok = mbar_wait(&full[slot], phase, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) {  // warp-uniform outcome
             if (lane == 0) {
                 *abort_flag = 1;

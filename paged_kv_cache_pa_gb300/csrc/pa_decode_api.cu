@@ -270,15 +270,15 @@ EncodeTiledFn tensor_map_encoder() {
 
 // 3-D view [head_dim / 64][rows][64] of a row-major [rows][head_dim] 16-bit
 // tensor (strides: a row is head_dim * 2 bytes, a 64-element half 128 bytes);
-// one box is box_rows rows with all halves, 128-byte swizzle; reads past the
-// last row return zeros.
+// one box is box_rows rows of box_halves halves (all halves, or one),
+// 128-byte swizzle; reads past the last row return zeros.
 bool encode_rows(CUtensorMap *map, const void *base, pa_dtype_t dtype, unsigned long long rows,
-                 int head_dim, int box_rows) {
+                 int head_dim, int box_rows, int box_halves) {
     EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[3] = {64u, (cuuint64_t)rows, (cuuint64_t)(head_dim / 64)};
     const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, 128u};
-    const cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, (cuuint32_t)(head_dim / 64)};
+    const cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, (cuuint32_t)box_halves};
     const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
     return enc(map,
                dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -289,6 +289,13 @@ bool encode_rows(CUtensorMap *map, const void *base, pa_dtype_t dtype, unsigned 
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// log2 of a supported pool block size (8 .. 256 tokens, a power of two), or -1
+int block_shift_of(int b) {
+    for (int sh = 3; sh <= 8; ++sh)
+        if (b == (1 << sh)) return sh;
+    return -1;
+}
 
 }  // namespace
 
@@ -328,9 +335,11 @@ pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, cons
                         const void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
                         int contig_rows, const int32_t *context_lens, int max_context_len,
                         int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-                        int num_blocks, float scale, pa_dtype_t dtype, void *workspace,
-                        size_t workspace_bytes, unsigned int *dev_error_word,
+                        int num_blocks, int block_size, float scale, pa_dtype_t dtype,
+                        void *workspace, size_t workspace_bytes, unsigned int *dev_error_word,
                         pa_stream_t stream) {
+    const int block_shift = block_shift_of(block_size);
+    if (block_shift < 0) return PA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0)
         return PA_ERR_INVALID_ARG;
     if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
@@ -342,11 +351,11 @@ pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, cons
     unsigned long long pool_rows;
     if (contig_rows == 0) {
         if (num_blocks <= 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
-        if ((long long)max_context_len > (long long)PA_BLOCK_SIZE * max_blocks_per_seq)
+        if ((long long)max_context_len > (long long)block_size * max_blocks_per_seq)
             return PA_ERR_INVALID_ARG;
-        pool_rows = (unsigned long long)num_blocks * num_kv_heads * PA_BLOCK_SIZE;
+        pool_rows = (unsigned long long)num_blocks * num_kv_heads * block_size;
     } else {
-        if (contig_rows < 0 || contig_rows % PA_BLOCK_SIZE != 0 || max_context_len > contig_rows)
+        if (contig_rows < 0 || contig_rows % kBlock != 0 || max_context_len > contig_rows)
             return PA_ERR_INVALID_ARG;
         pool_rows = (unsigned long long)num_seqs * num_kv_heads * contig_rows;
     }
@@ -365,10 +374,15 @@ pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, cons
     DecodeParams P;
     memset(&P, 0, sizeof(P));
     if (uses_tensor_cores(num_heads / num_kv_heads, head_dim)) {
+        // a 16-token chunk per box (all halves), or for 8-token blocks one
+        // block's 8 rows of one 64-element half
+        const bool eight = contig_rows == 0 && block_size < kBlock;
+        const int box_rows = eight ? block_size : kBlock;
+        const int box_halves = eight ? 1 : head_dim / 64;
         if (!encode_rows(&P.tmap_q, query, dtype, (unsigned long long)num_seqs * num_heads,
-                         head_dim, 8) ||
-            !encode_rows(&P.tmap_k, k_cache, dtype, pool_rows, head_dim, PA_BLOCK_SIZE) ||
-            !encode_rows(&P.tmap_v, v_cache, dtype, pool_rows, head_dim, PA_BLOCK_SIZE))
+                         head_dim, 8, head_dim / 64) ||
+            !encode_rows(&P.tmap_k, k_cache, dtype, pool_rows, head_dim, box_rows, box_halves) ||
+            !encode_rows(&P.tmap_v, v_cache, dtype, pool_rows, head_dim, box_rows, box_halves))
             return PA_ERR_CUDA;
     }
     P.out = out;
@@ -378,6 +392,8 @@ pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, cons
     P.v_cache = v_cache;
     P.block_tables = block_tables;
     P.max_blocks_per_seq = max_blocks_per_seq;
+    P.block_size = block_size;
+    P.block_shift = block_shift;
     P.contig_rows = contig_rows;
     P.context_lens = context_lens;
     P.max_context_len = max_context_len;
@@ -414,8 +430,6 @@ pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, cons
         st_launch = launch_decode_d256(P, dtype, (int)cap, st);
     if (st_launch != PA_OK) return st_launch;
 
-    if (st_launch != PA_OK) return st_launch;
-
     if (w.max_parts > 1) {
         if (num_heads > 65535) return PA_ERR_UNSUPPORTED;
         const dim3 grid((unsigned)num_seqs, (unsigned)num_heads);
@@ -433,6 +447,18 @@ pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, cons
 
 }  // namespace
 
+extern "C" pa_status_t pa_decode_attention_ex(
+    void *out, pa_dtype_t out_dtype, const void *query, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+    int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+    int num_blocks, int block_size, float scale, pa_dtype_t dtype, void *workspace,
+    size_t workspace_bytes, unsigned int *dev_error_word, pa_stream_t stream) {
+    return decode_impl(out, out_dtype, query, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                       0, context_lens, max_context_len, num_seqs, num_heads, num_kv_heads,
+                       head_dim, num_blocks, block_size, scale, dtype, workspace,
+                       workspace_bytes, dev_error_word, stream);
+}
+
 extern "C" pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, const void *query,
                                            const void *k_cache, const void *v_cache,
                                            const int32_t *block_tables, int max_blocks_per_seq,
@@ -444,8 +470,8 @@ extern "C" pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, cons
                                            pa_stream_t stream) {
     return decode_impl(out, out_dtype, query, k_cache, v_cache, block_tables, max_blocks_per_seq,
                        0, context_lens, max_context_len, num_seqs, num_heads, num_kv_heads,
-                       head_dim, num_blocks, scale, dtype, workspace, workspace_bytes,
-                       dev_error_word, stream);
+                       head_dim, num_blocks, PA_BLOCK_SIZE, scale, dtype, workspace,
+                       workspace_bytes, dev_error_word, stream);
 }
 
 extern "C" pa_status_t pa_decode_attention_contiguous(
@@ -456,6 +482,6 @@ extern "C" pa_status_t pa_decode_attention_contiguous(
     if (max_rows <= 0) return PA_ERR_INVALID_ARG;
     return decode_impl(out, out_dtype, query, k_cache, v_cache, nullptr, 0, max_rows,
                        context_lens, max_context_len, num_seqs, num_heads, num_kv_heads,
-                       head_dim, 0, scale, dtype, workspace, workspace_bytes, dev_error_word,
-                       stream);
+                       head_dim, 0, PA_BLOCK_SIZE, scale, dtype, workspace, workspace_bytes,
+                       dev_error_word, stream);
 }

@@ -14,11 +14,15 @@
 // Data movement: the producer warp fetches up to W blocks per stage (one
 // per consumer warp) with tiled bulk copies (TMA) through 3-D tensor maps of
 // the pools viewed as [head_dim / 64 halves][blocks * KV heads * 16 rows][64],
-// with the 128-byte swizzle: one copy brings a block's whole K (or V) tile as
-// [half][token][64], and the ldmatrix reads of the consumers are free of bank
-// conflicts.  The copies of a stage are issued by separate lanes in one warp
-// instruction.  The item's query rows (8-row box) ride with its
-// first stage.  A block's box always has 16 rows; rows past the sequence's
+// with the 128-byte swizzle: one copy brings a 16-token chunk's whole K (or V)
+// tile as [half][token][64], and the ldmatrix reads of the consumers are free
+// of bank conflicts.  The copies of a stage are issued by separate lanes in
+// one warp instruction.  The item's query rows (8-row box) ride with its
+// first stage.  A chunk's box always has 16 rows, all inside one pool block
+// for block sizes >= 16; with 8-token blocks the maps' boxes are 8 rows of
+// one 64-element half, and a chunk takes two blocks x head_dim/64 halves,
+// each landing at its place in the same [half][token][64] tile (8 rows of
+// 128 bytes are one whole swizzle pattern).  Rows past the sequence's
 // length are masked out of the scores and zeroed in the V tile before P V,
 // so stale or poisoned data never reaches the output.
 //
@@ -37,7 +41,8 @@
 
 namespace pa {
 
-constexpr size_t kBoxBytes = 16 * 128;  // one block's 64-element box: 16 rows x 128 B
+constexpr size_t kBoxBytes = 16 * 128;  // one chunk's 64-element box: 16 rows x 128 B
+constexpr size_t kHalfBoxBytes = 8 * 128;  // an 8-token block's box: 8 rows x 128 B
 constexpr size_t kQBoxBytes = 8 * 128;  // the query box: 8 rows x 128 B
 
 // Per-item hand-off from the consumer warps to the epilogue warp.
@@ -162,13 +167,68 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
     while (items.valid()) {
         const unsigned cA = items.cX;
         const int4 eA = items.eX;
-        const int tA = items.tX;
+        const int2 tA = items.tX;
 
         const int s = eA.x, part = eA.y, ntok = eA.z, nparts = eA.w;
         const int hk = (int)(cA % Hkv);
         const int nblk = (ntok + kBlock - 1) / kBlock;
         const int nst = (nblk + W - 1) / W;
+        const bool split = !P.contig_rows && P.block_size < kBlock;  // 8-token blocks
+        const int t_item = part * P.part_tokens;  // the item's first token
         for (int st = 0; st < nst; ++st, ++k) {
+            // Everything that does not depend on the ring is worked out before
+            // waiting for the slot, so a freed slot is refilled at once.
+            const int j0 = st * W;
+            const int nb = min(W, nblk - j0);
+            // lane b < nb checks chunk b's block ids
+            const int lb = min(j0 + min(lane, W - 1), 31);
+            const int pc0 = __shfl_sync(0xffffffffu, tA.x, lb);
+            const int pc1 = __shfl_sync(0xffffffffu, tA.y, lb);
+            const bool second = split && lane < nb && ntok - (j0 + lane) * kBlock > P.block_size;
+            const bool bad_l = lane < nb && !P.contig_rows &&
+                               (pc0 < 0 || pc0 >= P.num_blocks ||
+                                (second && (pc1 < 0 || pc1 >= P.num_blocks)));
+            // chunks with an out-of-range block id are skipped
+            const unsigned bad = __ballot_sync(0xffffffffu, bad_l);
+            // 8-token blocks: chunks that need their second block
+            const unsigned two = __ballot_sync(0xffffffffu, second);
+            const uint32_t kv = split ? (uint32_t)(2 * KB * kHalfBoxBytes) *
+                                            (uint32_t)(nb - __popc(bad) + __popc(two & ~bad))
+                                      : (uint32_t)(2 * (nb - __popc(bad)) * KB * kBoxBytes);
+            const uint32_t tx = kv + (st == 0 ? (uint32_t)(KB * kQBoxBytes) : 0u);
+            // this lane's copy: its place in the stage, its row and half, K or V
+            bool issue;
+            int y, z = 0, is_v;
+            size_t off;
+            if (!split) {
+                // lane 2b fetches chunk b's K tile, lane 2b+1 its V tile (both
+                // 64-element halves in one 3-D box)
+                const int b = min(lane >> 1, W - 1);
+                const int pb = __shfl_sync(0xffffffffu, tA.x, min(j0 + b, 31));
+                issue = lane < 2 * nb && !((bad >> b) & 1u);
+                off = (size_t)b * KB * kBoxBytes;
+                const int t0 = t_item + (j0 + b) * kBlock;  // the chunk's first token
+                y = P.contig_rows ? (s * P.num_kv_heads + hk) * P.contig_rows + t0
+                                  : ((pb * P.num_kv_heads + hk) << P.block_shift) +
+                                        (t0 & (P.block_size - 1));
+                is_v = lane & 1;
+            } else {
+                // 8-token blocks: lane = ((b * 2 + u) * KB + h) * 2 + kv fetches
+                // half h of block u (0: first, 1: second) of chunk b, K or V
+                static_assert(W * 2 * KB * 2 <= 32, "one copy per lane");
+                const int h = (lane >> 1) % KB, u = (lane >> 1) / KB % 2,
+                          b = min((lane >> 1) / (2 * KB), W - 1);
+                const int p0 = __shfl_sync(0xffffffffu, tA.x, min(j0 + b, 31));
+                const int p1 = __shfl_sync(0xffffffffu, tA.y, min(j0 + b, 31));
+                issue = lane < W * 2 * KB * 2 && b < nb && !((bad >> b) & 1u) &&
+                        (u == 0 || ((two >> b) & 1u));
+                off = (size_t)b * KB * kBoxBytes + h * kBoxBytes + u * kHalfBoxBytes;
+                y = ((u ? p1 : p0) * P.num_kv_heads + hk) << P.block_shift;
+                z = h;
+                is_v = lane & 1;
+            }
+            if (lane == 0 && bad && P.err) atomicOr(P.err, PA_ERRBIT_BLOCK_OOB);
+
             const int slot = (int)(k % R);
             bool ok = true;
             if (lane == 0) ok = mbar_wait(&empty[slot], ((k / R) & 1u) ^ 1u, abort_flag);
@@ -176,43 +236,22 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
                 aborted = true;
                 break;
             }
-            const int j0 = st * W;
-            const int nb = min(W, nblk - j0);
-            int phys[W];
-            unsigned bad = 0;  // blocks with an out-of-range id are skipped
-#pragma unroll
-            for (int b = 0; b < W; ++b) {
-                phys[b] = __shfl_sync(0xffffffffu, tA, min(j0 + b, 31));
-                if (b < nb && !P.contig_rows && (phys[b] < 0 || phys[b] >= P.num_blocks))
-                    bad |= 1u << b;
-            }
             if (lane == 0) {
-                if (bad && P.err) atomicOr(P.err, PA_ERRBIT_BLOCK_OOB);
-                const uint32_t bytes = (uint32_t)(2 * (nb - __popc(bad)) * KB * kBoxBytes) +
-                                       (st == 0 ? (uint32_t)(KB * kQBoxBytes) : 0u);
                 StageMeta m;
                 m.s = s; m.hk = hk; m.p = part; m.nparts = nparts;
                 m.j = st; m.nblk = nst; m.nvalid = ntok - j0 * kBlock; m.flags = (int)(bad << 8);
                 meta[slot] = m;
-                mbar_arrive_expect_tx(&full[slot], bytes);
+                mbar_arrive_expect_tx(&full[slot], tx);
             }
             __syncwarp();
-            // one copy per lane: lane 2b fetches block b's K tile, lane 2b+1 its
-            // V tile (both 64-element halves in one 3-D box); lane 2*W the
-            // item's query rows
-            if (lane < 2 * nb && !((bad >> (lane >> 1)) & 1u)) {
-                const int b = lane >> 1;
-                const size_t off = (size_t)(slot * W + b) * KB * kBoxBytes;
-                const int y = P.contig_rows
-                                  ? (s * P.num_kv_heads + hk) * P.contig_rows +
-                                        (part * (P.part_tokens / kBlock) + j0 + b) * kBlock
-                                  : (phys[b] * P.num_kv_heads + hk) * kBlock;
-                if (lane & 1)
-                    tma_load_3d(sv + off, &P.tmap_v, 0, y, 0, &full[slot], policy);
+            if (issue) {
+                const size_t o = (size_t)slot * W * KB * kBoxBytes + off;
+                if (is_v)
+                    tma_load_3d(sv + o, &P.tmap_v, 0, y, z, &full[slot], policy);
                 else
-                    tma_load_3d(sk + off, &P.tmap_k, 0, y, 0, &full[slot], policy);
+                    tma_load_3d(sk + o, &P.tmap_k, 0, y, z, &full[slot], policy);
             }
-            if (st == 0 && lane == 2 * W)
+            if (st == 0 && lane == 0)
                 tma_load_3d(sq + (size_t)slot * KB * kQBoxBytes, &P.tmap_q, 0,
                             s * P.num_heads + hk * G, 0, &full[slot], policy);
             __syncwarp();

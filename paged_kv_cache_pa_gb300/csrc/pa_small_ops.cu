@@ -3,7 +3,7 @@
 // Both kernels move bytes unchanged with 16-byte vector loads and stores:
 //   - cache write: a grid over (new token, 16-byte chunk group); the token's
 //     Hkv rows of K and of V (Hkv * head_dim * 2 bytes each) go to block
-//     slot/16, offset slot%16
+//     slot/B, offset slot%B for block size B
 //     [Efficient Memory Management for Large Language Model Serving with
 //     PagedAttention, "Kernel-Level Optimizations", 1. fused reshape and
 //     block write].
@@ -20,8 +20,6 @@
 
 namespace {
 
-constexpr int kBlock = PA_BLOCK_SIZE;
-
 constexpr int kWriteThreads = 256;
 
 // grid (token, chunk group): every thread moves one 16-byte chunk of the
@@ -29,7 +27,7 @@ constexpr int kWriteThreads = 256;
 __global__ void __launch_bounds__(kWriteThreads) cache_write_kernel(
     const uint4 *__restrict__ key, const uint4 *__restrict__ value, uint4 *__restrict__ k_cache,
     uint4 *__restrict__ v_cache, const int64_t *__restrict__ slot_mapping, long long num_slots,
-    int num_kv_heads, int chunks_per_row, unsigned int *err) {
+    int block_shift, int num_kv_heads, int chunks_per_row, unsigned int *err) {
     pa::pdl_trigger();
     pa::pdl_wait();  // earlier kernels on the stream may still read or write the pools
     const int t = blockIdx.x;
@@ -42,10 +40,11 @@ __global__ void __launch_bounds__(kWriteThreads) cache_write_kernel(
         return;
     }
     if (i >= total) return;
-    const int64_t blk = slot / kBlock, off = slot % kBlock;
+    const int64_t blk = slot >> block_shift, off = slot & ((1 << block_shift) - 1);
     const int h = i / chunks_per_row, c = i - h * chunks_per_row;
     const size_t src = (size_t)t * total + i;
-    const size_t dst = (((size_t)blk * num_kv_heads + h) * kBlock + off) * chunks_per_row + c;
+    const size_t dst =
+        ((((size_t)blk * num_kv_heads + h) << block_shift) + off) * chunks_per_row + c;
     const uint4 kv = __ldcs(key + src);
     const uint4 vv = __ldcs(value + src);
     k_cache[dst] = kv;
@@ -96,14 +95,23 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
 
+// log2 of a supported block size, or -1
+int block_shift_of(int b) {
+    for (int sh = 3; sh <= 8; ++sh)
+        if (b == (1 << sh)) return sh;
+    return -1;
+}
+
 }  // namespace
 
-extern "C" pa_status_t pa_cache_write(const void *key, const void *value, void *k_cache,
-                                      void *v_cache, const int64_t *slot_mapping, int num_tokens,
-                                      int num_blocks, int num_kv_heads, int head_dim,
-                                      pa_dtype_t dtype, unsigned int *dev_error_word,
-                                      pa_stream_t stream) {
+extern "C" pa_status_t pa_cache_write_ex(const void *key, const void *value, void *k_cache,
+                                         void *v_cache, const int64_t *slot_mapping,
+                                         int num_tokens, int num_blocks, int block_size,
+                                         int num_kv_heads, int head_dim, pa_dtype_t dtype,
+                                         unsigned int *dev_error_word, pa_stream_t stream) {
     if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0) return PA_ERR_INVALID_ARG;
+    const int shift = block_shift_of(block_size);
+    if (shift < 0) return PA_ERR_UNSUPPORTED;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
     if (!head_dim_ok(head_dim)) return PA_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PA_OK;
@@ -116,18 +124,29 @@ extern "C" pa_status_t pa_cache_write(const void *key, const void *value, void *
     const cudaError_t e = pa::launch_pdl(
         cache_write_kernel, dim3((unsigned)num_tokens, (unsigned)groups), dim3(kWriteThreads), 0,
         (cudaStream_t)stream, (const uint4 *)key, (const uint4 *)value, (uint4 *)k_cache,
-        (uint4 *)v_cache, slot_mapping, (long long)num_blocks * kBlock, num_kv_heads,
+        (uint4 *)v_cache, slot_mapping, (long long)num_blocks << shift, shift, num_kv_heads,
         chunks_per_row, dev_error_word);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-extern "C" pa_status_t pa_copy_blocks(void *const *k_caches, void *const *v_caches,
-                                      int num_layers, const int64_t *block_pairs, int num_pairs,
+extern "C" pa_status_t pa_cache_write(const void *key, const void *value, void *k_cache,
+                                      void *v_cache, const int64_t *slot_mapping, int num_tokens,
                                       int num_blocks, int num_kv_heads, int head_dim,
                                       pa_dtype_t dtype, unsigned int *dev_error_word,
                                       pa_stream_t stream) {
+    return pa_cache_write_ex(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_blocks,
+                             PA_BLOCK_SIZE, num_kv_heads, head_dim, dtype, dev_error_word,
+                             stream);
+}
+
+extern "C" pa_status_t pa_copy_blocks_ex(void *const *k_caches, void *const *v_caches,
+                                         int num_layers, const int64_t *block_pairs,
+                                         int num_pairs, int num_blocks, int block_size,
+                                         int num_kv_heads, int head_dim, pa_dtype_t dtype,
+                                         unsigned int *dev_error_word, pa_stream_t stream) {
     if (num_layers <= 0 || num_pairs < 0 || num_blocks <= 0 || num_kv_heads <= 0)
         return PA_ERR_INVALID_ARG;
+    if (block_shift_of(block_size) < 0) return PA_ERR_UNSUPPORTED;
     if (num_layers > PA_MAX_LAYERS) return PA_ERR_UNSUPPORTED;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
     if (!head_dim_ok(head_dim)) return PA_ERR_UNSUPPORTED;
@@ -140,7 +159,7 @@ extern "C" pa_status_t pa_copy_blocks(void *const *k_caches, void *const *v_cach
         pools.k[l] = (uint4 *)k_caches[l];
         pools.v[l] = (uint4 *)v_caches[l];
     }
-    const long long chunks_per_block = (long long)num_kv_heads * kBlock * head_dim * 2 / 16;
+    const long long chunks_per_block = (long long)num_kv_heads * block_size * head_dim * 2 / 16;
     // about 32 KiB per CTA: enough bytes in flight per CTA, enough CTAs per copy
     const long long chunks_per_cta = 2048;
     const long long splits = (chunks_per_block + chunks_per_cta - 1) / chunks_per_cta;
@@ -151,6 +170,16 @@ extern "C" pa_status_t pa_copy_blocks(void *const *k_caches, void *const *v_cach
                        pools, block_pairs, num_blocks, chunks_per_block, chunks_per_cta,
                        dev_error_word);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" pa_status_t pa_copy_blocks(void *const *k_caches, void *const *v_caches,
+                                      int num_layers, const int64_t *block_pairs, int num_pairs,
+                                      int num_blocks, int num_kv_heads, int head_dim,
+                                      pa_dtype_t dtype, unsigned int *dev_error_word,
+                                      pa_stream_t stream) {
+    return pa_copy_blocks_ex(k_caches, v_caches, num_layers, block_pairs, num_pairs, num_blocks,
+                             PA_BLOCK_SIZE, num_kv_heads, head_dim, dtype, dev_error_word,
+                             stream);
 }
 
 extern "C" const char *pa_status_string(pa_status_t s) {

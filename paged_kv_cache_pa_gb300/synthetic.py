@@ -33,6 +33,9 @@ nearest integer, then clipped.  Seeds are 1001 + config index unless given.
 A step of the decode path is: copy-on-write copies (``beams`` only), the
 cache write of one new token per sequence into the slot of position L - 1,
 then attention over the L tokens.
+
+Blocks hold 16 tokens unless a workload is re-laid with :func:`relayout`,
+which keeps the lengths and deals blocks of another size.
 """
 from __future__ import annotations
 
@@ -65,6 +68,7 @@ class Workload:
     scale: float = 0.0
     used_blocks: Optional[np.ndarray] = None   # int64 ids holding context tokens
     info: Dict[str, float] = field(default_factory=dict)
+    block_size: int = BLOCK_SIZE    # tokens per pool block
 
     def __post_init__(self):
         if not self.scale:
@@ -95,9 +99,10 @@ def _lognormal_int(rng: np.random.Generator, mean: float, n: int, lo: int, hi: i
     return np.clip(x, lo, hi).astype(np.int64)
 
 
-def _deal_tables(lens: np.ndarray, ids: np.ndarray, max_blocks: Optional[int] = None):
-    """Give sequence s the next ceil(L_s/16) ids of ``ids``, in sequence order."""
-    nb = [blocks_for(int(L)) for L in lens]
+def _deal_tables(lens: np.ndarray, ids: np.ndarray, max_blocks: Optional[int] = None,
+                 block_size: int = BLOCK_SIZE):
+    """Give sequence s the next ceil(L_s/B) ids of ``ids``, in sequence order."""
+    nb = [blocks_for(int(L), block_size) for L in lens]
     maxb = max_blocks or max(max(nb) if nb else 1, 1)
     tables = np.full((len(lens), maxb), -1, np.int32)
     pos = 0
@@ -107,29 +112,32 @@ def _deal_tables(lens: np.ndarray, ids: np.ndarray, max_blocks: Optional[int] = 
     return tables
 
 
-def _slots_of_last(tables: np.ndarray, lens: np.ndarray) -> np.ndarray:
+def _slots_of_last(tables: np.ndarray, lens: np.ndarray,
+                   block_size: int = BLOCK_SIZE) -> np.ndarray:
     """Slot of position L-1 of each sequence (the token the step writes)."""
+    B = block_size
     pos = np.maximum(lens.astype(np.int64) - 1, 0)
-    blk = tables[np.arange(len(lens)), pos // BLOCK_SIZE].astype(np.int64)
-    return np.where(lens > 0, blk * BLOCK_SIZE + pos % BLOCK_SIZE, -1)   # empty: no token
+    blk = tables[np.arange(len(lens)), pos // B].astype(np.int64)
+    return np.where(lens > 0, blk * B + pos % B, -1)   # empty: no token
 
 
 def _from_lengths(name, lens, num_heads, num_kv_heads, head_dim, dtype, seed,
-                  rng, pool_blocks=None, max_blocks=None) -> Workload:
+                  rng, pool_blocks=None, max_blocks=None, block_size=BLOCK_SIZE) -> Workload:
     lens = np.asarray(lens, np.int64)
-    need = int(sum(blocks_for(int(L)) for L in lens))
+    need = int(sum(blocks_for(int(L), block_size) for L in lens))
     if pool_blocks is None:
         pool_blocks = need
         ids = rng.permutation(pool_blocks)
     else:
         ids = rng.choice(pool_blocks, size=need, replace=False)
-    tables = _deal_tables(lens, ids, max_blocks)
+    tables = _deal_tables(lens, ids, max_blocks, block_size)
     return Workload(name=name, num_seqs=len(lens), num_heads=num_heads,
                     num_kv_heads=num_kv_heads, head_dim=head_dim, dtype=dtype,
                     num_blocks=pool_blocks, context_lens=lens.astype(np.int32),
-                    block_tables=tables, slot_mapping=_slots_of_last(tables, lens),
+                    block_tables=tables, slot_mapping=_slots_of_last(tables, lens, block_size),
                     seed=seed, used_blocks=np.sort(ids[:need]).astype(np.int64),
-                    info={"mean_len": float(lens.mean()) if len(lens) else 0.0})
+                    info={"mean_len": float(lens.mean()) if len(lens) else 0.0},
+                    block_size=block_size)
 
 
 def make_tiny(seed: Optional[int] = None, num_seqs: int = 4) -> Workload:
@@ -229,15 +237,44 @@ def make_beams(seed: Optional[int] = None, groups: int = 32, beams: int = 6,
 def in_order(wl: Workload) -> Workload:
     """The same workload with every sequence's blocks laid out consecutively
     in the pool (sequence 0's blocks first), for comparing placements."""
+    B = wl.block_size
     lens = wl.context_lens.astype(np.int64)
-    need = int(sum(blocks_for(int(L)) for L in lens))
+    need = int(sum(blocks_for(int(L), B) for L in lens))
     ids = np.arange(need, dtype=np.int64)
-    tables = _deal_tables(lens, ids, wl.max_blocks_per_seq)
+    tables = _deal_tables(lens, ids, wl.max_blocks_per_seq, B)
     return Workload(name=wl.name + "-inorder", num_seqs=wl.num_seqs, num_heads=wl.num_heads,
                     num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim, dtype=wl.dtype,
                     num_blocks=max(need, 1), context_lens=wl.context_lens.copy(),
-                    block_tables=tables, slot_mapping=_slots_of_last(tables, lens),
-                    seed=wl.seed, scale=wl.scale, used_blocks=ids, info=dict(wl.info))
+                    block_tables=tables, slot_mapping=_slots_of_last(tables, lens, B),
+                    seed=wl.seed, scale=wl.scale, used_blocks=ids, info=dict(wl.info),
+                    block_size=B)
+
+
+def relayout(wl: Workload, block_size: int, seed: Optional[int] = None) -> Workload:
+    """The same sequences (lengths, shapes, dtype, seed) stored in blocks of
+    ``block_size`` tokens, scattered over a pool of the same byte size as
+    ``wl``'s (or just large enough, if rounding each sequence up to whole
+    blocks needs more).  Tables are dealt in sequence order from a seeded
+    random choice of pool blocks, as the 16-token workloads are.  Copy-on-
+    write pairs are not carried over (their blocks have no meaning here)."""
+    if len(wl.copy_pairs):
+        raise ValueError("relayout keeps no copy-on-write pairs")
+    B = int(block_size)
+    rng = np.random.default_rng(wl.seed if seed is None else seed)
+    lens = wl.context_lens.astype(np.int64)
+    need = int(sum(blocks_for(int(L), B) for L in lens))
+    same_bytes = -(-wl.num_blocks * wl.block_size // B)
+    pool = max(need, same_bytes, 1)
+    ids = rng.permutation(pool) if pool == need else rng.choice(pool, size=need, replace=False)
+    maxb = max(-(-wl.max_blocks_per_seq * wl.block_size // B), 1)
+    tables = _deal_tables(lens, ids, maxb, B)
+    return Workload(name=f"{wl.name}-b{B}", num_seqs=wl.num_seqs, num_heads=wl.num_heads,
+                    num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim, dtype=wl.dtype,
+                    num_blocks=pool, context_lens=wl.context_lens.copy(),
+                    block_tables=tables, slot_mapping=_slots_of_last(tables, lens, B),
+                    seed=wl.seed, scale=wl.scale,
+                    used_blocks=np.sort(ids[:need]).astype(np.int64), info=dict(wl.info),
+                    block_size=B)
 
 
 MAKERS = {"tiny": make_tiny, "opt13b": make_opt13b, "gqa": make_gqa, "beams": make_beams,
@@ -261,7 +298,7 @@ def _torch_dtype(dtype: str):
 def make_values(wl: Workload, device="cpu", seed: Optional[int] = None,
                 fill_all_blocks: Optional[bool] = None, poison_unused: bool = False):
     """Tensors for one step: q [S][H][D], key/value [S][Hkv][D] (the new token),
-    k_cache / v_cache [num_blocks][Hkv][16][D].
+    k_cache / v_cache [num_blocks][Hkv][block_size][D].
 
     Blocks listed in ``wl.used_blocks`` (and CoW destinations) always get
     N(0, 1) values.  Other blocks are filled too when ``fill_all_blocks``
@@ -276,6 +313,7 @@ def make_values(wl: Workload, device="cpu", seed: Optional[int] = None,
     g = torch.Generator(device=device)
     g.manual_seed(seed)
     S, H, Hkv, D, NB = wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.num_blocks
+    B = wl.block_size
 
     def randn(*shape):
         return torch.randn(*shape, generator=g, device=device, dtype=torch.float32).to(dt)
@@ -283,42 +321,43 @@ def make_values(wl: Workload, device="cpu", seed: Optional[int] = None,
     q = randn(S, H, D)
     key = randn(S, Hkv, D)
     value = randn(S, Hkv, D)
-    pool_bytes = NB * Hkv * BLOCK_SIZE * D * 2
+    pool_bytes = NB * Hkv * B * D * 2
     if fill_all_blocks is None:
         fill_all_blocks = pool_bytes <= (4 << 30)
-    k_cache = torch.empty(NB, Hkv, BLOCK_SIZE, D, dtype=dt, device=device)
-    v_cache = torch.empty(NB, Hkv, BLOCK_SIZE, D, dtype=dt, device=device)
+    k_cache = torch.empty(NB, Hkv, B, D, dtype=dt, device=device)
+    v_cache = torch.empty(NB, Hkv, B, D, dtype=dt, device=device)
     if fill_all_blocks:
-        chunk = max(1, (256 << 20) // (Hkv * BLOCK_SIZE * D * 4))
+        chunk = max(1, (256 << 20) // (Hkv * B * D * 4))
         for c in (k_cache, v_cache):
             for b0 in range(0, NB, chunk):
                 b1 = min(NB, b0 + chunk)
-                c[b0:b1] = randn(b1 - b0, Hkv, BLOCK_SIZE, D)
+                c[b0:b1] = randn(b1 - b0, Hkv, B, D)
     else:
         ids = np.asarray(wl.used_blocks if wl.used_blocks is not None else [], np.int64)
         if len(wl.copy_pairs):
             ids = np.union1d(ids, wl.copy_pairs.reshape(-1))
         idx_all = torch.as_tensor(ids, device=device)
-        chunk = max(1, (256 << 20) // (Hkv * BLOCK_SIZE * D * 4))
+        chunk = max(1, (256 << 20) // (Hkv * B * D * 4))
         for c in (k_cache, v_cache):
             for i0 in range(0, len(ids), chunk):
                 idx = idx_all[i0:i0 + chunk]
-                c.index_copy_(0, idx, randn(len(idx), Hkv, BLOCK_SIZE, D))
+                c.index_copy_(0, idx, randn(len(idx), Hkv, B, D))
     if poison_unused:
         poison_pools(wl, k_cache, v_cache)
     return {"q": q, "key": key, "value": value, "k_cache": k_cache, "v_cache": v_cache}
 
 
 def coverage_mask(wl: Workload) -> np.ndarray:
-    """bool [num_blocks][16]: True where some sequence's context covers the slot
-    (the new token's slot included)."""
-    m = np.zeros((wl.num_blocks, BLOCK_SIZE), bool)
+    """bool [num_blocks][block_size]: True where some sequence's context covers
+    the slot (the new token's slot included)."""
+    B = wl.block_size
+    m = np.zeros((wl.num_blocks, B), bool)
     for s in range(wl.num_seqs):
         L = int(wl.context_lens[s])
-        nb = blocks_for(L)
+        nb = blocks_for(L, B)
         for j in range(nb):
             b = int(wl.block_tables[s, j])
-            n = min(BLOCK_SIZE, L - j * BLOCK_SIZE)
+            n = min(B, L - j * B)
             m[b, :n] = True
     return m
 

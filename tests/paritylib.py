@@ -55,8 +55,9 @@ def host_inputs(wl, vals, blocks=None):
         h["k_cache"] = codes(vals["k_cache"].index_select(0, idx))
         h["v_cache"] = codes(vals["v_cache"].index_select(0, idx))
         relabel = lambda b: np.searchsorted(blocks, b)
+        B = wl.block_size
         tables = np.where(tables >= 0, relabel(np.maximum(tables, 0)), -1)
-        slots = relabel(slots // 16) * 16 + slots % 16
+        slots = np.where(slots >= 0, relabel(np.maximum(slots, 0) // B) * B + slots % B, -1)
         if len(pairs):
             pairs = relabel(pairs)
     h["tables"] = tables.astype(np.int32)
@@ -92,14 +93,16 @@ def max_abs(a, b) -> float:
 
 
 def custom_workload(lens, num_heads, num_kv_heads, head_dim, dtype, seed=7, extra_blocks=5,
-                    scale=None):
-    """A workload with the given lengths, blocks scattered over a slightly
-    larger pool (so some blocks belong to no sequence)."""
+                    scale=None, block_size=16):
+    """A workload with the given lengths, blocks of ``block_size`` tokens
+    scattered over a slightly larger pool (so some blocks belong to no
+    sequence)."""
     rng = np.random.default_rng(seed)
     lens = np.asarray(lens, np.int64)
+    B = block_size
     wl = synthetic._from_lengths("custom", lens, num_heads, num_kv_heads, head_dim, dtype, seed,
-                                 rng, pool_blocks=int(sum(-(-int(L) // 16) for L in lens)) +
-                                 extra_blocks)
+                                 rng, pool_blocks=int(sum(-(-int(L) // B) for L in lens)) +
+                                 extra_blocks, block_size=B)
     if scale is not None:
         wl.scale = scale
     return wl

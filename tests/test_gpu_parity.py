@@ -175,6 +175,97 @@ def test_output_is_bit_reproducible():
 
 
 # ---------------------------------------------------------------------------
+# other block sizes (pools of B tokens per block, the *_ex entry points)
+# ---------------------------------------------------------------------------
+
+BS_LENS = [1, 7, 8, 9, 15, 16, 17, 31, 33, 63, 64, 65, 100, 255, 257, 511, 513, 700, 1025]
+
+
+@pytest.mark.parametrize("B", [8, 32, 64, 128, 256])
+@pytest.mark.parametrize("H,Hkv,D,dtype", [
+    (4, 4, 128, "f16"), (12, 2, 128, "bf16"), (8, 2, 64, "f16"), (6, 2, 256, "bf16"),
+    (3, 3, 64, "bf16"),
+])
+def test_block_sizes_step_parity(B, H, Hkv, D, dtype):
+    """The whole step (cache write + attention) over pools of B-token
+    blocks, NaN in every uncovered slot: pools bit-exact, attention within
+    the bar, both tensor-core (G >= 2, D <= 128) and CUDA-core paths."""
+    wl = custom_workload(BS_LENS, H, Hkv, D, dtype, seed=B * 7 + H, block_size=B)
+    got, want = _run_and_check(wl, poison=True)
+    assert max_abs(got, want) <= ATOL
+
+
+@pytest.mark.parametrize("B", [8, 64])
+def test_block_sizes_partition_edges(B):
+    """512-token partitions over 8- and 64-token blocks."""
+    lens = ([511, 512, 513, 1023, 1024, 1025, 1536, 1537, 2047, 2048] * 7)[:64]
+    wl = custom_workload(lens, 40, 40, 128, "f16", seed=B, block_size=B)
+    got, want = _run_and_check(wl)
+    assert max_abs(got, want) <= ATOL
+
+
+@pytest.mark.parametrize("B", [8, 128])
+def test_block_sizes_gqa_workload(B):
+    """The GQA workload (12 query heads on 2 KV heads, bf16) re-laid with
+    other block sizes."""
+    wl = synthetic.relayout(synthetic.make("gqa"), B)
+    got, want = _run_and_check(wl)
+    assert max_abs(got, want) <= ATOL
+
+
+@pytest.mark.parametrize("B", [8, 64, 256])
+def test_copy_blocks_block_sizes_bit_exact(B):
+    import oracle
+    L, NB, Hkv, D = 3, 12, 2, 128
+    g = torch.Generator(device=DEV).manual_seed(B)
+    ks = [torch.randn(NB, Hkv, B, D, generator=g, device=DEV).bfloat16() for _ in range(L)]
+    vs = [torch.randn(NB, Hkv, B, D, generator=g, device=DEV).bfloat16() for _ in range(L)]
+    pairs = np.array([[3, 10], [7, 11], [0, 5]], np.int64)
+    hk = [codes(k) for k in ks]
+    hv = [codes(v) for v in vs]
+    oracle.copy_blocks(hk, hv, pairs)
+    err = _err_word()
+    pa.copy_blocks(ks, vs, torch.as_tensor(pairs, device=DEV), error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for l in range(L):
+        assert np.array_equal(codes(ks[l]), hk[l])
+        assert np.array_equal(codes(vs[l]), hv[l])
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (12, 2)])
+def test_eight_token_blocks_second_block_out_of_range(H, Hkv):
+    """With 8-token blocks a 16-token chunk spans two table entries; a bad
+    id in the second one is flagged and the output stays finite."""
+    wl = custom_workload([40, 40, 40], H, Hkv, 128, "bf16", seed=4, block_size=8)
+    vals = synthetic.make_values(wl, device=DEV)
+    tables = torch.as_tensor(wl.block_tables, device=DEV)
+    tables[1, 3] = wl.num_blocks + 3                   # second block of chunk 1
+    lens = torch.as_tensor(wl.context_lens, device=DEV)
+    err = _err_word()
+    out = pa.decode_attention(vals["q"], vals["k_cache"], vals["v_cache"], tables, lens, 40,
+                              wl.scale, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.ERRBIT_BLOCK_OOB
+    assert torch.all(torch.isfinite(out))
+
+
+def test_unsupported_block_sizes_are_refused():
+    q = torch.zeros(2, 4, 128, dtype=torch.float16, device=DEV)
+    t = torch.zeros(2, 4, dtype=torch.int32, device=DEV)
+    ln = torch.ones(2, dtype=torch.int32, device=DEV)
+    for B in (4, 12, 512):
+        kc = torch.zeros(4, 4, B, 128, dtype=torch.float16, device=DEV)
+        with pytest.raises(pa.PaError) as ei:
+            pa.decode_attention(q, kc, kc, t, ln, 1, 0.1)
+        assert ei.value.status == 2
+        with pytest.raises(pa.PaError) as ei:
+            pa.cache_write(q[:, :4], q[:, :4], kc, kc, torch.zeros(2, dtype=torch.int64,
+                                                                    device=DEV))
+        assert ei.value.status == 2
+
+
+# ---------------------------------------------------------------------------
 # block copy across layers; device-detected errors; host-detected errors
 # ---------------------------------------------------------------------------
 

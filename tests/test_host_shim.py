@@ -157,3 +157,27 @@ def test_lognormal_reading():
     rng = np.random.default_rng(0)
     x = synthetic._lognormal_int(rng, 220.0, 200000, 1, 10 ** 9)
     assert abs(x.mean() / 220.0 - 1) < 0.02
+
+
+@pytest.mark.parametrize("B", [8, 32, 64, 256])
+def test_relayout_keeps_lengths_and_resolves_slots(B):
+    """Re-laying a workload in B-token blocks keeps every length; each
+    sequence gets ceil(L/B) distinct in-range blocks and the step's slot is
+    position L-1 resolved through the new table."""
+    wl = synthetic.make("gqa")
+    r = synthetic.relayout(wl, B)
+    assert r.block_size == B and np.array_equal(r.context_lens, wl.context_lens)
+    assert r.num_blocks * B >= wl.num_blocks * wl.block_size
+    used = []
+    for s in range(r.num_seqs):
+        L = int(r.context_lens[s])
+        nb = blocks_for(L, B)
+        row = r.block_tables[s]
+        assert np.all(row[:nb] >= 0) and np.all(row[:nb] < r.num_blocks)
+        assert np.all(row[nb:] == -1)
+        used.extend(row[:nb].tolist())
+        assert r.slot_mapping[s] == row[(L - 1) // B] * B + (L - 1) % B
+    assert len(set(used)) == len(used)
+    assert r.max_blocks_per_seq * B >= r.max_context_len
+    o = synthetic.in_order(r)
+    assert o.block_size == B and o.block_tables[0, 0] == 0
