@@ -16,6 +16,8 @@ header of ``pa_oracle.c``.  In short:
   the pool's block size, its third dimension).
 * ``copy_blocks``: byte copy of block ``src`` onto block ``dst`` in every
   layer's K and V pool.
+* ``swap_blocks``: the same byte copy between two pools (GPU pool and CPU
+  swap space, either way).
 * ``decode_attention``: softmax(scale * q.K^T) V over the sequence's
   ``context_lens[s]`` tokens reached through ``block_tables[s]``, two-pass,
   accumulated in double.
@@ -76,6 +78,8 @@ def _load():
             lib.pa_oracle_cache_write.argtypes = [P, P, P, P, P, I, I, I, I, I]
             lib.pa_oracle_copy_blocks.restype = I
             lib.pa_oracle_copy_blocks.argtypes = [P, P, I, P, I, I, I, I, I]
+            lib.pa_oracle_swap_blocks.restype = I
+            lib.pa_oracle_swap_blocks.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I]
             attn = [P, P, P, P, P, I, P, I, I, I, I, I, I, ctypes.c_double, I, I]
             lib.pa_oracle_decode_attention.restype = I
             lib.pa_oracle_decode_attention.argtypes = attn
@@ -164,6 +168,25 @@ def copy_blocks(k_caches, v_caches, block_pairs) -> None:
     _check(_load().pa_oracle_copy_blocks(ctypes.cast(kp, ctypes.c_void_p),
                                          ctypes.cast(vp, ctypes.c_void_p), len(ks),
                                          _ptr(pairs), pairs.shape[0], nb, hkv, d, bs))
+
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, block_pairs) -> None:
+    """In place on the destination pools: for every layer,
+    dst[pair dst] = src[pair src] for each (src, dst) row of block_pairs.
+    Source and destination pools may have different block counts."""
+    pairs = np.ascontiguousarray(block_pairs, dtype=np.int64).reshape(-1, 2)
+    dk, dv = [_u16(x) for x in dst_k], [_u16(x) for x in dst_v]
+    sk, sv = [_u16(x) for x in src_k], [_u16(x) for x in src_v]
+    for a, b in zip(dk + dv, list(dst_k) + list(dst_v)):
+        if not np.shares_memory(a, b):
+            raise ValueError("destination pools must be contiguous 16-bit arrays")
+    nd, hkv, bs, d = dk[0].shape
+    ns = sk[0].shape[0]
+    assert sk[0].shape[1:] == (hkv, bs, d)
+    arr = lambda xs: ctypes.cast((ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs]),
+                                 ctypes.c_void_p)
+    _check(_load().pa_oracle_swap_blocks(arr(dk), arr(dv), arr(sk), arr(sv), len(dk),
+                                         _ptr(pairs), pairs.shape[0], nd, ns, hkv, d, bs))
 
 
 def _attn_args(q, k_cache, v_cache, block_tables, context_lens):

@@ -25,6 +25,10 @@
  *
  *   - block copy: for every layer and every (src, dst) pair, block dst of the
  *     K pool and of the V pool becomes a byte copy of block src.
+ *
+ *   - swap: the same byte copy between two pools (the GPU pool and the CPU
+ *     swap space, in either direction): block dst of the destination pool
+ *     becomes a copy of block src of the source pool.
  *     [Efficient Memory Management ..., "Kernel-Level Optimizations", 3. fused
  *     block copy; "Copy-on-write mechanism"]
  *
@@ -192,6 +196,36 @@ int pa_oracle_copy_blocks(uint16_t *const *k_caches, uint16_t *const *v_caches, 
             memcpy(k_caches[l] + (size_t)dst * block_elems, k_caches[l] + (size_t)src * block_elems,
                    sizeof(uint16_t) * block_elems);
             memcpy(v_caches[l] + (size_t)dst * block_elems, v_caches[l] + (size_t)src * block_elems,
+                   sizeof(uint16_t) * block_elems);
+        }
+    }
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Swap: for each layer and pair, dst_pool[dst] = src_pool[src] (K and V),    */
+/* between two pools (GPU pool and CPU swap space, either way).               */
+/* [Efficient Memory Management ..., "Scheduling and Preemption", swapping:   */
+/* evicted blocks are copied to CPU RAM and copied back when the sequence     */
+/* resumes, with a CPU block allocator mirroring the GPU one]                 */
+/* ------------------------------------------------------------------------ */
+int pa_oracle_swap_blocks(uint16_t *const *dst_k, uint16_t *const *dst_v,
+                          const uint16_t *const *src_k, const uint16_t *const *src_v,
+                          int num_layers, const int64_t *block_pairs, int num_pairs,
+                          int num_dst_blocks, int num_src_blocks, int num_kv_heads, int head_dim,
+                          int block_size) {
+    if (num_layers < 0 || num_pairs < 0 || num_dst_blocks <= 0 || num_src_blocks <= 0 ||
+        block_size <= 0)
+        return 1;
+    size_t block_elems = (size_t)num_kv_heads * block_size * head_dim;
+    int rc = 0;
+    for (int l = 0; l < num_layers; ++l) {
+        for (int i = 0; i < num_pairs; ++i) {
+            int64_t src = block_pairs[2 * i], dst = block_pairs[2 * i + 1];
+            if (src < 0 || src >= num_src_blocks || dst < 0 || dst >= num_dst_blocks) { rc = 2; continue; }
+            memcpy(dst_k[l] + (size_t)dst * block_elems, src_k[l] + (size_t)src * block_elems,
+                   sizeof(uint16_t) * block_elems);
+            memcpy(dst_v[l] + (size_t)dst * block_elems, src_v[l] + (size_t)src * block_elems,
                    sizeof(uint16_t) * block_elems);
         }
     }

@@ -448,3 +448,39 @@ def test_pool_layout_matches_kv_size_closed_forms():
             raise AssertionError(unit)
     # the paper summary's own arithmetic: 2 x 5120 x 40 x 2 bytes
     assert 2 * 5120 * 40 * 2 == 40 * (2 * 40 * 128 * 2) == 819200
+
+
+# ---------------------------------------------------------------------------
+# swap between two pools
+# ---------------------------------------------------------------------------
+
+def test_swap_out_and_back_in_restores_the_pool(oracle_mod):
+    """Swap-out copies the named device blocks into free swap blocks, and
+    swap-in of the same pairs reversed brings them back byte for byte; other
+    blocks of both pools are untouched; the pairs map layer by layer."""
+    rng = np.random.default_rng(19)
+    L, ND, NS, Hkv, B, D = 3, 10, 7, 2, 8, 16
+    gk = [rng.integers(0, 1 << 16, (ND, Hkv, B, D), dtype=np.uint16) for _ in range(L)]
+    gv = [rng.integers(0, 1 << 16, (ND, Hkv, B, D), dtype=np.uint16) for _ in range(L)]
+    ck = [rng.integers(0, 1 << 16, (NS, Hkv, B, D), dtype=np.uint16) for _ in range(L)]
+    cv = [rng.integers(0, 1 << 16, (NS, Hkv, B, D), dtype=np.uint16) for _ in range(L)]
+    g0 = [x.copy() for x in gk + gv]
+    c0 = [x.copy() for x in ck + cv]
+    out_pairs = np.array([[9, 0], [2, 5], [4, 3]], np.int64)          # (gpu, cpu)
+    oracle_mod.swap_blocks(ck, cv, gk, gv, out_pairs)
+    for l in range(L):
+        for g, c in out_pairs:
+            assert np.array_equal(ck[l][c], gk[l][g]) and np.array_equal(cv[l][c], gv[l][g])
+        for c in set(range(NS)) - set(out_pairs[:, 1].tolist()):
+            assert np.array_equal(ck[l][c], c0[l][c]) and np.array_equal(cv[l][c], c0[L + l][c])
+    # the GPU blocks are freed and overwritten, then swapped back into other ids
+    for x in gk + gv:
+        x[[9, 2, 4]] = 0
+    in_pairs = np.array([[0, 1], [5, 6], [3, 8]], np.int64)           # (cpu, new gpu)
+    oracle_mod.swap_blocks(gk, gv, ck, cv, in_pairs)
+    for l in range(L):
+        for (g_old, _), (_, g_new) in zip(out_pairs, in_pairs):
+            assert np.array_equal(gk[l][g_new], g0[l][g_old])
+            assert np.array_equal(gv[l][g_new], g0[L + l][g_old])
+    with pytest.raises(oracle_mod.OracleError):
+        oracle_mod.swap_blocks(ck, cv, gk, gv, np.array([[0, NS]], np.int64))
