@@ -357,6 +357,85 @@ def block_size_sweep(args, wl, dev):
                       "steps": args.steps, "results": res}), flush=True)
 
 
+def swap_sweep(args, dev, tokens=2048, layers=40, num_kv_heads=40, head_dim=128):
+    """Swap-out (device pool -> pinned host pool) and swap-in (back, into
+    other block ids) of one request's KV cache over every layer, one
+    pa_swap_blocks call per direction, at block sizes 8 .. 256.  The default
+    request is a full-length OPT-13B-shaped one: 2048 tokens x 40 layers x
+    40 KV heads x 128 x fp16, K and V = 1.68 GB each way.  Device pools hold
+    twice the request's blocks; block ids on both sides are seeded random."""
+    import torch
+    import paged_kv_cache_pa_gb300 as pa
+    row = num_kv_heads * head_dim                     # elements per token per pool
+    dflat = [[torch.randn(2 * tokens * row, device=dev).half() for _ in range(2)]
+             for _ in range(layers)]
+    hflat = [[torch.empty(tokens * row, dtype=torch.float16).pin_memory() for _ in range(2)]
+             for _ in range(layers)]
+    nbytes = 2 * layers * tokens * row * 2
+    res = {}
+    rng = np.random.default_rng(2048)
+    for B in pa.BLOCK_SIZES:
+        nblk = tokens // B
+        gk = [x[0].view(2 * nblk, num_kv_heads, B, head_dim) for x in dflat]
+        gv = [x[1].view(2 * nblk, num_kv_heads, B, head_dim) for x in dflat]
+        ck = [x[0].view(nblk, num_kv_heads, B, head_dim) for x in hflat]
+        cv = [x[1].view(nblk, num_kv_heads, B, head_dim) for x in hflat]
+        host_ids = rng.permutation(nblk)
+        out_p = torch.as_tensor(np.stack([rng.choice(2 * nblk, nblk, replace=False), host_ids], 1),
+                                device=dev)
+        in_p = torch.as_tensor(np.stack([host_ids, rng.choice(2 * nblk, nblk, replace=False)], 1),
+                               device=dev)
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize(dev)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            n = max(5, min(args.steps, 50))
+            a.record()
+            for _ in range(n):
+                fn()
+            b.record()
+            torch.cuda.synchronize(dev)
+            return a.elapsed_time(b) / n
+
+        t_out = timed(lambda: pa.swap_blocks(ck, cv, gk, gv, out_p))
+        t_in = timed(lambda: pa.swap_blocks(gk, gv, ck, cv, in_p))
+        res[f"b{B}"] = {"blocks_per_layer": nblk, "out_ms": round(t_out, 4),
+                        "in_ms": round(t_in, 4), "out_GBps": round(nbytes / t_out / 1e6, 1),
+                        "in_GBps": round(nbytes / t_in / 1e6, 1),
+                        "in_plus_out_ms": round(t_in + t_out, 4)}
+    # reference: the same bytes as one contiguous copy-engine transfer each way
+    del dflat, hflat
+    torch.cuda.empty_cache()
+    dbig = torch.empty(nbytes // 2, dtype=torch.float16, device=dev)
+    hbig = torch.empty(nbytes // 2, dtype=torch.float16).pin_memory()
+
+    def timed_copy(dst, src):
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(10):
+            dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / 10
+
+    t_d2h = timed_copy(hbig, dbig)
+    t_h2d = timed_copy(dbig, hbig)
+    ref = {"d2h_ms": round(t_d2h, 4), "h2d_ms": round(t_h2d, 4),
+           "d2h_GBps": round(nbytes / t_d2h / 1e6, 1), "h2d_GBps": round(nbytes / t_h2d / 1e6, 1)}
+    print(json.dumps({"swap_sweep": f"one {tokens}-token request, {layers} layers, "
+                      f"{num_kv_heads} KV heads x {head_dim}, fp16, K and V",
+                      "bytes_per_direction": nbytes, "host_memory": "pinned (cudaHostAlloc)",
+                      "results": res,
+                      "one_contiguous_copy_engine_transfer": ref}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -372,6 +451,9 @@ def main():
     ap.add_argument("--layout-sweep", action="store_true",
                     help="time the attention call with blocks scattered, blocks in order, and "
                          "on a contiguous (unpaged) cache; prints its own JSON line")
+    ap.add_argument("--swap-sweep", action="store_true",
+                    help="time swap-out and swap-in of one full-length request over all "
+                         "layers at block sizes 8..256; prints its own JSON line")
     ap.add_argument("--block-size-sweep", action="store_true",
                     help="time the attention call with the workload's sequences in blocks of "
                          "8..256 tokens, scattered and in order, against a contiguous cache; "
@@ -408,6 +490,9 @@ def main():
         return
     if args.block_size_sweep:
         block_size_sweep(args, wl, dev)
+        return
+    if args.swap_sweep:
+        swap_sweep(args, dev)
         return
 
     vals = synthetic.make_values(wl, device=dev)

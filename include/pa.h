@@ -14,6 +14,9 @@
  *   pa_decode_attention  fused block read and attention (with context-split
  *                        partitions and a merge for long sequences)
  *   pa_copy_blocks       fused copy-on-write block copy, all pairs and layers
+ * and the pages' other block move:
+ *   pa_swap_blocks       swap-out / swap-in between the GPU pool and a CPU
+ *                        swap space, all pairs and layers
  *
  * Conventions for every entry point:
  *   - Every pointer named "device" is device memory owned by the caller; the
@@ -312,6 +315,46 @@ pa_status_t pa_copy_blocks_ex(void *const *k_caches, void *const *v_caches, int 
                               const int64_t *block_pairs, int num_pairs, int num_blocks,
                               int block_size, int num_kv_heads, int head_dim, pa_dtype_t dtype,
                               unsigned int *dev_error_word, pa_stream_t stream);
+
+/*
+ * pa_swap_blocks -- move whole blocks between two pools, every pair and
+ * every layer in one launch: the swap-out of a preempted sequence's blocks
+ * from the GPU pool to a CPU swap space, and the swap-in that brings them
+ * back when it resumes.
+ *
+ * Defines: for every layer l < num_layers and pair i < num_pairs with
+ * (src, dst) = (block_pairs[2i], block_pairs[2i+1]):
+ *     dst_k_caches[l][dst] = src_k_caches[l][src] and the same for V,
+ * whole blocks (num_kv_heads * block_size * head_dim elements), bytes
+ * unchanged; the source pools are left as they were.
+ * [Efficient Memory Management ..., "Scheduling and Preemption": swapping
+ * copies the evicted blocks to CPU RAM and back to GPU DRAM when the
+ * sequence is rescheduled, with a CPU block allocator beside the GPU one;
+ * the swap-space bound (never more blocks than the GPU pool holds) is the
+ * caller's allocator's to keep]
+ *
+ * dst_k_caches, dst_v_caches, src_k_caches, src_v_caches
+ *               HOST arrays of num_layers pool pointers.  Each pool is
+ *               [num_blocks][num_kv_heads][block_size][head_dim] with
+ *               num_dst_blocks / num_src_blocks blocks, and is either device
+ *               memory of the current device, managed memory, or pinned
+ *               (page-locked, mapped) host memory such as cudaHostAlloc or
+ *               cudaHostRegister gives; the kernel reads and writes host pools
+ *               directly through their device mapping.  Pageable host memory
+ *               is refused (PA_ERR_INVALID_ARG) before anything is enqueued.
+ * block_pairs   int64 [num_pairs][2] (src, dst), device or pinned host memory
+ * block_size    a power of two in [PA_MIN_BLOCK_SIZE, PA_MAX_BLOCK_SIZE]
+ * num_layers    1 .. PA_MAX_LAYERS
+ * Each dst must be distinct; src == dst is a real copy (two pools).  The
+ * host memory must stay pinned until the work on `stream` has finished.
+ * dev_error_word  device, may be NULL: PA_ERRBIT_BLOCK_OOB (pair skipped)
+ */
+pa_status_t pa_swap_blocks(void *const *dst_k_caches, void *const *dst_v_caches,
+                           const void *const *src_k_caches, const void *const *src_v_caches,
+                           int num_layers, const int64_t *block_pairs, int num_pairs,
+                           int num_dst_blocks, int num_src_blocks, int block_size,
+                           int num_kv_heads, int head_dim, pa_dtype_t dtype,
+                           unsigned int *dev_error_word, pa_stream_t stream);
 
 /* Static, human-readable name of a status. */
 const char *pa_status_string(pa_status_t status);

@@ -11,6 +11,7 @@ device, raises.
     decode_attention(query, k_cache, v_cache, block_tables, context_lens,
                      max_context_len, scale, out=None, ...)
     copy_blocks(k_caches, v_caches, block_pairs)
+    swap_blocks(dst_k_caches, dst_v_caches, src_k_caches, src_v_caches, block_pairs)
 
 Pools are [num_blocks][num_kv_heads][block_size][head_dim]; the block size
 is read from their third dimension: 16 goes to the plain entry points, other
@@ -29,7 +30,7 @@ __all__ = ["cache_write", "decode_attention", "decode_attention_contiguous",
            "decode_workspace_size", "decode_partition_tokens", "copy_blocks",
            "status_string", "PaError", "library_path", "load_library", "BLOCK_SIZE",
            "ERRBIT_BLOCK_OOB", "ERRBIT_SLOT_OOB", "ERRBIT_CONTEXT_LEN", "ERRBIT_TIMEOUT",
-           "MAX_LAYERS", "BLOCK_SIZES"]
+           "MAX_LAYERS", "BLOCK_SIZES", "swap_blocks"]
 
 BLOCK_SIZE = 16
 BLOCK_SIZES = (8, 16, 32, 64, 128, 256)
@@ -57,6 +58,7 @@ _SIGNATURES = {
                                             ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P]),
     "pa_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P]),
     "pa_copy_blocks_ex": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "pa_swap_blocks": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -254,3 +256,46 @@ def copy_blocks(k_caches: Sequence, v_caches: Sequence, block_pairs, error_word=
         _check(lib.pa_copy_blocks(*head, *tail), "pa_copy_blocks")
     else:
         _check(lib.pa_copy_blocks_ex(*head, bs, *tail), "pa_copy_blocks_ex")
+
+
+def _pool_ptr(t, name):
+    """Pool pointer for pa_swap_blocks: a CUDA tensor or a pinned CPU tensor."""
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def swap_blocks(dst_k_caches: Sequence, dst_v_caches: Sequence, src_k_caches: Sequence,
+                src_v_caches: Sequence, block_pairs, error_word=None, stream=None) -> None:
+    """For every layer: dst[pair dst] = src[pair src] for each (src, dst) row
+    of block_pairs (int64 [P][2], on the device).  Pools are
+    [num_blocks][Hkv][block_size][D]; either side may be device memory or
+    pinned host memory (the CPU swap space)."""
+    import torch
+    L = len(dst_k_caches)
+    if not (L == len(dst_v_caches) == len(src_k_caches) == len(src_v_caches)) or not L:
+        raise ValueError("need the same, non-zero number of pools on each side")
+    if block_pairs.dtype != torch.int64:
+        raise TypeError("block_pairs must be int64")
+    nd, hkv, bs, d = dst_k_caches[0].shape
+    ns = src_k_caches[0].shape[0]
+    dt = dst_k_caches[0].dtype
+    for c in list(dst_k_caches) + list(dst_v_caches):
+        if tuple(c.shape) != (nd, hkv, bs, d) or c.dtype != dt:
+            raise ValueError("destination pools must have one shape and dtype")
+    for c in list(src_k_caches) + list(src_v_caches):
+        if tuple(c.shape) != (ns, hkv, bs, d) or c.dtype != dt:
+            raise ValueError("source pools must match the destination's block shape and dtype")
+    arr = lambda xs, n: ctypes.cast((ctypes.c_void_p * L)(*[_pool_ptr(x, n) for x in xs]),
+                                    ctypes.c_void_p)
+    npairs = block_pairs.shape[0] if block_pairs.numel() else 0
+    dev = next((c.device for c in [block_pairs] + list(dst_k_caches) + list(src_k_caches)
+                if c.is_cuda), None)
+    st = load_library().pa_swap_blocks(
+        arr(dst_k_caches, "dst_k_caches"), arr(dst_v_caches, "dst_v_caches"),
+        arr(src_k_caches, "src_k_caches"), arr(src_v_caches, "src_v_caches"), L,
+        block_pairs.data_ptr() if npairs else None, npairs, nd, ns, bs, hkv, d, _dtype_code(dt),
+        _opt_ptr(error_word, "error_word"), _stream_ptr(stream, dev))
+    _check(st, "pa_swap_blocks")

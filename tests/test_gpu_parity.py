@@ -355,6 +355,69 @@ def test_host_detected_errors():
 
 
 # ---------------------------------------------------------------------------
+# swap between the device pool and a CPU swap space in pinned host memory
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,dtype", [(8, torch.float16), (16, torch.bfloat16),
+                                     (256, torch.float16)])
+def test_swap_out_and_in_bit_exact(B, dtype):
+    """Swap-out (device -> pinned host) and swap-in (host -> device, into
+    other block ids), all layers in one call each: both pools equal the
+    oracle's byte for byte."""
+    import oracle
+    L, ND, NS, Hkv, D = 3, 24, 16, 4, 128
+    g = torch.Generator(device=DEV).manual_seed(B)
+    gk = [torch.randn(ND, Hkv, B, D, generator=g, device=DEV).to(dtype) for _ in range(L)]
+    gv = [torch.randn(ND, Hkv, B, D, generator=g, device=DEV).to(dtype) for _ in range(L)]
+    ck = [torch.randn(NS, Hkv, B, D).to(dtype).pin_memory() for _ in range(L)]
+    cv = [torch.randn(NS, Hkv, B, D).to(dtype).pin_memory() for _ in range(L)]
+    hgk, hgv = [codes(x) for x in gk], [codes(x) for x in gv]
+    hck = [x.view(torch.int16).numpy().view(np.uint16).copy() for x in ck]
+    hcv = [x.view(torch.int16).numpy().view(np.uint16).copy() for x in cv]
+    rng = np.random.default_rng(B)
+    out_pairs = np.stack([rng.choice(ND, 9, replace=False), rng.choice(NS, 9, replace=False)], 1)
+    in_pairs = np.stack([out_pairs[:, 1], rng.choice(ND, 9, replace=False)], 1)
+    err = _err_word()
+    pa.swap_blocks(ck, cv, gk, gv, torch.as_tensor(out_pairs, device=DEV), error_word=err)
+    oracle.swap_blocks(hck, hcv, hgk, hgv, out_pairs)
+    torch.cuda.synchronize()
+    for l in range(L):
+        assert np.array_equal(ck[l].view(torch.int16).numpy().view(np.uint16), hck[l])
+        assert np.array_equal(cv[l].view(torch.int16).numpy().view(np.uint16), hcv[l])
+    pa.swap_blocks(gk, gv, ck, cv, torch.as_tensor(in_pairs, device=DEV), error_word=err)
+    oracle.swap_blocks(hgk, hgv, hck, hcv, in_pairs)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for l in range(L):
+        assert np.array_equal(codes(gk[l]), hgk[l])
+        assert np.array_equal(codes(gv[l]), hgv[l])
+
+
+def test_swap_bad_pair_is_flagged_and_pageable_memory_refused():
+    ND, NS, Hkv, B, D = 4, 4, 1, 16, 64
+    gk = torch.zeros(ND, Hkv, B, D, dtype=torch.float16, device=DEV)
+    ck = torch.ones(NS, Hkv, B, D, dtype=torch.float16).pin_memory()
+    err = _err_word()
+    pairs = torch.tensor([[0, NS], [1, 2]], dtype=torch.int64, device=DEV)
+    pa.swap_blocks([ck], [ck], [gk], [gk], pairs, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.ERRBIT_BLOCK_OOB
+    assert torch.all(ck[2] == 0) and torch.all(ck[0] == 1) and torch.all(ck[3] == 1)
+    # a pageable host pool is refused on the host, before any launch
+    lib = pa.load_library()
+    import ctypes
+    pageable = np.zeros((NS, Hkv, B, D), np.uint16)
+    arr = (ctypes.c_void_p * 1)(pageable.ctypes.data)
+    dev_arr = (ctypes.c_void_p * 1)(gk.data_ptr())
+    st = lib.pa_swap_blocks(ctypes.cast(arr, ctypes.c_void_p), ctypes.cast(arr, ctypes.c_void_p),
+                            ctypes.cast(dev_arr, ctypes.c_void_p),
+                            ctypes.cast(dev_arr, ctypes.c_void_p), 1, pairs.data_ptr(), 1, NS,
+                            ND, B, Hkv, D, 0, None, None)
+    assert st == 1
+    assert np.all(pageable == 0)
+
+
+# ---------------------------------------------------------------------------
 # contiguous (unpaged) cache: the layout the block table replaces
 # ---------------------------------------------------------------------------
 
