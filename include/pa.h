@@ -65,7 +65,8 @@ typedef enum {
     PA_ERR_UNSUPPORTED = 2,   /* a size this build has no kernel for */
     PA_ERR_CUDA = 3,          /* a CUDA launch or attribute call failed */
     PA_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required */
-    PA_ERR_TIMEOUT = 5        /* reserved: reported through PA_ERRBIT_TIMEOUT */
+    PA_ERR_TIMEOUT = 5,       /* reserved: reported through PA_ERRBIT_TIMEOUT */
+    PA_ERR_NO_BLOCKS = 6      /* block manager (pa_bm.h): not enough free blocks */
 } pa_status_t;
 
 #define PA_BLOCK_SIZE 16

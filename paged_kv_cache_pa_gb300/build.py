@@ -2,8 +2,9 @@
 
     python -m paged_kv_cache_pa_gb300.build [--force]
 
-Every .cu file under csrc/ is compiled in parallel to _build/*.o, then linked
-into paged_kv_cache_pa_gb300/libpa_gb300.so (CUDA runtime linked statically).
+Every .cu file under csrc/ is compiled with nvcc and every .cpp file (host
+code) with g++, in parallel, to _build/*.o, then linked into
+paged_kv_cache_pa_gb300/libpa_gb300.so (CUDA runtime linked statically).
 A stamp of the sources and flags skips the build when nothing changed.
 """
 from __future__ import annotations
@@ -27,6 +28,9 @@ CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptx
                  "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]
 
 
+CXXFLAGS = ["-O2", "-std=c++17", "-fPIC", "-Wall", f"-I{INCLUDE}", f"-I{CSRC}"]
+
+
 def _nvcc() -> str:
     for cand in (os.environ.get("NVCC"), "/usr/local/cuda/bin/nvcc", "nvcc"):
         if cand and (os.path.sep not in cand or os.path.exists(cand)):
@@ -36,9 +40,9 @@ def _nvcc() -> str:
 
 def _stamp(sources) -> str:
     h = hashlib.sha256()
-    h.update(" ".join(CFLAGS).encode())
+    h.update(" ".join(CFLAGS + CXXFLAGS).encode())
     for path in sorted(sources + glob.glob(os.path.join(CSRC, "*.cuh")) +
-                       [os.path.join(INCLUDE, "pa.h")]):
+                       glob.glob(os.path.join(INCLUDE, "*.h"))):
         with open(path, "rb") as f:
             h.update(path.encode())
             h.update(f.read())
@@ -46,7 +50,7 @@ def _stamp(sources) -> str:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     stamp = _stamp(sources)
     stamp_file = LIB + ".stamp"
     if (not force and os.path.exists(LIB) and os.path.exists(stamp_file)
@@ -57,10 +61,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [nvcc] + CFLAGS + ["-c", src, "-o", obj]
+        if src.endswith(".cpp"):
+            cmd = [os.environ.get("CXX", "g++")] + CXXFLAGS + ["-c", src, "-o", obj]
+        else:
+            cmd = [nvcc] + CFLAGS + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"compile failed on {src}:\n{r.stdout}\n{r.stderr}")
         return obj, r.stderr
 
     with ThreadPoolExecutor(max_workers=min(8, len(sources))) as ex:

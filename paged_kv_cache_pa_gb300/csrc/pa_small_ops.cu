@@ -268,6 +268,7 @@ extern "C" const char *pa_status_string(pa_status_t s) {
         case PA_ERR_CUDA: return "PA_ERR_CUDA";
         case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
         case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+        case PA_ERR_NO_BLOCKS: return "PA_ERR_NO_BLOCKS";
     }
     return "PA_ERR_UNKNOWN";
 }
