@@ -21,6 +21,8 @@ header of ``pa_oracle.c``.  In short:
 * ``decode_attention``: softmax(scale * q.K^T) V over the sequence's
   ``context_lens[s]`` tokens reached through ``block_tables[s]``, two-pass,
   accumulated in double.
+* ``prefill_attention``: chunked-prefill attention, each new token over the
+  sequence's positions up to its own (causal), read through the block table.
 * ``decode_attention_blockwise``: the same through per-block partial states
   and a merge (the block-wise form of the attention equation).
 * ``attention_weights``: the normalised weights a_t alongside the output.
@@ -78,6 +80,9 @@ def _load():
             lib.pa_oracle_cache_write.argtypes = [P, P, P, P, P, I, I, I, I, I]
             lib.pa_oracle_copy_blocks.restype = I
             lib.pa_oracle_copy_blocks.argtypes = [P, P, I, P, I, I, I, I, I]
+            lib.pa_oracle_prefill_attention.restype = I
+            lib.pa_oracle_prefill_attention.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I,
+                                                        I, I, ctypes.c_double, I, I]
             lib.pa_oracle_swap_blocks.restype = I
             lib.pa_oracle_swap_blocks.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I]
             attn = [P, P, P, P, P, I, P, I, I, I, I, I, I, ctypes.c_double, I, I]
@@ -209,6 +214,28 @@ def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale: flo
     _check(_load().pa_oracle_decode_attention(
         _ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cl), s, h, hkv,
         d, nb, bs, float(scale), DTYPES[dtype], nthreads or default_threads()))
+    return out
+
+
+def prefill_attention(q, k_cache, v_cache, block_tables, query_start_loc, context_lens,
+                      scale: float, dtype: str, nthreads: int | None = None) -> np.ndarray:
+    """float64 [T][H][D]: chunked-prefill attention.  q [T][H][D] holds the new
+    tokens of every sequence (sequence s: rows query_start_loc[s] ..
+    query_start_loc[s+1]-1), already written to the cache as the sequence's
+    last positions; context_lens[s] counts the tokens after the chunk.  Row
+    i of sequence s attends causally over positions 0 .. context_lens[s] - n_s + i."""
+    q, kc, vc = _u16(q), _u16(k_cache), _u16(v_cache)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    T, H, D = q.shape
+    nb, hkv, bs, d2 = kc.shape
+    S = len(cl)
+    assert d2 == D and vc.shape == kc.shape and qsl.shape == (S + 1,) and bt.shape[0] == S
+    out = np.zeros((T, H, D), np.float64)
+    _check(_load().pa_oracle_prefill_attention(
+        _ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(qsl), _ptr(cl), S, T,
+        H, hkv, D, nb, bs, float(scale), DTYPES[dtype], nthreads or default_threads()))
     return out
 
 

@@ -46,6 +46,11 @@
  *     lookup); Paged Attention: Managing the KV Cache ..., "Attention over
  *     scattered blocks" (row(): block, kv head, offset, dim addressing)]
  *
+ *   - prefill (chunked prefill) attention: the i-th of a sequence's n new
+ *     tokens, at position p = context_lens[s] - n + i, attends causally over
+ *     positions 0 .. p: the decode attention of its query row over the first
+ *     p + 1 tokens of the sequence.
+ *
  *   - block-wise decode attention: the same output computed block by block
  *     with a per-block partial state (max, sum of exponentials, weighted sum of
  *     values) and a final merge, the block-wise form of the attention equation.
@@ -257,11 +262,11 @@ static const uint16_t *token_row(const attn_job *J, const uint16_t *pool, int s,
     return pool + (((size_t)blk * J->num_kv_heads + hk) * B + off) * J->head_dim;
 }
 
-/* Token-wise form: two passes, scores first, then max, exp, sums. */
-static int attend_tokenwise(const attn_job *J, int s, int h, double *x, double *qd, double *o) {
+/* Token-wise form: two passes, scores first, then max, exp, sums, for the
+ * query row qrow (query head h) of sequence s over its first L tokens. */
+static int attend_rows(const attn_job *J, int s, int h, const uint16_t *qrow, int L, double *x,
+                       double *qd, double *o, double *weights_row) {
     const int D = J->head_dim, G = J->num_heads / J->num_kv_heads, hk = h / G;
-    const int L = J->context_lens[s];
-    const uint16_t *qrow = J->q + ((size_t)s * J->num_heads + h) * D;
     for (int d = 0; d < D; ++d) qd[d] = pa_oracle_half_to_double(qrow[d], J->dtype);
     for (int d = 0; d < D; ++d) o[d] = 0.0;
     if (L <= 0) return 0;                                   /* empty context: zeros */
@@ -287,11 +292,16 @@ static int attend_tokenwise(const attn_job *J, int s, int h, double *x, double *
         for (int d = 0; d < D; ++d) o[d] += x[t] * pa_oracle_half_to_double(vrow[d], J->dtype);
     }
     for (int d = 0; d < D; ++d) o[d] /= Z;
-    if (J->weights) {
-        double *w = J->weights + ((size_t)s * J->num_heads + h) * J->max_ctx;
-        for (int t = 0; t < L; ++t) w[t] = x[t] / Z;
-    }
+    if (weights_row)
+        for (int t = 0; t < L; ++t) weights_row[t] = x[t] / Z;
     return 0;
+}
+
+/* Decode: sequence s's one query row per head over its context_lens[s] tokens. */
+static int attend_tokenwise(const attn_job *J, int s, int h, double *x, double *qd, double *o) {
+    const uint16_t *qrow = J->q + ((size_t)s * J->num_heads + h) * J->head_dim;
+    double *w = J->weights ? J->weights + ((size_t)s * J->num_heads + h) * J->max_ctx : NULL;
+    return attend_rows(J, s, h, qrow, J->context_lens[s], x, qd, o, w);
 }
 
 /* Block-wise form: each logical block j yields (m_j, l_j, acc_j) over its own
@@ -407,6 +417,95 @@ static int run_attention(double *out, double *weights, const uint16_t *q,
     int rc = 0;
     for (int i = 0; i < nthreads; ++i) if (jobs[i].rc && !rc) rc = jobs[i].rc;
     free(jobs); free(th);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Prefill (chunked prefill) attention.                                       */
+/* Sequence s has n_s = query_start_loc[s+1] - query_start_loc[s] new tokens, */
+/* already written to the cache as its last n_s positions, so its i-th new    */
+/* token sits at position p = context_lens[s] - n_s + i and attends causally  */
+/* over positions 0 .. p: the decode attention of that row over the first     */
+/* p + 1 tokens.  [Efficient Memory Management ..., "End-to-End Decoding":    */
+/* the prompt phase computes the KV cache of all prompt tokens and attends    */
+/* over them in one pass; vLLM Internals ..., the scheduler's chunked prefill  */
+/* (a prompt processed a token budget at a time)]                              */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    attn_job base;
+    const int32_t *qsl;          /* [num_seqs + 1] */
+    int num_tokens;
+} prefill_job;
+
+static void *prefill_worker(void *arg) {
+    prefill_job *P = (prefill_job *)arg;
+    attn_job *J = &P->base;
+    const int D = J->head_dim;
+    double *x = (double *)malloc(sizeof(double) * (size_t)(J->max_ctx > 1 ? J->max_ctx : 1));
+    double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!x || !qd) {
+        J->rc = 4;
+    } else {
+        const long total = (long)P->num_tokens * J->num_heads;
+        for (long i = J->tid; i < total; i += J->nthreads) {
+            const int t = (int)(i / J->num_heads), h = (int)(i % J->num_heads);
+            int s = 0;
+            while (s + 1 < J->num_seqs && P->qsl[s + 1] <= t) ++s;     /* t's sequence */
+            const int n = P->qsl[s + 1] - P->qsl[s];
+            const int L = J->context_lens[s] - n + (t - P->qsl[s]) + 1;
+            const uint16_t *qrow = J->q + ((size_t)t * J->num_heads + h) * D;
+            int rc = attend_rows(J, s, h, qrow, L, x, qd, J->out + (size_t)i * D, NULL);
+            if (rc && !J->rc) J->rc = rc;
+        }
+    }
+    free(x);
+    free(qd);
+    return NULL;
+}
+
+int pa_oracle_prefill_attention(double *out, const uint16_t *q, const uint16_t *k_cache,
+                                const uint16_t *v_cache, const int32_t *block_tables,
+                                int max_blocks_per_seq, const int32_t *query_start_loc,
+                                const int32_t *context_lens, int num_seqs, int num_tokens,
+                                int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+                                int block_size, double scale, int dtype, int nthreads) {
+    if (num_seqs < 0 || num_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || num_heads % num_kv_heads != 0 || num_blocks <= 0 || block_size <= 0 ||
+        max_blocks_per_seq < 0 || (dtype != ORACLE_F16 && dtype != ORACLE_BF16))
+        return 1;
+    if (query_start_loc[0] != 0 || query_start_loc[num_seqs] != num_tokens) return 1;
+    int max_ctx = 0;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int n = query_start_loc[s + 1] - query_start_loc[s];
+        if (n < 0 || context_lens[s] < n ||
+            (int64_t)context_lens[s] > (int64_t)max_blocks_per_seq * block_size)
+            return 1;
+        if (context_lens[s] > max_ctx) max_ctx = context_lens[s];
+    }
+    if (nthreads < 1) nthreads = 1;
+    prefill_job *jobs = (prefill_job *)calloc((size_t)nthreads, sizeof(prefill_job));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) { free(jobs); free(th); return 4; }
+    for (int i = 0; i < nthreads; ++i) {
+        attn_job J = {out, NULL, q, k_cache, v_cache, block_tables, context_lens,
+                      max_blocks_per_seq, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks,
+                      block_size, max_ctx, dtype, 0, scale, nthreads, i, 0};
+        jobs[i].base = J;
+        jobs[i].qsl = query_start_loc;
+        jobs[i].num_tokens = num_tokens;
+    }
+    int started = 0;
+    for (int i = 1; i < nthreads; ++i) {
+        if (pthread_create(&th[i], NULL, prefill_worker, &jobs[i]) != 0) break;
+        started = i;
+    }
+    for (int i = started + 1; i < nthreads; ++i) prefill_worker(&jobs[i]);
+    prefill_worker(&jobs[0]);
+    for (int i = 1; i <= started; ++i) pthread_join(th[i], NULL);
+    int rc = 0;
+    for (int i = 0; i < nthreads; ++i) if (jobs[i].base.rc && !rc) rc = jobs[i].base.rc;
+    free(jobs);
+    free(th);
     return rc;
 }
 

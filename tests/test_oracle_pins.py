@@ -484,3 +484,66 @@ def test_swap_out_and_back_in_restores_the_pool(oracle_mod):
             assert np.array_equal(gv[l][g_new], g0[L + l][g_old])
     with pytest.raises(oracle_mod.OracleError):
         oracle_mod.swap_blocks(ck, cv, gk, gv, np.array([[0, NS]], np.int64))
+
+
+# ---------------------------------------------------------------------------
+# prefill (chunked prefill) attention
+# ---------------------------------------------------------------------------
+
+def _prefill_problem(rng, cases, H, Hkv, D, B, dtype):
+    """(cached, new) token counts per sequence -> paged pools holding every
+    sequence's full context, q rows of the new tokens, tables, qsl, lens."""
+    S = len(cases)
+    lens = np.array([c + n for c, n in cases], np.int32)
+    qsl = np.concatenate([[0], np.cumsum([n for _, n in cases])]).astype(np.int32)
+    rows_k = [_codes(rng.standard_normal((Hkv, int(L), D)), dtype) for L in lens]
+    rows_v = [_codes(rng.standard_normal((Hkv, int(L), D)), dtype) for L in lens]
+    kc, vc, tables = _relayout(rows_k, rows_v, lens, B, rng)
+    q = _codes(rng.standard_normal((int(qsl[-1]), H, D)), dtype)
+    return q, kc, vc, tables, qsl, lens, rows_k, rows_v
+
+
+@pytest.mark.parametrize("H,Hkv,D,B,dtype", [(4, 4, 16, 16, "f16"), (6, 2, 32, 8, "bf16"),
+                                             (8, 1, 16, 64, "f16")])
+def test_prefill_matches_causal_sdpa(oracle_mod, H, Hkv, D, B, dtype):
+    """Each sequence's new tokens against torch SDPA (CPU float64) on the
+    gathered rows with an explicit causal mask: new token i at position
+    c + i sees keys 0 .. c + i; grouped query heads repeated consecutively."""
+    rng = np.random.default_rng(H * 10 + B)
+    cases = [(0, 1), (0, 37), (20, 16), (100, 33), (5, 70), (64, 1)]
+    q, kc, vc, tables, qsl, lens, rows_k, rows_v = _prefill_problem(rng, cases, H, Hkv, D, B,
+                                                                    dtype)
+    got = oracle_mod.prefill_attention(q, kc, vc, tables, qsl, lens, 0.21, dtype)
+    G = H // Hkv
+    for s, (c, n) in enumerate(cases):
+        K = torch.from_numpy(oracle_mod.half_to_double(rows_k[s], dtype)).repeat_interleave(G, 0)
+        V = torch.from_numpy(oracle_mod.half_to_double(rows_v[s], dtype)).repeat_interleave(G, 0)
+        Q = torch.from_numpy(oracle_mod.half_to_double(q[qsl[s]:qsl[s + 1]], dtype))
+        Q = Q.permute(1, 0, 2)                                     # [H][n][D]
+        mask = torch.arange(c + n)[None, :] <= (c + torch.arange(n))[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=mask,
+                                                               scale=0.21)
+        np.testing.assert_allclose(got[qsl[s]:qsl[s + 1]], ref.permute(1, 0, 2).numpy(),
+                                   rtol=0, atol=1e-12)
+
+
+def test_prefill_in_two_chunks_equals_one(oracle_mod):
+    """Chunked prefill: the same new tokens prefilled in one call, or in two
+    calls whose first covers only the earlier tokens (the cache then holds
+    fewer tokens), give identical rows."""
+    rng = np.random.default_rng(5)
+    H, Hkv, D, B = 4, 2, 16, 16
+    cases = [(10, 50), (0, 33)]
+    q, kc, vc, tables, qsl, lens, _, _ = _prefill_problem(rng, cases, H, Hkv, D, B, "f16")
+    whole = oracle_mod.prefill_attention(q, kc, vc, tables, qsl, lens, 0.3, "f16")
+    first = [20, 12]                                   # new tokens in the first chunk
+    q1 = np.concatenate([q[qsl[s]:qsl[s] + first[s]] for s in range(2)])
+    qsl1 = np.array([0, first[0], first[0] + first[1]], np.int32)
+    lens1 = np.array([cases[s][0] + first[s] for s in range(2)], np.int32)
+    part1 = oracle_mod.prefill_attention(q1, kc, vc, tables, qsl1, lens1, 0.3, "f16")
+    q2 = np.concatenate([q[qsl[s] + first[s]:qsl[s + 1]] for s in range(2)])
+    qsl2 = np.array([0, cases[0][1] - first[0], q2.shape[0]], np.int32)
+    part2 = oracle_mod.prefill_attention(q2, kc, vc, tables, qsl2, lens, 0.3, "f16")
+    for s in range(2):
+        a = np.concatenate([part1[qsl1[s]:qsl1[s + 1]], part2[qsl2[s]:qsl2[s + 1]]])
+        assert np.array_equal(a, whole[qsl[s]:qsl[s + 1]])
