@@ -212,6 +212,55 @@ pa_status_t pa_decode_attention_ex(void *out, pa_dtype_t out_dtype, const void *
                                    unsigned int *dev_error_word, pa_stream_t stream);
 
 /*
+ * pa_prefill_attention -- chunked-prefill attention over the paged KV cache:
+ * every new token of a batch of sequences attends causally over its
+ * sequence's cached tokens up to its own position.
+ *
+ * Defines: sequence s has n_s = query_start_loc[s+1] - query_start_loc[s] new
+ * tokens, query rows query_start_loc[s] .. query_start_loc[s+1]-1, whose K/V
+ * are already in the cache (pa_cache_write) as the sequence's last n_s of
+ * context_lens[s] positions.  New token i (0-based) is at position
+ * p = context_lens[s] - n_s + i, and for query head h (KV head h / G):
+ *     out[t][h] = sum_{j <= p} exp(x_j - max x) v_j / sum_{j <= p} exp(x_j - max x),
+ *     x_j = scale * <query[t][h], k_j>,
+ * with token j of the sequence read at block block_tables[s][j / block_size],
+ * offset j % block_size.  A sequence with n_s = 1 is a decode step; one with
+ * context_lens[s] = n_s is a whole prompt.  fp32 accumulation; P V uses the
+ * probabilities rounded to the operand type (in two parts for bf16).
+ * [Efficient Memory Management ..., "End-to-End Decoding": the prompt phase
+ * computes and stores the KV cache of all prompt tokens and attends over them
+ * in one pass; "PagedAttention Algorithm"; vLLM Internals ..., the
+ * scheduler's chunked prefill, a prompt processed a token budget at a time]
+ *
+ * out           device [num_tokens][num_heads][head_dim], out_dtype = PA_F32
+ *               or the input dtype (round to nearest even)
+ * query         device [num_tokens][num_heads][head_dim], dtype
+ * k_cache, v_cache  device pools [num_blocks][num_kv_heads][block_size][head_dim]
+ * block_tables  device int32 [num_seqs][max_blocks_per_seq]
+ * query_start_loc  device int32 [num_seqs + 1], non-decreasing from 0 to
+ *               num_tokens
+ * context_lens  device int32 [num_seqs], n_s <= context_lens[s] <= max_context_len
+ * max_query_len host-known bound on n_s; max_context_len host-known bound on
+ *               context_lens, <= block_size * max_blocks_per_seq
+ * head_dim 64 or 128 (PA_ERR_UNSUPPORTED otherwise); block_size a power of
+ * two in [PA_MIN_BLOCK_SIZE, PA_MAX_BLOCK_SIZE]; num_heads % num_kv_heads == 0
+ * dev_error_word  device, may be NULL: PA_ERRBIT_CONTEXT_LEN for a sequence
+ *               whose lengths break the rules above (its rows are zeroed),
+ *               PA_ERRBIT_BLOCK_OOB (the chunk's keys are skipped),
+ *               PA_ERRBIT_TIMEOUT.
+ * No workspace.  Enqueues one kernel (one CTA per query head, sequence and 64
+ * new tokens).
+ */
+pa_status_t pa_prefill_attention(void *out, pa_dtype_t out_dtype, const void *query,
+                                 const void *k_cache, const void *v_cache,
+                                 const int32_t *block_tables, int max_blocks_per_seq,
+                                 const int32_t *query_start_loc, const int32_t *context_lens,
+                                 int max_query_len, int max_context_len, int num_seqs,
+                                 int num_tokens, int num_heads, int num_kv_heads, int head_dim,
+                                 int num_blocks, int block_size, float scale, pa_dtype_t dtype,
+                                 unsigned int *dev_error_word, pa_stream_t stream);
+
+/*
  * pa_decode_attention_contiguous -- the same decode attention over a
  * contiguous (unpaged) KV cache: sequence s's tokens for KV head hk are rows
  * 0 .. context_lens[s]-1 of k_cache[s][hk] and v_cache[s][hk]; no block

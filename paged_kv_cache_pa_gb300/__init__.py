@@ -12,6 +12,8 @@ device, raises.
                      max_context_len, scale, out=None, ...)
     copy_blocks(k_caches, v_caches, block_pairs)
     swap_blocks(dst_k_caches, dst_v_caches, src_k_caches, src_v_caches, block_pairs)
+    prefill_attention(query, k_cache, v_cache, block_tables, query_start_loc,
+                      context_lens, max_query_len, max_context_len, scale, ...)
 
 Pools are [num_blocks][num_kv_heads][block_size][head_dim]; the block size
 is read from their third dimension: 16 goes to the plain entry points, other
@@ -30,7 +32,7 @@ __all__ = ["cache_write", "decode_attention", "decode_attention_contiguous",
            "decode_workspace_size", "decode_partition_tokens", "copy_blocks",
            "status_string", "PaError", "library_path", "load_library", "BLOCK_SIZE",
            "ERRBIT_BLOCK_OOB", "ERRBIT_SLOT_OOB", "ERRBIT_CONTEXT_LEN", "ERRBIT_TIMEOUT",
-           "MAX_LAYERS", "BLOCK_SIZES", "swap_blocks"]
+           "MAX_LAYERS", "BLOCK_SIZES", "swap_blocks", "prefill_attention"]
 
 BLOCK_SIZE = 16
 BLOCK_SIZES = (8, 16, 32, 64, 128, 256)
@@ -58,6 +60,8 @@ _SIGNATURES = {
                                             ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P]),
     "pa_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P]),
     "pa_copy_blocks_ex": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "pa_prefill_attention": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I,
+                                  _I, _I, _I, ctypes.c_float, _I, _P, _P]),
     "pa_swap_blocks": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -299,3 +303,36 @@ def swap_blocks(dst_k_caches: Sequence, dst_v_caches: Sequence, src_k_caches: Se
         block_pairs.data_ptr() if npairs else None, npairs, nd, ns, bs, hkv, d, _dtype_code(dt),
         _opt_ptr(error_word, "error_word"), _stream_ptr(stream, dev))
     _check(st, "pa_swap_blocks")
+
+
+def prefill_attention(query, k_cache, v_cache, block_tables, query_start_loc, context_lens,
+                      max_query_len: int, max_context_len: int, scale: float, out=None,
+                      out_dtype=None, error_word=None, stream=None):
+    """Chunked-prefill attention: query [T][H][D] holds every sequence's new
+    tokens (sequence s: rows query_start_loc[s] .. query_start_loc[s+1]-1),
+    already written to the cache as its last positions; context_lens[s]
+    counts the tokens after the chunk.  Returns out [T][H][D]."""
+    import torch
+    T, H, D = query.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if d2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("pool shape mismatch")
+    for t, n in ((block_tables, "block_tables"), (query_start_loc, "query_start_loc"),
+                 (context_lens, "context_lens")):
+        if t.dtype != torch.int32:
+            raise TypeError(f"{n} must be int32")
+    S = context_lens.shape[0]
+    if query_start_loc.shape != (S + 1,) or block_tables.dim() != 2 or \
+            block_tables.shape[0] != S:
+        raise ValueError("query_start_loc must be [S+1], block_tables [S][max_blocks]")
+    if out is None:
+        out = torch.empty(T, H, D, dtype=out_dtype or torch.float32, device=query.device)
+    st = load_library().pa_prefill_attention(
+        _dev(out, "out"), _dtype_code(out.dtype), _dev(query, "query"), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"), block_tables.shape[1],
+        _dev(query_start_loc, "query_start_loc"), _dev(context_lens, "context_lens"),
+        int(max_query_len), int(max_context_len), S, T, H, hkv, D, nb, bs, float(scale),
+        _dtype_code(query.dtype), _opt_ptr(error_word, "error_word"),
+        _stream_ptr(stream, query.device))
+    _check(st, "pa_prefill_attention")
+    return out

@@ -1,0 +1,164 @@
+"""GPU parity for chunked-prefill attention: the chunk's K/V go into the cache
+through pa_cache_write, then pa_prefill_attention runs on the device and the
+oracle runs the same two steps on host copies.  Bars as for decode: pools
+bit-exact, attention max |gpu - oracle| <= 2e-3 on fp32 output."""
+import numpy as np
+import pytest
+import torch
+
+from paritylib import ATOL, codes, max_abs
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU, skipped
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import oracle  # noqa: E402
+import paged_kv_cache_pa_gb300 as pa  # noqa: E402
+
+DEV = torch.device("cuda:0")
+TDT = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def _problem(cases, H, Hkv, D, dtype, B, seed, extra_blocks=3):
+    """(cached, new) per sequence -> device tensors and host copies.  Blocks
+    are scattered; every slot no context covers holds NaN."""
+    rng = np.random.default_rng(seed)
+    S = len(cases)
+    lens = np.array([c + n for c, n in cases], np.int32)
+    qsl = np.concatenate([[0], np.cumsum([n for _, n in cases])]).astype(np.int32)
+    nbs = [-(-int(L) // B) for L in lens]
+    NB = sum(nbs) + extra_blocks
+    perm = rng.permutation(NB)
+    maxb = max(max(nbs), 1)
+    tables = np.full((S, maxb), -1, np.int32)
+    pos = 0
+    for s, n in enumerate(nbs):
+        tables[s, :n] = perm[pos:pos + n]
+        pos += n
+    slots = np.concatenate([tables[s, np.arange(c, c + n) // B].astype(np.int64) * B +
+                            np.arange(c, c + n) % B for s, (c, n) in enumerate(cases)])
+    T = int(qsl[-1])
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    dt = TDT[dtype]
+    kc = torch.randn(NB, Hkv, B, D, generator=g, device=DEV).to(dt)
+    vc = torch.randn(NB, Hkv, B, D, generator=g, device=DEV).to(dt)
+    cover = np.zeros((NB, B), bool)
+    for s, L in enumerate(lens):
+        for t in range(int(L)):
+            cover[tables[s, t // B], t % B] = True
+    cv = torch.as_tensor(cover, device=DEV)[:, None, :, None]
+    nan = torch.tensor(float("nan"), dtype=dt, device=DEV)
+    kc = torch.where(cv, kc, nan).contiguous()
+    vc = torch.where(cv, vc, nan).contiguous()
+    q = torch.randn(T, H, D, generator=g, device=DEV).to(dt)
+    key = torch.randn(T, Hkv, D, generator=g, device=DEV).to(dt)
+    val = torch.randn(T, Hkv, D, generator=g, device=DEV).to(dt)
+    d = dict(q=q, kc=kc, vc=vc, key=key, val=val, tables=tables, qsl=qsl, lens=lens,
+             slots=slots, maxq=max(n for _, n in cases), maxc=int(lens.max()))
+    d["host"] = {k: codes(d[k]) for k in ("q", "kc", "vc", "key", "val")}
+    return d
+
+
+def _run(d, scale, out_dtype=torch.float32, err=None):
+    pa.cache_write(d["key"], d["val"], d["kc"], d["vc"], torch.as_tensor(d["slots"], device=DEV),
+                   error_word=err)
+    return pa.prefill_attention(d["q"], d["kc"], d["vc"], torch.as_tensor(d["tables"], device=DEV),
+                                torch.as_tensor(d["qsl"], device=DEV),
+                                torch.as_tensor(d["lens"], device=DEV), d["maxq"], d["maxc"],
+                                scale, out_dtype=out_dtype, error_word=err)
+
+
+def _oracle(d, scale, dtype):
+    h = d["host"]
+    oracle.cache_write(h["key"], h["val"], h["kc"], h["vc"], d["slots"])
+    return oracle.prefill_attention(h["q"], h["kc"], h["vc"], d["tables"], d["qsl"], d["lens"],
+                                    scale, dtype)
+
+
+CASES = [(0, 1), (0, 64), (0, 65), (0, 200), (37, 1), (100, 16), (500, 130), (63, 64), (1, 127),
+         (64, 64), (15, 49)]
+
+
+@pytest.mark.parametrize("H,Hkv,D,dtype,B", [
+    (8, 8, 128, "f16", 16), (12, 2, 128, "bf16", 16), (8, 2, 64, "f16", 16),
+    (4, 4, 64, "bf16", 8), (12, 2, 128, "bf16", 8), (8, 1, 128, "f16", 64),
+    (6, 3, 64, "bf16", 256),
+])
+def test_prefill_parity(H, Hkv, D, dtype, B):
+    d = _problem(CASES, H, Hkv, D, dtype, B, seed=H * 100 + D + B)
+    scale = 1.0 / np.sqrt(D)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(d, scale, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want = _oracle(d, scale, dtype)
+    assert np.array_equal(codes(d["kc"]), d["host"]["kc"])
+    assert np.array_equal(codes(d["vc"]), d["host"]["vc"])
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    e = max_abs(got, want)
+    print(f"prefill H={H} Hkv={Hkv} D={D} {dtype} B={B}: max|gpu-oracle| = {e:.3e}")
+    assert e <= ATOL
+
+
+def test_prefill_long_mixed_chunks():
+    """A chunked-prefill batch like a scheduler's token budget: long cached
+    prefixes with 512-token chunks, a whole 700-token prompt, decode rows."""
+    cases = [(1536, 512), (0, 700), (3000, 1), (2047, 1), (511, 512), (4000, 96)]
+    d = _problem(cases, 12, 2, 128, "bf16", 16, seed=77)
+    scale = 1.0 / np.sqrt(128)
+    out = _run(d, scale)
+    torch.cuda.synchronize()
+    want = _oracle(d, scale, "bf16")
+    assert max_abs(out.cpu().numpy(), want) <= ATOL
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_prefill_half_output_is_rounded_fp32_output(dtype):
+    cases = [(0, 90), (40, 33)]
+    d = _problem(cases, 8, 2, 128, dtype, 16, seed=3)
+    d2 = {k: (v.clone() if torch.is_tensor(v) else v) for k, v in d.items()}
+    scale = 0.09
+    o32 = _run(d, scale)
+    o16 = _run(d2, scale, out_dtype=TDT[dtype])
+    torch.cuda.synchronize()
+    assert torch.equal(o32.to(TDT[dtype]).view(torch.int16), o16.view(torch.int16))
+
+
+def test_prefill_of_one_token_matches_decode():
+    """Sequences with one new token: the prefill rows agree with decode
+    attention over the same cache (both within the bar of the oracle)."""
+    cases = [(10, 1), (300, 1), (1000, 1), (0, 1)]
+    d = _problem(cases, 12, 2, 128, "bf16", 16, seed=5)
+    scale = 1.0 / np.sqrt(128)
+    out = _run(d, scale)
+    dec = pa.decode_attention(d["q"], d["kc"], d["vc"], torch.as_tensor(d["tables"], device=DEV),
+                              torch.as_tensor(d["lens"], device=DEV), d["maxc"], scale)
+    torch.cuda.synchronize()
+    assert max_abs(out.cpu().numpy(), dec.cpu().numpy()) <= ATOL
+
+
+def test_prefill_errors_are_flagged():
+    cases = [(20, 30), (0, 40), (5, 5)]
+    d = _problem(cases, 4, 2, 64, "f16", 16, seed=9)
+    lens = torch.as_tensor(d["lens"], device=DEV)
+    lens[1] = 10                                   # fewer cached tokens than new ones
+    tables = torch.as_tensor(d["tables"], device=DEV)
+    tables[2, 0] = 10_000                          # a block id past the pool
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = pa.prefill_attention(d["q"], d["kc"], d["vc"], tables,
+                               torch.as_tensor(d["qsl"], device=DEV), lens, d["maxq"], d["maxc"],
+                               0.1, error_word=err)
+    torch.cuda.synchronize()
+    e = int(err.item())
+    assert e & pa.ERRBIT_CONTEXT_LEN and e & pa.ERRBIT_BLOCK_OOB
+    assert torch.all(out[30:70] == 0)              # the bad sequence's rows
+    assert torch.all(torch.isfinite(out))
+    with pytest.raises(pa.PaError) as ei:          # head_dim 256: not built for prefill
+        q = torch.zeros(4, 2, 256, dtype=torch.float16, device=DEV)
+        k = torch.zeros(4, 2, 16, 256, dtype=torch.float16, device=DEV)
+        pa.prefill_attention(q, k, k, tables[:1], torch.tensor([0, 4], dtype=torch.int32,
+                                                               device=DEV),
+                             torch.tensor([4], dtype=torch.int32, device=DEV), 4, 4, 0.1)
+    assert ei.value.status == 2
