@@ -436,6 +436,101 @@ def swap_sweep(args, dev, tokens=2048, layers=40, num_kv_heads=40, head_dim=128)
                       "one_contiguous_copy_engine_transfer": ref}), flush=True)
 
 
+PREFILL_SHAPES = {
+    "opt13b": (40, 40, 128, "f16"),
+    "gqa": (12, 2, 128, "bf16"),
+}
+
+
+def prefill_flops(cached, new, num_heads, head_dim):
+    """Algorithmic FLOPs of causal chunked prefill: new token i of a
+    sequence with c cached tokens sees c + i + 1 keys, each costing 2 D for
+    q.k and 2 D for p.v, per query head."""
+    keys = sum(n * c + n * (n + 1) // 2 for c, n in zip(cached, new))
+    return 4 * head_dim * num_heads * keys
+
+
+def prefill_bench(args, dev):
+    """One chunked-prefill step: 8 sequences, 512 new tokens each, on cached
+    prefixes of 0, 0, 512, 512, 1024, 1024, 1536, 1536 tokens (a 4096-token
+    budget), heads as the named workload; blocks of 16 tokens scattered over
+    the pool.  Times the cache write of the chunk plus the prefill attention,
+    and the attention alone, over back-to-back steps."""
+    import torch
+    import paged_kv_cache_pa_gb300 as pa
+    H, Hkv, D, dtype = PREFILL_SHAPES[args.config]
+    dt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    cached = [0, 0, 512, 512, 1024, 1024, 1536, 1536]
+    new = [512] * 8
+    B = 16
+    lens = np.array([c + n for c, n in zip(cached, new)], np.int32)
+    qsl = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
+    rng = np.random.default_rng(4096)
+    nbs = [-(-int(L) // B) for L in lens]
+    perm = rng.permutation(sum(nbs))
+    maxb = max(nbs)
+    tables = np.full((8, maxb), -1, np.int32)
+    pos = 0
+    for s_, n_ in enumerate(nbs):
+        tables[s_, :n_] = perm[pos:pos + n_]
+        pos += n_
+    slots = np.concatenate([tables[s_, np.arange(c, c + n) // B].astype(np.int64) * B +
+                            np.arange(c, c + n) % B for s_, (c, n) in enumerate(zip(cached, new))])
+    T = int(qsl[-1])
+    g = torch.Generator(device=dev).manual_seed(4096)
+    kc = torch.randn(sum(nbs), Hkv, B, D, generator=g, device=dev).to(dt)
+    vc = torch.randn(sum(nbs), Hkv, B, D, generator=g, device=dev).to(dt)
+    q = torch.randn(T, H, D, generator=g, device=dev).to(dt)
+    key = torch.randn(T, Hkv, D, generator=g, device=dev).to(dt)
+    val = torch.randn(T, Hkv, D, generator=g, device=dev).to(dt)
+    out = torch.empty(T, H, D, dtype=torch.float32, device=dev)
+    t_d = torch.as_tensor(tables, device=dev)
+    q_d = torch.as_tensor(qsl, device=dev)
+    l_d = torch.as_tensor(lens, device=dev)
+    s_d = torch.as_tensor(slots, device=dev)
+    scale = 1.0 / np.sqrt(D)
+
+    def attn():
+        pa.prefill_attention(q, kc, vc, t_d, q_d, l_d, max(new), int(lens.max()), scale, out=out)
+
+    def step():
+        pa.cache_write(key, val, kc, vc, s_d)
+        attn()
+
+    def timed(fn, n):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / n
+
+    n = max(10, min(args.steps, 200))
+    ms_step = timed(step, n)
+    ms_attn = timed(attn, n)
+    flops = prefill_flops(cached, new, H, D)
+    peak = None
+    try:
+        peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"]
+    except (OSError, KeyError, ValueError):
+        peak = 1900.0
+    tf = flops / (ms_attn * 1e-3) / 1e12
+    print(json.dumps({"prefill": args.config,
+                      "workload": f"chunked prefill: 8 sequences x 512 new tokens on cached "
+                                  f"prefixes 0..1536 (4096-token budget), {H} query / {Hkv} KV "
+                                  f"heads, D={D}, {dtype}, block 16, scattered blocks",
+                      "steps": n, "algorithmic_tflop": round(flops / 1e12, 4),
+                      "ms_attention": round(ms_attn, 4), "ms_step": round(ms_step, 4),
+                      "tflops": round(tf, 1), "peak_tflops": peak,
+                      "peak_kind": "measured dense bf16 matmul (burst)",
+                      "frac": round(tf / peak, 4)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -451,6 +546,9 @@ def main():
     ap.add_argument("--layout-sweep", action="store_true",
                     help="time the attention call with blocks scattered, blocks in order, and "
                          "on a contiguous (unpaged) cache; prints its own JSON line")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time a chunked-prefill step (8 x 512 new tokens) with the named "
+                         "workload's heads; prints its own JSON line")
     ap.add_argument("--swap-sweep", action="store_true",
                     help="time swap-out and swap-in of one full-length request over all "
                          "layers at block sizes 8..256; prints its own JSON line")
@@ -493,6 +591,9 @@ def main():
         return
     if args.swap_sweep:
         swap_sweep(args, dev)
+        return
+    if args.prefill:
+        prefill_bench(args, dev)
         return
 
     vals = synthetic.make_values(wl, device=dev)

@@ -11,8 +11,10 @@
 // Algorithm"; vLLM Internals ..., chunked prefill in the scheduler (a prompt
 // processed a token budget at a time)].
 //
-// How: one CTA per (query head h, sequence s, tile of 64 new tokens), the
-// tiles with the most keys launched first.  Warp 0 loads the Q tile with one
+// How: one CTA per (query head h, sequence s, tile of 64 new tokens).  The
+// grid runs the tiles of one (sequence, head) next to each other, heaviest
+// first, and the heads of one KV head side by side, so the K/V tiles they
+// all read come from L2 rather than HBM.  Warp 0 loads the Q tile with one
 // tiled bulk copy (TMA, a 4-D view [head_dim/64][tokens][heads][64] of the
 // query) and then streams 64-token K and V tiles of the sequence -- four
 // 16-row chunks each, every chunk a TMA box of one pool block (two boxes per
@@ -120,9 +122,9 @@ struct PItem {
 
 __device__ __forceinline__ PItem make_item(const PrefillParams &P) {
     PItem it;
-    it.h = blockIdx.x;
-    it.s = blockIdx.y;
-    it.m = (int)gridDim.z - 1 - (int)blockIdx.z;  // heaviest tiles first
+    it.m = (int)gridDim.x - 1 - (int)blockIdx.x;  // heaviest tiles first
+    it.h = blockIdx.y;
+    it.s = blockIdx.z;
     it.hk = it.h / P.G;
     const int a = P.query_start_loc[it.s], b = P.query_start_loc[it.s + 1];
     it.L = P.context_lens[it.s];
@@ -575,7 +577,7 @@ extern "C" pa_status_t pa_prefill_attention(
     if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_INVALID_ARG;
     const long long mtiles = (max_query_len + kPQ - 1) / kPQ;
-    if (num_heads > INT_MAX || num_seqs > 65535 || mtiles > 65535) return PA_ERR_UNSUPPORTED;
+    if (num_heads > 65535 || num_seqs > 65535 || mtiles > INT_MAX) return PA_ERR_UNSUPPORTED;
 
     PrefillParams P;
     memset(&P, 0, sizeof(P));
@@ -616,7 +618,7 @@ extern "C" pa_status_t pa_prefill_attention(
     P.num_blocks = num_blocks;
     P.scale_log2 = scale * 1.4426950408889634f;
     P.err = dev_error_word;
-    const dim3 grid((unsigned)num_heads, (unsigned)num_seqs, (unsigned)mtiles);
+    const dim3 grid((unsigned)mtiles, (unsigned)num_heads, (unsigned)num_seqs);
     cudaStream_t st = (cudaStream_t)stream;
     if (head_dim == 64)
         return dtype == PA_F16 ? launch_prefill<64, __half>(P, grid, st)
