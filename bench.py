@@ -462,7 +462,7 @@ def prefill_bench(args, dev):
     dt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
     cached = [0, 0, 512, 512, 1024, 1024, 1536, 1536]
     new = [512] * 8
-    B = 16
+    B = args.prefill_block_size
     lens = np.array([c + n for c, n in zip(cached, new)], np.int32)
     qsl = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
     rng = np.random.default_rng(4096)
@@ -523,7 +523,7 @@ def prefill_bench(args, dev):
     print(json.dumps({"prefill": args.config,
                       "workload": f"chunked prefill: 8 sequences x 512 new tokens on cached "
                                   f"prefixes 0..1536 (4096-token budget), {H} query / {Hkv} KV "
-                                  f"heads, D={D}, {dtype}, block 16, scattered blocks",
+                                  f"heads, D={D}, {dtype}, block {B}, scattered blocks",
                       "steps": n, "algorithmic_tflop": round(flops / 1e12, 4),
                       "ms_attention": round(ms_attn, 4), "ms_step": round(ms_step, 4),
                       "tflops": round(tf, 1), "peak_tflops": peak,
@@ -541,6 +541,8 @@ def main():
     ap.add_argument("--seqs", type=int, default=0,
                     help="batch size override (smaller cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="e2e leg: launch the steps eagerly instead of replaying a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layout-sweep", action="store_true",
@@ -549,6 +551,8 @@ def main():
     ap.add_argument("--prefill", action="store_true",
                     help="time a chunked-prefill step (8 x 512 new tokens) with the named "
                          "workload's heads; prints its own JSON line")
+    ap.add_argument("--prefill-block-size", type=int, default=16,
+                    help="tokens per block for --prefill (8 .. 256)")
     ap.add_argument("--swap-sweep", action="store_true",
                     help="time swap-out and swap-in of one full-length request over all "
                          "layers at block sizes 8..256; prints its own JSON line")
@@ -668,9 +672,11 @@ def main():
     attn_gbs = b_attn / (attn_ms * 1e-3) / 1e9
     peak, peak_kind = peaks()
 
-    # end to end through the Python API: the step's inputs go host -> device
-    # in one copy from a pinned staging buffer, the output comes back to
-    # pinned host memory; the KV pools are the cache and stay resident
+    # end to end through the Python API: every step's inputs go host -> device
+    # in one copy from a pinned staging buffer and its output comes back to
+    # pinned host memory, the copies of neighbouring steps overlapping the
+    # compute as a serving loop would; the KV pools are the cache and stay
+    # resident
     e2e = None
     if not args.no_e2e:
         host_parts = [vals["q"].cpu(), vals["key"].cpu(), vals["value"].cpu(),
@@ -684,38 +690,107 @@ def main():
         for t, o in zip(host_parts, offs):
             nb = t.numel() * t.element_size()
             staging[o:o + nb].copy_(t.contiguous().view(-1).view(torch.uint8))
-        hout = torch.empty(S, H, D, dtype=torch.float32).pin_memory()
         h2d = int(total)
-        d2h = hout.numel() * hout.element_size()
+        d2h = S * H * D * 4
 
-        dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
-        q_d, k_d, v_d, s_d, t_d, l_d = [
-            dev_buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-            for t, o in zip(host_parts, offs)]
+        # Two sets of device inputs and outputs: step i+1's inputs go host ->
+        # device and step i-1's output device -> host on a copy stream while
+        # step i computes; events order the reuse of each buffer.
+        copy_stream = torch.cuda.Stream(dev)
+        hout = [torch.empty(S, H, D, dtype=torch.float32).pin_memory() for _ in range(2)]
+        outs = [torch.empty(S, H, D, dtype=torch.float32, device=dev) for _ in range(2)]
+        bufs, views = [], []
+        for _ in range(2):
+            b_ = torch.empty(total, dtype=torch.uint8, device=dev)
+            bufs.append(b_)
+            views.append([b_[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                          for t, o in zip(host_parts, offs)])
+        ev = lambda: torch.cuda.Event()
+        h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
 
-        def e2e_step():
-            dev_buf.copy_(staging, non_blocking=True)
-            if pairs is not None:
-                pa.copy_blocks([vals["k_cache"]], [vals["v_cache"]], pairs)
-            pa.cache_write(k_d, v_d, vals["k_cache"], vals["v_cache"], s_d)
-            o = pa.decode_attention(q_d, vals["k_cache"], vals["v_cache"], t_d, l_d,
-                                    wl.max_context_len, wl.scale, out=out, workspace=ws)
-            hout.copy_(o, non_blocking=True)
+        def pipeline(n):
+            # n steps; step i's inputs and step i-1's output move on the copy
+            # stream while step i computes on `stream`
+            cs = torch.cuda.current_stream(dev)
+            for i in range(n + 1):
+                b = i % 2
+                if i < n:
+                    with torch.cuda.stream(copy_stream):
+                        if i >= 2:
+                            copy_stream.wait_event(comp_done[b])   # step i-2 read bufs[b]
+                        bufs[b].copy_(staging, non_blocking=True)
+                        h2d_done[b].record(copy_stream)
+                    cs.wait_event(h2d_done[b])
+                    if i >= 2:
+                        cs.wait_event(d2h_done[b])                  # outs[b] read back
+                    q_d, k_d, v_d, s_d, t_d, l_d = views[b]
+                    if pairs is not None:
+                        pa.copy_blocks([vals["k_cache"]], [vals["v_cache"]], pairs)
+                    pa.cache_write(k_d, v_d, vals["k_cache"], vals["v_cache"], s_d)
+                    pa.decode_attention(q_d, vals["k_cache"], vals["v_cache"], t_d, l_d,
+                                        wl.max_context_len, wl.scale, out=outs[b], workspace=ws)
+                    comp_done[b].record(cs)
+                if i >= 1:  # the previous step's result back to the host
+                    pb = (i - 1) % 2
+                    with torch.cuda.stream(copy_stream):
+                        copy_stream.wait_event(comp_done[pb])
+                        hout[pb].copy_(outs[pb], non_blocking=True)
+                        d2h_done[pb].record(copy_stream)
 
-        for _ in range(3):
-            e2e_step()
-        barrier()
+        def e2e_steps(n, t_start=None, t_end=None):
+            stream.synchronize()
+            if t_start is not None:
+                t_start.record(copy_stream)
+            pipeline(n)
+            if t_end is not None:
+                t_end.record(copy_stream)
+            copy_stream.synchronize()
+            stream.synchronize()
+
+        # Short steps are bound by the host's launch overhead: capture 25
+        # pipelined steps (the same public calls and copies) in a CUDA graph
+        # and replay it; fall back to the eager loop if capture fails.
+        kg = 25
+        graph, launch = None, "eager"
+        if not args.no_graph:
+            try:
+                e2e_steps(3)
+                g_ = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g_):
+                    cap = torch.cuda.current_stream(dev)
+                    copy_stream.wait_stream(cap)
+                    pipeline(kg)
+                    cap.wait_stream(copy_stream)
+                g_.replay()
+                torch.cuda.synchronize(dev)
+                graph, launch = g_, f"CUDA graph of {kg} pipelined steps"
+            except Exception as exc:  # capture not possible here: eager loop
+                graph = None
+                launch = f"eager (graph capture failed: {type(exc).__name__})"
+                torch.cuda.synchronize(dev)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        barrier()
-        e_ms = reduce_max(e0.elapsed_time(e1) / args.e2e_steps, dist, dev)
+        if graph is not None:
+            reps = max(1, args.e2e_steps // kg)
+            for _ in range(3):
+                graph.replay()
+            barrier()
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
+            barrier()
+            n_e2e = reps * kg
+        else:
+            e2e_steps(3)
+            barrier()
+            e2e_steps(args.e2e_steps, e0, e1)
+            barrier()
+            n_e2e = args.e2e_steps
+        e_ms = reduce_max(e0.elapsed_time(e1) / n_e2e, dist, dev)
         e2e = {"value": round(world * b_step / (e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": round(e_ms, 4)}
+               "ms_per_step": round(e_ms, 4), "steps": n_e2e, "launch": launch}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
