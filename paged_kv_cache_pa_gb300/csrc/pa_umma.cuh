@@ -4,7 +4,8 @@
 // and stores.  Device code only.
 //
 // Operand layouts used here (16-bit elements, 128-byte swizzle, 1024-byte
-// aligned tiles):
+// aligned tiles; an A operand may instead sit in tensor memory, see
+// umma_f16_tmem_a):
 //   K-major [rows][64] per 64-element slice of K: row r at r * 128 bytes, the
 //     16-byte chunk c of a row at (c ^ (r % 8)) * 16; 8-row groups 1024
 //     bytes apart (the descriptor's stride byte offset); the next 64 K
@@ -71,6 +72,19 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A * B with A read from tensor memory: row i of A in lane i,
+// two 16-bit elements per 32-bit column, the lower-indexed element in the low
+// half; one K = 16 step spans 8 columns.  B from a shared-memory descriptor.
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
