@@ -490,8 +490,12 @@ def prefill_bench(args, dev):
     s_d = torch.as_tensor(slots, device=dev)
     scale = 1.0 / np.sqrt(D)
 
+    ws = torch.empty(max(256, pa.prefill_workspace_size(8, H, Hkv, max(new))), dtype=torch.uint8,
+                     device=dev)
+
     def attn():
-        pa.prefill_attention(q, kc, vc, t_d, q_d, l_d, max(new), int(lens.max()), scale, out=out)
+        pa.prefill_attention(q, kc, vc, t_d, q_d, l_d, max(new), int(lens.max()), scale, out=out,
+                             workspace=ws)
 
     def step():
         pa.cache_write(key, val, kc, vc, s_d)

@@ -212,6 +212,14 @@ pa_status_t pa_decode_attention_ex(void *out, pa_dtype_t out_dtype, const void *
                                    unsigned int *dev_error_word, pa_stream_t stream);
 
 /*
+ * pa_prefill_workspace_size -- bytes of device workspace pa_prefill_attention
+ * needs for these sizes (the work list: 4 bytes per work item plus 8); 0 if
+ * the sizes are invalid.  Host only, no CUDA calls.
+ */
+size_t pa_prefill_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                 int max_query_len);
+
+/*
  * pa_prefill_attention -- chunked-prefill attention over the paged KV cache:
  * every new token of a batch of sequences attends causally over its
  * sequence's cached tokens up to its own position.
@@ -244,12 +252,17 @@ pa_status_t pa_decode_attention_ex(void *out, pa_dtype_t out_dtype, const void *
  *               context_lens, <= block_size * max_blocks_per_seq
  * head_dim 64 or 128 (PA_ERR_UNSUPPORTED otherwise); block_size a power of
  * two in [PA_MIN_BLOCK_SIZE, PA_MAX_BLOCK_SIZE]; num_heads % num_kv_heads == 0
+ * workspace     device, >= pa_prefill_workspace_size(...) bytes, 256-byte
+ *               aligned (PA_ERR_WORKSPACE otherwise); holds the work list.
+ *               Calls in flight at once must not share one workspace.
  * dev_error_word  device, may be NULL: PA_ERRBIT_CONTEXT_LEN for a sequence
  *               whose lengths break the rules above (its rows are zeroed),
- *               PA_ERRBIT_BLOCK_OOB (the chunk's keys are skipped),
+ *               PA_ERRBIT_BLOCK_OOB (the block's keys are skipped),
  *               PA_ERRBIT_TIMEOUT.
- * No workspace.  Enqueues one kernel (one CTA per query head, sequence and 64
- * new tokens).
+ * Enqueues two kernels: a plan (one CTA: the work items -- two 128-token
+ * query tiles that read the same keys -- that have work, heaviest first) and
+ * the attention kernel (persistent, one CTA per SM, taking items from the
+ * list in order).
  */
 pa_status_t pa_prefill_attention(void *out, pa_dtype_t out_dtype, const void *query,
                                  const void *k_cache, const void *v_cache,
@@ -257,7 +270,7 @@ pa_status_t pa_prefill_attention(void *out, pa_dtype_t out_dtype, const void *qu
                                  const int32_t *query_start_loc, const int32_t *context_lens,
                                  int max_query_len, int max_context_len, int num_seqs,
                                  int num_tokens, int num_heads, int num_kv_heads, int head_dim,
-                                 int num_blocks, int block_size, float scale, pa_dtype_t dtype,
+                                 int num_blocks, int block_size, float scale, pa_dtype_t dtype, void *workspace, size_t workspace_bytes,
                                  unsigned int *dev_error_word, pa_stream_t stream);
 
 /*

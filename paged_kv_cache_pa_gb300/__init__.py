@@ -61,7 +61,8 @@ _SIGNATURES = {
     "pa_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P]),
     "pa_copy_blocks_ex": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pa_prefill_attention": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I,
-                                  _I, _I, _I, ctypes.c_float, _I, _P, _P]),
+                                  _I, _I, _I, ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P]),
+    "pa_prefill_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "pa_swap_blocks": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -305,13 +306,21 @@ def swap_blocks(dst_k_caches: Sequence, dst_v_caches: Sequence, src_k_caches: Se
     _check(st, "pa_swap_blocks")
 
 
+def prefill_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int,
+                           max_query_len: int) -> int:
+    return int(load_library().pa_prefill_workspace_size(num_seqs, num_heads, num_kv_heads,
+                                                        max_query_len))
+
+
 def prefill_attention(query, k_cache, v_cache, block_tables, query_start_loc, context_lens,
                       max_query_len: int, max_context_len: int, scale: float, out=None,
-                      out_dtype=None, error_word=None, stream=None):
+                      out_dtype=None, workspace=None, error_word=None, stream=None):
     """Chunked-prefill attention: query [T][H][D] holds every sequence's new
     tokens (sequence s: rows query_start_loc[s] .. query_start_loc[s+1]-1),
     already written to the cache as its last positions; context_lens[s]
-    counts the tokens after the chunk.  Returns out [T][H][D]."""
+    counts the tokens after the chunk.  ``workspace`` (uint8, >=
+    prefill_workspace_size bytes) is allocated here when not given.  Returns
+    out [T][H][D]."""
     import torch
     T, H, D = query.shape
     nb, hkv, bs, d2 = k_cache.shape
@@ -327,12 +336,16 @@ def prefill_attention(query, k_cache, v_cache, block_tables, query_start_loc, co
         raise ValueError("query_start_loc must be [S+1], block_tables [S][max_blocks]")
     if out is None:
         out = torch.empty(T, H, D, dtype=out_dtype or torch.float32, device=query.device)
+    if workspace is None:
+        nbytes = prefill_workspace_size(S, H, hkv, int(max_query_len))
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=query.device)
     st = load_library().pa_prefill_attention(
         _dev(out, "out"), _dtype_code(out.dtype), _dev(query, "query"), _dev(k_cache, "k_cache"),
         _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"), block_tables.shape[1],
         _dev(query_start_loc, "query_start_loc"), _dev(context_lens, "context_lens"),
         int(max_query_len), int(max_context_len), S, T, H, hkv, D, nb, bs, float(scale),
-        _dtype_code(query.dtype), _opt_ptr(error_word, "error_word"),
+        _dtype_code(query.dtype), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _opt_ptr(error_word, "error_word"),
         _stream_ptr(stream, query.device))
     _check(st, "pa_prefill_attention")
     return out

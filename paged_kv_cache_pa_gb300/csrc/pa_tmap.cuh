@@ -31,19 +31,21 @@ inline EncodeTiledFn tmap_encoder() {
     return reinterpret_cast<EncodeTiledFn>(f);
 }
 
-// A tiled map of a 16-bit tensor with `rank` dimensions (innermost first),
-// byte strides of dimensions 1.. , a box, and the 128-byte swizzle; reads
-// outside the tensor return zeros.
+// A tiled map of an fp32, fp16 or bf16 tensor with `rank` dimensions
+// (innermost first), byte strides of dimensions 1.. , a box, and the 128-byte
+// swizzle; reads outside the tensor return zeros, stores outside it are
+// dropped.
 inline bool encode_tiled(CUtensorMap *map, const void *base, pa_dtype_t dtype, int rank,
                          const cuuint64_t *dims, const cuuint64_t *strides,
                          const cuuint32_t *box) {
     EncodeTiledFn enc = tmap_encoder();
     if (!enc) return false;
     const cuuint32_t elem_strides[5] = {1u, 1u, 1u, 1u, 1u};
-    return enc(map,
-               dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-               (cuuint32_t)rank, const_cast<void *>(base), dims, strides, box, elem_strides,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    const CUtensorMapDataType ty = dtype == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return enc(map, ty, (cuuint32_t)rank, const_cast<void *>(base), dims, strides, box,
+               elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -60,13 +60,13 @@ def _problem(cases, H, Hkv, D, dtype, B, seed, extra_blocks=3):
     return d
 
 
-def _run(d, scale, out_dtype=torch.float32, err=None):
+def _run(d, scale, out_dtype=torch.float32, err=None, workspace=None):
     pa.cache_write(d["key"], d["val"], d["kc"], d["vc"], torch.as_tensor(d["slots"], device=DEV),
                    error_word=err)
     return pa.prefill_attention(d["q"], d["kc"], d["vc"], torch.as_tensor(d["tables"], device=DEV),
                                 torch.as_tensor(d["qsl"], device=DEV),
                                 torch.as_tensor(d["lens"], device=DEV), d["maxq"], d["maxc"],
-                                scale, out_dtype=out_dtype, error_word=err)
+                                scale, out_dtype=out_dtype, workspace=workspace, error_word=err)
 
 
 def _oracle(d, scale, dtype):
@@ -162,3 +162,51 @@ def test_prefill_errors_are_flagged():
                                                                device=DEV),
                              torch.tensor([4], dtype=torch.int32, device=DEV), 4, 4, 0.1)
     assert ei.value.status == 2
+
+
+@pytest.mark.parametrize("H,Hkv,dtype", [(8, 2, "bf16"), (6, 6, "f16"), (9, 3, "bf16")])
+def test_prefill_many_items_per_cta(H, Hkv, dtype):
+    """Far more work items (query-tile pairs) than SMs, of very different
+    lengths: the persistent CTAs take several items each, heaviest first, and
+    every pipeline runs on across items.  The same workspace serves two
+    calls (the plan resets the claim counter)."""
+    rng = np.random.default_rng(H * 7 + Hkv)
+    cases = [(int(rng.integers(0, 600)), int(rng.integers(1, 330))) for _ in range(48)]
+    cases[5] = (0, 384)                      # exactly three query tiles
+    cases[11] = (700, 1)                     # decode rows among the chunks
+    d = _problem(cases, H, Hkv, 128, dtype, 16, seed=H + Hkv)
+    maxq = d["maxq"]
+    nbytes = pa.prefill_workspace_size(len(cases), H, Hkv, maxq)
+    mt = -(-maxq // 128)
+    ix, iy = (mt, H // 2) if (H // Hkv) % 2 == 0 else (-(-mt // 2), H)
+    assert nbytes >= 4 * (2 + len(cases) * ix * iy) and nbytes % 256 == 0
+    assert len(cases) * ix * iy > 2 * 152
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    scale = 1.0 / np.sqrt(128)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(d, scale, err=err, workspace=ws)
+    out2 = pa.prefill_attention(d["q"], d["kc"], d["vc"], torch.as_tensor(d["tables"], device=DEV),
+                                torch.as_tensor(d["qsl"], device=DEV),
+                                torch.as_tensor(d["lens"], device=DEV), maxq, d["maxc"], scale,
+                                workspace=ws, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want = _oracle(d, scale, dtype)
+    e = max_abs(out.cpu().numpy(), want)
+    print(f"many items H={H} Hkv={Hkv} {dtype}: max|gpu-oracle| = {e:.3e}")
+    assert e <= ATOL
+    assert torch.equal(out, out2)           # same arithmetic whatever CTA took an item
+
+
+def test_prefill_workspace_checks():
+    cases = [(10, 20), (0, 5)]
+    d = _problem(cases, 4, 2, 64, "f16", 16, seed=1)
+    need = pa.prefill_workspace_size(2, 4, 2, d["maxq"])
+    assert need == 256                       # 2 header words + 2 x 1 x 2 items, rounded up
+    assert pa.prefill_workspace_size(2, 5, 2, 10) == 0      # heads not a multiple of KV heads
+    small = torch.empty(need, dtype=torch.uint8, device=DEV)[1:]    # misaligned
+    with pytest.raises(pa.PaError) as ei:
+        _run(d, 0.1, workspace=small)
+    assert ei.value.status == 4
+    big = pa.prefill_workspace_size(2, 4, 2, 100_000)
+    assert big > need
