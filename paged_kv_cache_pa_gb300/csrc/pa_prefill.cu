@@ -897,18 +897,30 @@ __device__ __forceinline__ void run_softmax_p(const PrefillParams &P, int t, con
             float mxa[kAcc];
 #pragma unroll
             for (int q = 0; q < kAcc; ++q) mxa[q] = m_ref;
-            if (!bits && kb + kKN - 1 <= qpos) {  // every key of the tile is visible
+            // the masked form is taken by the whole warp or not at all (a
+            // warp on the diagonal would otherwise run both)
+            if (__all_sync(0xffffffffu, !bits && kb + kKN - 1 <= qpos)) {  // all keys visible
 #pragma unroll
                 for (int e = 0; e < kKN; ++e) {
                     s[e] *= sc;
                     mxa[e % kAcc] = fmaxf(mxa[e % kAcc], s[e]);
                 }
             } else {
+                // keys kb .. kb + nvis - 1 are at or before the row's position
+                const int nvis = max(0, min(kKN, qpos - kb + 1));
+                if (!bits) {  // (bits is the same in every lane)
 #pragma unroll
-                for (int e = 0; e < kKN; ++e) {
-                    const bool masked = kb + e > qpos || ((bits >> (e >> g.lg_tbr)) & 1u);
-                    s[e] = masked ? -INFINITY : s[e] * sc;
-                    mxa[e % kAcc] = fmaxf(mxa[e % kAcc], s[e]);
+                    for (int e = 0; e < kKN; ++e) {
+                        s[e] = e >= nvis ? -INFINITY : s[e] * sc;
+                        mxa[e % kAcc] = fmaxf(mxa[e % kAcc], s[e]);
+                    }
+                } else {  // and the keys of skipped blocks
+#pragma unroll
+                    for (int e = 0; e < kKN; ++e) {
+                        const bool masked = e >= nvis || ((bits >> (e >> g.lg_tbr)) & 1u);
+                        s[e] = masked ? -INFINITY : s[e] * sc;
+                        mxa[e % kAcc] = fmaxf(mxa[e % kAcc], s[e]);
+                    }
                 }
             }
 #pragma unroll
