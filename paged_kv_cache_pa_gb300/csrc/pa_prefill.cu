@@ -156,7 +156,8 @@ struct PLayout {
     static constexpr size_t k_off = stage_off + (size_t)kSoftmaxWarps * kStageWarpBytes;
     static constexpr size_t v_off = k_off + (size_t)RK * tile_bytes;
     static constexpr size_t item_off = v_off + (size_t)RV * tile_bytes;   // two PItem slots
-    static constexpr size_t bar_off = (item_off + 2 * sizeof(PItem) + 7) / 8 * 8;
+    static constexpr size_t tag_off = item_off + 2 * sizeof(PItem);        // int [RK + RV]
+    static constexpr size_t bar_off = (tag_off + 4 * (RK + RV) + 7) / 8 * 8;
     // q_full[2], q_free[2], k_full[RK], k_empty[RK], v_full[RV], v_empty[RV],
     // v_land, item_full[2], item_empty[2], s_full[2], s_free[2], p_full[2][2],
     // pv_done[2][2], o_free[2], o_done[2][2]
@@ -169,6 +170,9 @@ struct PLayout {
 };
 
 struct Bars {
+    // k_tag[s] / v_tag[s]: the K/V tile (counted from the CTA's first) the
+    // producer last armed stage s with, written before the arming arrival
+    volatile int *k_tag, *v_tag;
     uint64_t *q_full, *q_free;                // [2 tiles]
     uint64_t *k_full, *k_empty, *v_full, *v_empty, *v_land;
     uint64_t *item_full, *item_empty;         // [2 slots]
@@ -316,6 +320,26 @@ __device__ __forceinline__ const PItem *take_item(const PItem *items, const Bars
 __device__ __forceinline__ void give_item_back(const Bars &B, int n, int lane, unsigned mask) {
     __syncwarp(mask);
     if (lane == 0) mbar_arrive(&B.item_empty[n & 1]);
+}
+
+// Wait until K/V tile q (counted from the CTA's first) has landed in stage
+// q % R.  A consumer that skips stages (its query tile needs fewer K/V tiles
+// than the item's other one) can be a whole ring ahead of the producer, and
+// then the parity of the phase it waits for is also the parity of the phase
+// before; the stage's tag tells the two apart.
+__device__ __forceinline__ bool wait_tile(uint64_t *full, volatile int *tag, int q, int R,
+                                          volatile int *abort_flag) {
+    const int st = q % R;
+    const uint32_t parity = (uint32_t)(q / R) & 1u;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t polls = 0; polls < kWaitLimitPolls; ++polls) {
+        if (mbar_try_wait(&full[st], parity) && tag[st] == q) return true;
+        if ((polls & 31u) == 31u) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
+    return false;
 }
 
 // What the softmax needs of an item's sequence.
@@ -466,7 +490,10 @@ __device__ __forceinline__ bool produce_item(const PrefillParams &P, const KVIte
         }
         uint64_t *bar = tail ? B.v_land : &full[slot];
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(bar, tx);
+        if (lane == 0) {
+            (kIsV ? B.v_tag : B.k_tag)[slot] = rc;  // before the arrival that arms the stage
+            mbar_arrive_expect_tx(bar, tx);
+        }
         __syncwarp();
         if (issue) tma_load_3d(st + off, tmap, 0, y, sl, bar, policy);
         __syncwarp();
@@ -665,20 +692,24 @@ __device__ __forceinline__ void run_mma_p(const PrefillParams &P, int t, int pv,
         if (stop) break;
         if (!iok) continue;
         // A K/V stage is released by two arrivals, one per tile; past the
-        // other tile's last K/V tile this issuer gives both.
+        // other tile's last K/V tile this issuer gives both.  An issuer never
+        // arrives for a stage before it has seen that stage's tile land
+        // (wait_tile), so its arrival cannot fall into an earlier phase.
         auto release = [&](uint64_t *bar, int j) {
             umma_commit(bar);
             if (j >= nt_other) umma_commit(bar);
         };
-        if (!pv && nt > 0) {
-            ok = mbar_wait(&B.q_full[t], (uint32_t)qa & 1u, abort_flag);
-            tc_fence_after();
+        if (!pv) {
+            if (nt > 0) {
+                ok = mbar_wait(&B.q_full[t], (uint32_t)qa & 1u, abort_flag);
+                tc_fence_after();
+            }
             // S_j into the tile's S buffer once the softmax has loaded the
             // previous S.  A K step of 16 is 32 bytes inside a 64-element
             // slice; slices are whole tiles apart.
             for (int j = 0; ok && j < nt; ++j, ++sc) {
                 const int q = rc + j, ks = q % RK;
-                ok = mbar_wait(&B.k_full[ks], (uint32_t)(q / RK) & 1u, abort_flag) &&
+                ok = wait_tile(B.k_full, B.k_tag, q, RK, abort_flag) &&
                      (sc == 0 || mbar_wait(&B.s_free[t], (uint32_t)(sc - 1) & 1u, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
@@ -695,16 +726,18 @@ __device__ __forceinline__ void run_mma_p(const PrefillParams &P, int t, int pv,
                 umma_commit(&B.s_full[t]);
                 release(&B.k_empty[ks], j);
             }
-            umma_commit(&B.q_free[t]);  // Q_t is not read once these have completed
-            ++qa;
-        } else if (pv && nt > 0) {
+            if (nt > 0) {
+                umma_commit(&B.q_free[t]);  // Q_t is not read once these have completed
+                ++qa;
+            }
+        } else {
             // O += P_j V_j: P from its buffer (hi, then lo for bf16 32 columns
             // on), V MN-major (16 keys = 2048 bytes per K step, slices of
             // head_dim a tile slice apart); the item's first product starts
             // O afresh once the softmax has read out the previous item's O
             for (int j = 0; ok && j < nt; ++j, ++pc) {
                 const int q = rc + j, vs = q % RV, pb = pc % kNP;
-                ok = mbar_wait(&B.v_full[vs], (uint32_t)(q / RV) & 1u, abort_flag) &&
+                ok = wait_tile(B.v_full, B.v_tag, q, RV, abort_flag) &&
                      mbar_wait(&B.p_full[2 * t + pb], (uint32_t)(pc / kNP) & 1u, abort_flag) &&
                      (j > 0 || oa == 0 ||
                       mbar_wait(&B.o_free[t], (uint32_t)(oa - 1) & 1u, abort_flag));
@@ -724,7 +757,7 @@ __device__ __forceinline__ void run_mma_p(const PrefillParams &P, int t, int pv,
                 umma_commit(&B.pv_done[2 * t + pb]);
                 release(&B.v_empty[vs], j);
             }
-            ++oa;
+            if (nt > 0) ++oa;
         }
         if (!ok) break;
         rc += ntiles;
@@ -1034,6 +1067,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     PItem *items = reinterpret_cast<PItem *>(smem + L::item_off);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off);
     Bars B;
+    B.k_tag = reinterpret_cast<volatile int *>(smem + L::tag_off);
+    B.v_tag = B.k_tag + RK;
     B.q_full = bars;
     B.q_free = B.q_full + 2;
     B.k_full = B.q_free + 2;
@@ -1068,6 +1103,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         }
         for (int b = 0; b < RK; ++b) mbar_init(&B.k_empty[b], 2);  // one arrival per tile
         for (int b = 0; b < RV; ++b) mbar_init(&B.v_empty[b], 2);
+        for (int b = 0; b < RK + RV; ++b) B.k_tag[b] = -1;
         *abort_flag = 0;
         fence_mbar_init();
     }
