@@ -72,35 +72,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     return false;
 }
 
-// The same wait, but each try suspends the thread for up to `hint_ns` (it
-// wakes when the phase completes), so a waiting warp leaves the issue slots
-// to the warps doing work.  The time limit still applies; polls are counted
-// in tries.
-__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity,
-                                                   uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity,
-                                                volatile int *abort, uint32_t hint_ns = 2000u) {
-    if (mbar_try_wait_hint(bar, parity, hint_ns)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t polls = 1; polls < kWaitLimitPolls; ++polls) {
-        if (mbar_try_wait_hint(bar, parity, hint_ns)) return true;
-        if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-    }
-    return false;
-}
-
 // L2 policy for data read once (the K/V stream).
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t p;
