@@ -270,7 +270,8 @@ pa_status_t pa_prefill_attention(void *out, pa_dtype_t out_dtype, const void *qu
                                  const int32_t *query_start_loc, const int32_t *context_lens,
                                  int max_query_len, int max_context_len, int num_seqs,
                                  int num_tokens, int num_heads, int num_kv_heads, int head_dim,
-                                 int num_blocks, int block_size, float scale, pa_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                                 int num_blocks, int block_size, float scale, pa_dtype_t dtype,
+                                 void *workspace, size_t workspace_bytes,
                                  unsigned int *dev_error_word, pa_stream_t stream);
 
 /*
