@@ -868,6 +868,9 @@ __device__ __forceinline__ void run_softmax_p(const PrefillParams &P, int t, con
     const uint32_t tm_s = tmem + (uint32_t)(t * 128) + lane_addr;
     const uint32_t tm_o = tmem + 256u + (uint32_t)(t * D) + lane_addr;
     const float sc = P.scale_log2;
+    const bool fold = sc > 0.f;             // the same in every thread
+    const float psc = fold ? sc : 1.f;      // scale applied in the exponent
+    const float msc = fold ? 1.f : sc;      // scale applied before the maximum
     const UnitGeo g = unit_geo(P.block_shift);
     const int tpb_mask = (1 << g.lg_tpb) - 1;
     const unsigned unit_mask = (1u << g.upt) - 1u;
@@ -923,20 +926,29 @@ __device__ __forceinline__ void run_softmax_p(const PrefillParams &P, int t, con
 #pragma unroll
             for (int e = 0; e < kKN; ++e) s[e] = __uint_as_float(su[e]);
             const int kb = j * kKN;
-            // scale to base 2; keys past the row's position or in a skipped
-            // block.  One warp per scheduler runs this code, so the reductions
-            // keep eight independent chains.
+            // Keys past the row's position or in a skipped block read -inf.
+            // With a positive scale the maximum is taken over the raw scores
+            // and the scale goes into the exponent's FMA below (one multiply
+            // a key less); otherwise the scores are scaled first.  In both
+            // forms s ends up in units with p = 2^(s * psc - m).  One warp per
+            // scheduler runs this code, so the reductions keep eight
+            // independent chains.
             constexpr int kAcc = 8;
             float mxa[kAcc];
 #pragma unroll
-            for (int q = 0; q < kAcc; ++q) mxa[q] = m_ref;
+            for (int q = 0; q < kAcc; ++q) mxa[q] = -INFINITY;
             // the masked form is taken by the whole warp or not at all (a
             // warp on the diagonal would otherwise run both)
             if (__all_sync(0xffffffffu, !bits && kb + kKN - 1 <= qpos)) {  // all keys visible
+                if (fold) {
 #pragma unroll
-                for (int e = 0; e < kKN; ++e) {
-                    s[e] *= sc;
-                    mxa[e % kAcc] = fmaxf(mxa[e % kAcc], s[e]);
+                    for (int e = 0; e < kKN; ++e) mxa[e % kAcc] = fmaxf(mxa[e % kAcc], s[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < kKN; ++e) {
+                        s[e] *= sc;
+                        mxa[e % kAcc] = fmaxf(mxa[e % kAcc], s[e]);
+                    }
                 }
             } else {
                 // keys kb .. kb + nvis - 1 are at or before the row's position
@@ -944,21 +956,21 @@ __device__ __forceinline__ void run_softmax_p(const PrefillParams &P, int t, con
                 if (!bits) {  // (bits is the same in every lane)
 #pragma unroll
                     for (int e = 0; e < kKN; ++e) {
-                        s[e] = e >= nvis ? -INFINITY : s[e] * sc;
+                        s[e] = e >= nvis ? -INFINITY : s[e] * msc;
                         mxa[e % kAcc] = fmaxf(mxa[e % kAcc], s[e]);
                     }
                 } else {  // and the keys of skipped blocks
 #pragma unroll
                     for (int e = 0; e < kKN; ++e) {
                         const bool masked = e >= nvis || ((bits >> (e >> g.lg_tbr)) & 1u);
-                        s[e] = masked ? -INFINITY : s[e] * sc;
+                        s[e] = masked ? -INFINITY : s[e] * msc;
                         mxa[e % kAcc] = fmaxf(mxa[e % kAcc], s[e]);
                     }
                 }
             }
 #pragma unroll
             for (int q = 1; q < kAcc; ++q) mxa[0] = fmaxf(mxa[0], mxa[q]);
-            const float mx = mxa[0];
+            const float mx = fmaxf(m_ref, mxa[0] * psc);  // base-2 units
             // lazy rescale: only when the maximum grew by more than 2^8; O
             // must then be stable (the item's previous P V finished)
             const bool grow = mx > m_ref + kRescaleLog2;
@@ -1007,7 +1019,7 @@ __device__ __forceinline__ void run_softmax_p(const PrefillParams &P, int t, con
             for (int q = 0; q < kAcc; ++q) lsa[q] = 0.f;
 #pragma unroll
             for (int c = 0; c < kKN / 2; ++c) {
-                const float p0 = ex2(s[2 * c] - ms), p1 = ex2(s[2 * c + 1] - ms);
+                const float p0 = ex2(fmaf(s[2 * c], psc, -ms)), p1 = ex2(fmaf(s[2 * c + 1], psc, -ms));
                 lsa[(2 * c) % kAcc] += p0;
                 lsa[(2 * c + 1) % kAcc] += p1;
                 ph[c] = pack2<T>(p0, p1);

@@ -210,3 +210,15 @@ def test_prefill_workspace_checks():
     assert ei.value.status == 4
     big = pa.prefill_workspace_size(2, 4, 2, 100_000)
     assert big > need
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.05])
+def test_prefill_non_positive_scale(scale):
+    """A scale of 0 (every visible key weighs the same) and a negative scale
+    take the form that scales the scores before the maximum."""
+    cases = [(30, 70), (0, 130), (200, 1)]
+    d = _problem(cases, 8, 2, 128, "bf16", 16, seed=11)
+    out = _run(d, scale)
+    torch.cuda.synchronize()
+    want = _oracle(d, scale, "bf16")
+    assert max_abs(out.cpu().numpy(), want) <= ATOL
