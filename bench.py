@@ -469,18 +469,27 @@ def prefill_flops(cached, new, num_heads, head_dim):
     return 4 * head_dim * num_heads * keys
 
 
+PREFILL_BATCHES = {
+    # 8 chunks of 512 tokens on cached prefixes up to 1536 (a 4096-token budget)
+    "chunks": ([0, 0, 512, 512, 1024, 1024, 1536, 1536], [512] * 8,
+               "8 sequences x 512 new tokens on cached prefixes 0..1536 (4096-token budget)"),
+    # one 512-token chunk on an 8192-token prefix among 40 fresh 256-token prompts
+    "skewed": ([8192] + [0] * 40, [512] + [256] * 40,
+               "one 512-token chunk on an 8192-token prefix with 40 fresh 256-token prompts"),
+}
+
+
 def prefill_bench(args, dev):
-    """One chunked-prefill step: 8 sequences, 512 new tokens each, on cached
-    prefixes of 0, 0, 512, 512, 1024, 1024, 1536, 1536 tokens (a 4096-token
-    budget), heads as the named workload; blocks of 16 tokens scattered over
-    the pool.  Times the cache write of the chunk plus the prefill attention,
-    and the attention alone, over back-to-back steps."""
+    """One chunked-prefill step (PREFILL_BATCHES[args.prefill_batch]), heads
+    as the named workload; blocks scattered over the pool.  Times the cache
+    write of the chunk plus the prefill attention, and the attention alone,
+    over back-to-back steps."""
     import torch
     import paged_kv_cache_pa_gb300 as pa
     H, Hkv, D, dtype = PREFILL_SHAPES[args.config]
     dt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
-    cached = [0, 0, 512, 512, 1024, 1024, 1536, 1536]
-    new = [512] * 8
+    cached, new, batch_desc = PREFILL_BATCHES[args.prefill_batch]
+    S = len(new)
     B = args.prefill_block_size
     lens = np.array([c + n for c, n in zip(cached, new)], np.int32)
     qsl = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
@@ -488,7 +497,7 @@ def prefill_bench(args, dev):
     nbs = [-(-int(L) // B) for L in lens]
     perm = rng.permutation(sum(nbs))
     maxb = max(nbs)
-    tables = np.full((8, maxb), -1, np.int32)
+    tables = np.full((S, maxb), -1, np.int32)
     pos = 0
     for s_, n_ in enumerate(nbs):
         tables[s_, :n_] = perm[pos:pos + n_]
@@ -509,8 +518,8 @@ def prefill_bench(args, dev):
     s_d = torch.as_tensor(slots, device=dev)
     scale = 1.0 / np.sqrt(D)
 
-    ws = torch.empty(max(256, pa.prefill_workspace_size(8, H, Hkv, max(new))), dtype=torch.uint8,
-                     device=dev)
+    ws = torch.empty(max(256, pa.prefill_workspace_size(S, H, Hkv, D, max(new))),
+                     dtype=torch.uint8, device=dev)
 
     def attn():
         pa.prefill_attention(q, kc, vc, t_d, q_d, l_d, max(new), int(lens.max()), scale, out=out,
@@ -544,8 +553,7 @@ def prefill_bench(args, dev):
         peak = 1900.0
     tf = flops / (ms_attn * 1e-3) / 1e12
     print(json.dumps({"prefill": args.config,
-                      "workload": f"chunked prefill: 8 sequences x 512 new tokens on cached "
-                                  f"prefixes 0..1536 (4096-token budget), {H} query / {Hkv} KV "
+                      "workload": f"chunked prefill: {batch_desc}, {H} query / {Hkv} KV "
                                   f"heads, D={D}, {dtype}, block {B}, scattered blocks",
                       "steps": n, "algorithmic_tflop": round(flops / 1e12, 4),
                       "ms_attention": round(ms_attn, 4), "ms_step": round(ms_step, 4),
@@ -576,6 +584,10 @@ def main():
                          "workload's heads; prints its own JSON line")
     ap.add_argument("--prefill-block-size", type=int, default=16,
                     help="tokens per block for --prefill (8 .. 256)")
+    ap.add_argument("--prefill-batch", choices=sorted(PREFILL_BATCHES), default="chunks",
+                    help="batch for --prefill: 'chunks' (8 x 512 on prefixes up to 1536) or "
+                         "'skewed' (one 512-token chunk on an 8192-token prefix among 40 "
+                         "fresh 256-token prompts)")
     ap.add_argument("--swap-sweep", action="store_true",
                     help="time swap-out and swap-in of one full-length request over all "
                          "layers at block sizes 8..256; prints its own JSON line")

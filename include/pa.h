@@ -213,10 +213,12 @@ pa_status_t pa_decode_attention_ex(void *out, pa_dtype_t out_dtype, const void *
 
 /*
  * pa_prefill_workspace_size -- bytes of device workspace pa_prefill_attention
- * needs for these sizes (the work list: 4 bytes per work item plus 8); 0 if
- * the sizes are invalid.  Host only, no CUDA calls.
+ * needs for these sizes: the work list (8-16 bytes per work item) and room
+ * for the partial results of up to 160 split items (4 x 128 x (head_dim + 2)
+ * floats each); 0 if the sizes are invalid (head_dim not 64 or 128, heads not
+ * a multiple of KV heads).  Host only, no CUDA calls.
  */
-size_t pa_prefill_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+size_t pa_prefill_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                  int max_query_len);
 
 /*
@@ -253,16 +255,20 @@ size_t pa_prefill_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
  * head_dim 64 or 128 (PA_ERR_UNSUPPORTED otherwise); block_size a power of
  * two in [PA_MIN_BLOCK_SIZE, PA_MAX_BLOCK_SIZE]; num_heads % num_kv_heads == 0
  * workspace     device, >= pa_prefill_workspace_size(...) bytes, 256-byte
- *               aligned (PA_ERR_WORKSPACE otherwise); holds the work list.
- *               Calls in flight at once must not share one workspace.
+ *               aligned (PA_ERR_WORKSPACE otherwise); holds the work list and
+ *               the partial results of split items.  Calls in flight at once
+ *               must not share one workspace.
  * dev_error_word  device, may be NULL: PA_ERRBIT_CONTEXT_LEN for a sequence
  *               whose lengths break the rules above (its rows are zeroed),
  *               PA_ERRBIT_BLOCK_OOB (the block's keys are skipped),
  *               PA_ERRBIT_TIMEOUT.
  * Enqueues two kernels: a plan (one CTA: the work items -- two 128-token
- * query tiles that read the same keys -- that have work, heaviest first) and
- * the attention kernel (persistent, one CTA per SM, taking items from the
- * list in order).
+ * query tiles that read the same keys -- that have work, heaviest first; an
+ * item with more than twice an SM's even share of the K/V tiles is split in
+ * two parts over its keys, merged exactly by the part that finishes second)
+ * and the
+ * attention kernel (persistent, one CTA per SM, taking entries from the list
+ * in order).
  */
 pa_status_t pa_prefill_attention(void *out, pa_dtype_t out_dtype, const void *query,
                                  const void *k_cache, const void *v_cache,

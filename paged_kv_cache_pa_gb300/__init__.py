@@ -62,7 +62,7 @@ _SIGNATURES = {
     "pa_copy_blocks_ex": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pa_prefill_attention": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I,
                                   _I, _I, _I, ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P]),
-    "pa_prefill_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "pa_prefill_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
     "pa_swap_blocks": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pa_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -306,10 +306,10 @@ def swap_blocks(dst_k_caches: Sequence, dst_v_caches: Sequence, src_k_caches: Se
     _check(st, "pa_swap_blocks")
 
 
-def prefill_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int,
+def prefill_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
                            max_query_len: int) -> int:
     return int(load_library().pa_prefill_workspace_size(num_seqs, num_heads, num_kv_heads,
-                                                        max_query_len))
+                                                        head_dim, max_query_len))
 
 
 def prefill_attention(query, k_cache, v_cache, block_tables, query_start_loc, context_lens,
@@ -337,7 +337,7 @@ def prefill_attention(query, k_cache, v_cache, block_tables, query_start_loc, co
     if out is None:
         out = torch.empty(T, H, D, dtype=out_dtype or torch.float32, device=query.device)
     if workspace is None:
-        nbytes = prefill_workspace_size(S, H, hkv, int(max_query_len))
+        nbytes = prefill_workspace_size(S, H, hkv, D, int(max_query_len))
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=query.device)
     st = load_library().pa_prefill_attention(
         _dev(out, "out"), _dtype_code(out.dtype), _dev(query, "query"), _dev(k_cache, "k_cache"),

@@ -97,7 +97,11 @@ constexpr float kRescaleLog2 = 8.f;  // lazy rescale threshold (base-2 units)
 constexpr int kMaxDevicesP = 64;
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanBuckets = 2048;   // item costs (K/V tiles), the last bucket open-ended
-constexpr int kWorkHeader = 2;       // work[0] claim counter, work[1] items listed
+// Workspace: a header of 4 words (claim counter, entries listed, items split),
+// the entries (uint2: item id, part code) heaviest first, then for each split
+// item a pair of finish counters and its two parts' partial results.
+constexpr int kWorkHeader = 4;
+constexpr int kMaxSplits = 160;      // items that may be split in two, at most
 
 struct PrefillParams {
     CUtensorMap tmap_q, tmap_k, tmap_v;
@@ -114,7 +118,13 @@ struct PrefillParams {
     int pair_heads;  // 1: an item's two tiles are heads 2y, 2y+1; 0: token tiles 2x, 2x+1
     int items_x, items_y;    // items of a sequence: x (token tiles or pairs) by y (heads or pairs)
     unsigned int num_items;  // num_seqs * items_x * items_y
-    unsigned int *work;      // claim counter, items listed, item ids heaviest first
+    unsigned int grid;       // persistent CTAs
+    int max_splits;          // split items the workspace has room for
+    unsigned int *work;      // header: claim counter, entries listed, items split
+    uint2 *entries;          // item id, part code (0: whole; 1 | part << 1 | slot << 2)
+    unsigned int *split_cnt; // [max_splits][2 tiles]: parts finished
+    float *part_m, *part_l;  // [max_splits][2 parts][2 tiles][128]: base-2 max and sum
+    float *part_o;           // [max_splits][2 parts][2 tiles][128][head_dim]: unnormalised O
     float scale_log2;
     unsigned int *err;
 };
@@ -134,12 +144,15 @@ struct PTile {
     bool act;
 };
 
-// One work item, the same in every thread that reads it.
+// One work item (or one part of a split item), the same in every thread that
+// reads it.
 struct PItem {
     int s, hk;
     int n, L, c;  // new tokens, context length after the chunk, cached before it
     int tok0;     // query row of the sequence's first new token
     int kv_end, ntiles;  // over both tiles
+    int kt0, kt1;        // K/V tiles kt0 .. kt1-1 of 0 .. ntiles-1 (a part of a split item)
+    int slot, part;      // split item: its partial-result slot and this part; slot -1: whole
     bool ok, run, stop;  // stop: no items left
     PTile t[2];
 };
@@ -164,7 +177,8 @@ struct PLayout {
     static constexpr int kBars = 2 + 2 + 2 * RK + 2 * RV + 1 + 2 + 2 + 2 + 2 + 4 + 4 + 2 + 4;
     static constexpr size_t tmem_off = bar_off + (size_t)kBars * 8;
     static constexpr size_t flag_off = tmem_off + 8;
-    static constexpr size_t used = flag_off + 8;
+    static constexpr size_t split_off = flag_off + 8;                  // unsigned [2 tiles]
+    static constexpr size_t used = split_off + 8;
     static constexpr size_t bytes = used + 1024;                       // base alignment slack
     static_assert(bytes <= 232448, "dynamic shared memory of one CTA");
 };
@@ -269,7 +283,22 @@ __device__ __forceinline__ PItem make_item(const PrefillParams &P, unsigned id) 
     it.hk = it.t[0].h / P.G;  // both tiles read the same KV head
     it.ntiles = (it.kv_end + kKN - 1) / kKN;
     it.run = it.t[0].act || it.t[1].act;
+    it.kt0 = 0;
+    it.kt1 = it.ntiles;
+    it.slot = -1;
+    it.part = 0;
     return it;
+}
+
+// A part of a split item: the first part takes K/V tiles 0 .. ceil(n/2)-1,
+// the second the rest.
+__device__ __forceinline__ void apply_part(PItem &it, unsigned code) {
+    if (!(code & 1u)) return;
+    it.part = (int)((code >> 1) & 1u);
+    it.slot = (int)(code >> 2);
+    const int half = (it.ntiles + 1) / 2;
+    it.kt0 = it.part ? half : 0;
+    it.kt1 = it.part ? it.ntiles : half;
 }
 
 // -1: nothing to do (both tiles past the sequence's new tokens); else the K/V
@@ -349,28 +378,20 @@ struct SeqRows {
 
 // What the producers need of an item.
 struct KVItem {
-    int s, hk, kv_end, ntiles;
+    int s, hk, kv_end, ntiles, kt0, kt1;
 };
 
 // ---------------------------------------------------------------------------
 // plan: the items with work, heaviest first (a counting sort on the number of
-// K/V tiles), into work[2 ..]; work[0] = 0 (claim counter), work[1] = count
+// K/V tiles), as entries in the workspace.  An item whose K/V tiles exceed
+// twice an SM's even share of the whole (2 total / grid) is split in two parts
+// over its K/V tiles, the costliest first and at most max_splits of them; the
+// two parts are separate entries and share a partial-result slot.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kPlanThreads, 1)
-    prefill_plan_kernel(const __grid_constant__ PrefillParams P) {
-    __shared__ unsigned int cnt[kPlanBuckets];
-    __shared__ unsigned int warp_sum[kPlanThreads / 32];
-    pdl_trigger();
+// exclusive start of each bucket in descending order of cost, in place; the
+// total is returned (every thread)
+__device__ __forceinline__ unsigned plan_scan_desc(unsigned *cnt, unsigned *warp_sum) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    for (int b = tid; b < kPlanBuckets; b += kPlanThreads) cnt[b] = 0;
-    __syncthreads();
-    for (unsigned id = tid; id < P.num_items; id += kPlanThreads) {
-        const int c = item_cost(P, id);
-        if (c >= 0) atomicAdd(&cnt[min(c, kPlanBuckets - 1)], 1u);
-    }
-    __syncthreads();
-    // start of each bucket in the list: the count of every costlier bucket
-    // (thread i owns buckets B-1-2i and B-2-2i, the costliest first)
     constexpr int kPer = kPlanBuckets / kPlanThreads;
     static_assert(kPer * kPlanThreads == kPlanBuckets, "buckets per thread");
     unsigned v[kPer], local = 0;
@@ -406,21 +427,96 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
         start += v[q];
     }
     __syncthreads();
-    // Everything above only read the inputs.  The work list is written once
-    // the kernel before this one has completed: the attention kernel depends
-    // on it as well (the cache write of the chunk), and an earlier attention
-    // call on this stream may still be taking items from the same workspace.
-    pdl_wait();
+    return total;
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1)
+    prefill_plan_kernel(const __grid_constant__ PrefillParams P) {
+    __shared__ unsigned int cnt[kPlanBuckets];
+    __shared__ unsigned int warp_sum[kPlanThreads / 32];
+    __shared__ unsigned long long s_total;
+    __shared__ int s_split_cost;  // items of at least this cost are split
+    __shared__ unsigned int s_slots;
+    __shared__ int s_max_cost;
+    pdl_trigger();
+    const int tid = threadIdx.x;
+    for (int b = tid; b < kPlanBuckets; b += kPlanThreads) cnt[b] = 0;
+    if (tid == 0) {
+        s_total = 0;
+        s_slots = 0;
+        s_max_cost = 0;
+    }
+    __syncthreads();
+    // items per cost, and the total
+    unsigned long long mine = 0;
+    int my_max = 0;
     for (unsigned id = tid; id < P.num_items; id += kPlanThreads) {
         const int c = item_cost(P, id);
         if (c >= 0) {
-            const unsigned pos = atomicAdd(&cnt[min(c, kPlanBuckets - 1)], 1u);
-            P.work[kWorkHeader + pos] = id;
+            atomicAdd(&cnt[min(c, kPlanBuckets - 1)], 1u);
+            mine += (unsigned long long)c;
+            my_max = max(my_max, min(c, kPlanBuckets - 1));
         }
     }
+    atomicAdd(&s_total, mine);
+    atomicMax(&s_max_cost, my_max);
+    __syncthreads();
+    // the split threshold: above an even share, and no more items than slots
+    if (tid == 0) {
+        // twice an SM's even share: a part's own costs (partial results,
+        // the merge) outweigh the balance gained below that
+        const unsigned long long share = (2 * s_total + P.grid - 1) / max(1u, P.grid);
+        int c = s_max_cost + 1;
+        unsigned above = 0;
+        while (c > 2 && (unsigned long long)(c - 1) > share &&
+               above + cnt[c - 1] <= (unsigned)P.max_splits) {
+            above += cnt[c - 1];
+            --c;
+        }
+        s_split_cost = c;  // costs >= c are split (max cost + 1: none)
+    }
+    __syncthreads();
+    const int split_cost = s_split_cost;
+    // entries per cost: a split item gives two parts of ceil(c/2) and floor(c/2)
+    for (int b = tid; b < kPlanBuckets; b += kPlanThreads) cnt[b] = 0;
+    __syncthreads();
+    for (unsigned id = tid; id < P.num_items; id += kPlanThreads) {
+        const int c = item_cost(P, id);
+        if (c < 0) continue;
+        if (c >= split_cost) {
+            atomicAdd(&cnt[min((c + 1) / 2, kPlanBuckets - 1)], 1u);
+            atomicAdd(&cnt[min(c / 2, kPlanBuckets - 1)], 1u);
+        } else {
+            atomicAdd(&cnt[min(c, kPlanBuckets - 1)], 1u);
+        }
+    }
+    __syncthreads();
+    const unsigned total = plan_scan_desc(cnt, warp_sum);
+    // Everything above only read the inputs.  The work list is written once
+    // the kernel before this one has completed: the attention kernel depends
+    // on it as well (the cache write of the chunk), and an earlier attention
+    // call on this stream may still be taking entries from this workspace.
+    pdl_wait();
+    for (unsigned id = tid; id < P.num_items; id += kPlanThreads) {
+        const int c = item_cost(P, id);
+        if (c < 0) continue;
+        if (c >= split_cost) {
+            const unsigned slot = atomicAdd(&s_slots, 1u);
+            const unsigned p0 = atomicAdd(&cnt[min((c + 1) / 2, kPlanBuckets - 1)], 1u);
+            const unsigned p1 = atomicAdd(&cnt[min(c / 2, kPlanBuckets - 1)], 1u);
+            P.entries[p0] = make_uint2(id, 1u | (0u << 1) | (slot << 2));
+            P.entries[p1] = make_uint2(id, 1u | (1u << 1) | (slot << 2));
+        } else {
+            const unsigned pos = atomicAdd(&cnt[min(c, kPlanBuckets - 1)], 1u);
+            P.entries[pos] = make_uint2(id, 0u);
+        }
+    }
+    __syncthreads();
+    for (unsigned i = tid; i < 2 * s_slots; i += kPlanThreads) P.split_cnt[i] = 0u;
     if (tid == 0) {
         P.work[0] = 0u;
         P.work[1] = total;
+        P.work[2] = s_slots;
     }
 }
 
@@ -446,10 +542,11 @@ __device__ __forceinline__ bool produce_item(const PrefillParams &P, const KVIte
     const uint32_t unit_bytes = (uint32_t)KB * 128u << g.lg_tbr;
     // rows from this key on are cleared in the last V tile
     const int tail_row = it.kv_end & (kKN - 1);
-    int cur = unit_entry(P, row, g, 0, it.kv_end, lane);
-    int nxt = unit_entry(P, row, g, 1, it.kv_end, lane);
-    for (int j = 0; j < it.ntiles; ++j, ++rc) {
-        if (j > 0 && (j & tpb_mask) == 0) {
+    const int b0 = it.kt0 >> g.lg_tpb;  // table batch of the first tile
+    int cur = unit_entry(P, row, g, b0, it.kv_end, lane);
+    int nxt = unit_entry(P, row, g, b0 + 1, it.kv_end, lane);
+    for (int j = it.kt0; j < it.kt1; ++j, ++rc) {
+        if (j > it.kt0 && (j & tpb_mask) == 0) {
             cur = nxt;
             nxt = unit_entry(P, row, g, (j >> g.lg_tpb) + 1, it.kv_end, lane);
         }
@@ -553,15 +650,21 @@ __device__ __forceinline__ void run_k_producer(const PrefillParams &P, unsigned 
             aborted = true;
             break;
         }
-        unsigned id = 0xffffffffu;
+        unsigned id = 0xffffffffu, code = 0u;
         if (lane == 0) {
             const unsigned v = atomicAdd(&P.work[0], 1u);
-            if (v < n_items) id = P.work[kWorkHeader + v];
+            if (v < n_items) {
+                const uint2 e = P.entries[v];
+                id = e.x;
+                code = e.y;
+            }
         }
         id = __shfl_sync(0xffffffffu, id, 0);
+        code = __shfl_sync(0xffffffffu, code, 0);
         PItem it;
         if (id != 0xffffffffu) {
             it = make_item(P, id);
+            apply_part(it, code);
         } else {
             memset(&it, 0, sizeof(it));
             it.stop = true;
@@ -591,7 +694,7 @@ __device__ __forceinline__ void run_k_producer(const PrefillParams &P, unsigned 
                 }
             }
         }
-        const KVItem kv{it.s, it.hk, it.kv_end, it.ntiles};
+        const KVItem kv{it.s, it.hk, it.kv_end, it.ntiles, it.kt0, it.kt1};
         if (!__shfl_sync(0xffffffffu, (int)ok, 0) ||
             !produce_item<D, false>(P, kv, sk, B, abort_flag, lane, rc, land, land_pending)) {
             aborted = true;
@@ -628,7 +731,7 @@ __device__ __forceinline__ void run_v_producer(const PrefillParams &P, unsigned 
             break;
         }
         const bool stop = ip->stop, iok = ip->ok;
-        const KVItem kv{ip->s, ip->hk, ip->kv_end, ip->ntiles};
+        const KVItem kv{ip->s, ip->hk, ip->kv_end, ip->ntiles, ip->kt0, ip->kt1};
         give_item_back(B, n, lane, 0xffffffffu);
         ++n;
         if (stop) break;
@@ -686,7 +789,8 @@ __device__ __forceinline__ void run_mma_p(const PrefillParams &P, int t, int pv,
         const bool stop = ip->stop, iok = ip->ok;
         const int nt = t ? ip->t[1].nt : ip->t[0].nt;
         const int nt_other = t ? ip->t[0].nt : ip->t[1].nt;
-        const int ntiles = ip->ntiles;
+        const int kt0 = ip->kt0, kt1 = ip->kt1;
+        const int end = min(kt1, nt);  // this tile's K/V tiles in the entry: kt0 .. end-1
         give_item_back(B, n, 0, 1u);
         ++n;
         if (stop) break;
@@ -700,15 +804,15 @@ __device__ __forceinline__ void run_mma_p(const PrefillParams &P, int t, int pv,
             if (j >= nt_other) umma_commit(bar);
         };
         if (!pv) {
-            if (nt > 0) {
+            if (end > kt0) {
                 ok = mbar_wait(&B.q_full[t], (uint32_t)qa & 1u, abort_flag);
                 tc_fence_after();
             }
             // S_j into the tile's S buffer once the softmax has loaded the
             // previous S.  A K step of 16 is 32 bytes inside a 64-element
             // slice; slices are whole tiles apart.
-            for (int j = 0; ok && j < nt; ++j, ++sc) {
-                const int q = rc + j, ks = q % RK;
+            for (int j = kt0; ok && j < end; ++j, ++sc) {
+                const int q = rc + (j - kt0), ks = q % RK;
                 ok = wait_tile(B.k_full, B.k_tag, q, RK, abort_flag) &&
                      (sc == 0 || mbar_wait(&B.s_free[t], (uint32_t)(sc - 1) & 1u, abort_flag));
                 if (!ok) break;
@@ -726,7 +830,7 @@ __device__ __forceinline__ void run_mma_p(const PrefillParams &P, int t, int pv,
                 umma_commit(&B.s_full[t]);
                 release(&B.k_empty[ks], j);
             }
-            if (nt > 0) {
+            if (end > kt0) {
                 umma_commit(&B.q_free[t]);  // Q_t is not read once these have completed
                 ++qa;
             }
@@ -735,11 +839,11 @@ __device__ __forceinline__ void run_mma_p(const PrefillParams &P, int t, int pv,
             // on), V MN-major (16 keys = 2048 bytes per K step, slices of
             // head_dim a tile slice apart); the item's first product starts
             // O afresh once the softmax has read out the previous item's O
-            for (int j = 0; ok && j < nt; ++j, ++pc) {
-                const int q = rc + j, vs = q % RV, pb = pc % kNP;
+            for (int j = kt0; ok && j < end; ++j, ++pc) {
+                const int q = rc + (j - kt0), vs = q % RV, pb = pc % kNP;
                 ok = wait_tile(B.v_full, B.v_tag, q, RV, abort_flag) &&
                      mbar_wait(&B.p_full[2 * t + pb], (uint32_t)(pc / kNP) & 1u, abort_flag) &&
-                     (j > 0 || oa == 0 ||
+                     (j > kt0 || oa == 0 ||
                       mbar_wait(&B.o_free[t], (uint32_t)(oa - 1) & 1u, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
@@ -750,17 +854,17 @@ __device__ __forceinline__ void run_mma_p(const PrefillParams &P, int t, int pv,
                     const uint64_t db =
                         umma_desc_sw128(vt + (uint32_t)(kk * 16 * 128), kSliceBytes, 1024);
                     umma_f16_tmem_a(to, tp + (uint32_t)(kk * 8), db, idesc_o,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
+                                    (j > kt0 || kk > 0) ? 1u : 0u);
                     if constexpr (kSplit)
                         umma_f16_tmem_a(to, tp + 32u + (uint32_t)(kk * 8), db, idesc_o, 1u);
                 }
                 umma_commit(&B.pv_done[2 * t + pb]);
                 release(&B.v_empty[vs], j);
             }
-            if (nt > 0) ++oa;
+            if (end > kt0) ++oa;
         }
         if (!ok) break;
-        rc += ntiles;
+        rc += kt1 - kt0;
     }
     if (!ok) {
         *abort_flag = 1;
@@ -854,14 +958,155 @@ __device__ __forceinline__ void store_rows(const PrefillParams &P, const SeqRows
 }
 
 // ---------------------------------------------------------------------------
+// split items.  Each part leaves its tile's unnormalised O (relative to its
+// base-2 maximum m) with m and the sum l in the workspace; the part that
+// finishes second combines them exactly:
+//     M = max(m_0, m_1),  c_p = 2^(m_p - M),  o = (c_0 O_0 + c_1 O_1) / (c_0 l_0 + c_1 l_1)
+// (a part that saw no key of a row has m = -inf and weighs nothing)
+// [Efficient Memory Management ..., "PagedAttention Algorithm": blocks may be
+// processed in any order and combined; vLLM Internals ..., partitions of a
+// long sequence merged afterwards].
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ size_t part_row(int slot, int part, int t) {
+    return (((size_t)slot * 2 + part) * 2 + t) * kQM;
+}
+
+// The tile's O rows (raw, fp32), m and l of part `part` to the workspace,
+// staged through shared memory so that stores write whole 128-byte rows.
+template <int D>
+__device__ __forceinline__ void store_partial(const PrefillParams &P, int slot, int part, int t,
+                                              uint32_t tm_o, float m, float l,
+                                              unsigned char *stage, uint64_t *o_free, int wq,
+                                              int lane) {
+    constexpr int CR = kStageWarpBytes / (32 * 4);  // 32 fp32 columns a round
+    const int r0 = 32 * wq;
+    const size_t prow = part_row(slot, part, t);
+    P.part_m[prow + r0 + lane] = m;
+    P.part_l[prow + r0 + lane] = l;
+    float *base = P.part_o + (prow + r0) * D;
+#pragma unroll
+    for (int q = 0; q < D / CR; ++q) {
+        if (lane == 0) bulk_wait_read();  // the stage's last tiled store has read it
+        __syncwarp();
+        uint32_t u[CR];
+#pragma unroll
+        for (int c = 0; c < CR; c += 16)
+            tmem_ld16(tm_o + (uint32_t)(q * CR + c), *reinterpret_cast<uint32_t(*)[16]>(&u[c]));
+        tmem_wait_ld();
+        if (q == D / CR - 1) {  // all of O has been read: the next item may start it afresh
+            tc_fence_before();
+            mbar_arrive(o_free);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int pos = k ^ (lane & 7);
+            *reinterpret_cast<uint4 *>(stage + lane * 128 + pos * 16) =
+                make_uint4(u[4 * k], u[4 * k + 1], u[4 * k + 2], u[4 * k + 3]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int it2 = 0; it2 < 8; ++it2) {
+            const int rr = it2 * 4 + lane / 8, k = lane % 8;
+            const uint4 w = *reinterpret_cast<const uint4 *>(stage + rr * 128 + ((k ^ (rr & 7)) * 16));
+            *reinterpret_cast<uint4 *>(base + (size_t)rr * D + q * CR + k * 4) = w;
+        }
+        __syncwarp();
+    }
+}
+
+// After a part's results are in the workspace: count the part finished for
+// tile t of split slot `slot`; true in the 128 threads of the part that
+// finished second.
+__device__ __forceinline__ bool split_last(const PrefillParams &P, int slot, int t,
+                                           volatile unsigned *split_old, int lane) {
+    __threadfence();  // this part's results, before the count
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + t), "n"(kTileThreads) : "memory");
+    if (threadIdx.x % kTileThreads == 0) split_old[t] = atomicAdd(&P.split_cnt[slot * 2 + t], 1u);
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + t), "n"(kTileThreads) : "memory");
+    const bool last = split_old[t] == 1u;
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + t), "n"(kTileThreads) : "memory");
+    if (last) __threadfence();  // the other part's results, after the count
+    return last;
+}
+
+template <typename OutT>
+__device__ __forceinline__ void store4(void *out, size_t idx, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(void *out, size_t idx, float4 v) {
+    *reinterpret_cast<float4 *>(static_cast<float *>(out) + idx) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__half>(void *out, size_t idx, float4 v) {
+    *reinterpret_cast<uint2 *>(static_cast<__half *>(out) + idx) =
+        make_uint2(pack2<__half>(v.x, v.y), pack2<__half>(v.z, v.w));
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(void *out, size_t idx, float4 v) {
+    *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(out) + idx) =
+        make_uint2(pack2<__nv_bfloat16>(v.x, v.y), pack2<__nv_bfloat16>(v.z, v.w));
+}
+
+// The merge of both parts for the warp's 32 rows: lane r holds row r's
+// weights; rows are read and written four at a time, 32 columns (128 bytes
+// of fp32) a row per instruction.
+template <int D, typename OutT>
+__device__ __forceinline__ void merge_rows(const PrefillParams &P, const SeqRows &sr,
+                                           const PTile &tl, int slot, int t, int wq, int lane) {
+    const int r0 = 32 * wq;
+    const size_t p0 = part_row(slot, 0, t) + r0, p1 = part_row(slot, 1, t) + r0;
+    const float m0 = P.part_m[p0 + lane], m1 = P.part_m[p1 + lane];
+    const float l0 = P.part_l[p0 + lane], l1 = P.part_l[p1 + lane];
+    const float M = fmaxf(m0, m1);
+    const float c0 = m0 == -INFINITY ? 0.f : ex2(m0 - M);
+    const float c1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
+    const float lt = c0 * l0 + c1 * l1;
+    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+    const float w0 = c0 * inv, w1 = c1 * inv;
+    const float *o0 = P.part_o + p0 * D, *o1 = P.part_o + p1 * D;
+#pragma unroll 2
+    for (int g4 = 0; g4 < 8; ++g4) {
+        const int rr = g4 * 4 + lane / 8;          // the row this lane works on
+        const float a0 = __shfl_sync(0xffffffffu, w0, rr);
+        const float a1 = __shfl_sync(0xffffffffu, w1, rr);
+        const int row = tl.q0 + r0 + rr;
+        const bool live = row < sr.n;
+#pragma unroll
+        for (int cb = 0; cb < D; cb += 32) {
+            const int col = cb + (lane % 8) * 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (a0 != 0.f) {
+                const float4 x = *reinterpret_cast<const float4 *>(o0 + (size_t)rr * D + col);
+                v = make_float4(a0 * x.x, a0 * x.y, a0 * x.z, a0 * x.w);
+            }
+            if (a1 != 0.f) {
+                const float4 x = *reinterpret_cast<const float4 *>(o1 + (size_t)rr * D + col);
+                v = make_float4(fmaf(a1, x.x, v.x), fmaf(a1, x.y, v.y), fmaf(a1, x.z, v.z),
+                                fmaf(a1, x.w, v.w));
+            }
+            if (live)
+                store4<OutT>(P.out, (((size_t)sr.tok0 + row) * P.num_heads + tl.h) * D + col, v);
+        }
+    }
+}
+
+template <int D, typename T>
+__device__ __forceinline__ void merge_parts(const PrefillParams &P, const SeqRows &sr,
+                                            const PTile &tl, int slot, int t, int wq, int lane) {
+    if (P.out_dtype == PA_F32)
+        merge_rows<D, float>(P, sr, tl, slot, t, wq, lane);
+    else
+        merge_rows<D, T>(P, sr, tl, slot, t, wq, lane);
+}
+
+// ---------------------------------------------------------------------------
 // warps 0..7: softmax of query tile t = warp / 4, one row per thread, and the
 // output, item after item
 // ---------------------------------------------------------------------------
 template <int D, typename T, bool kSplit>
 __device__ __forceinline__ void run_softmax_p(const PrefillParams &P, int t, const PItem *items,
                                               unsigned char *stage, uint32_t tmem,
-                                              const Bars &B, volatile int *abort_flag, int wq,
-                                              int lane) {
+                                              const Bars &B, volatile int *abort_flag,
+                                              volatile unsigned *split_old, int wq, int lane) {
     constexpr int kNP = kSplit ? 1 : 2;      // P buffers
     const int r = 32 * wq + lane;            // this thread's query row
     const uint32_t lane_addr = (uint32_t)(32 * wq) << 16;
@@ -885,10 +1130,19 @@ __device__ __forceinline__ void run_softmax_p(const PrefillParams &P, int t, con
         const bool stop = ip->stop;
         const PTile tl = t ? ip->t[1] : ip->t[0];
         const SeqRows sr{ip->s, ip->n, ip->c, ip->L, ip->tok0};
+        const int kt0 = ip->kt0, end = min(ip->kt1, tl.nt);  // this tile's K/V tiles
+        const int slot = ip->slot, part = ip->part;
         give_item_back(B, n, lane, 0xffffffffu);
         ++n;
         if (stop) break;
         if (!tl.act) continue;
+        if (end <= kt0) {  // a part of a split item with no keys for this tile
+            const size_t mi = (((size_t)slot * 2 + part) * 2 + t) * kQM + r;
+            P.part_m[mi] = -INFINITY;
+            P.part_l[mi] = 0.f;
+            if (split_last(P, slot, t, split_old, lane)) merge_parts<D, T>(P, sr, tl, slot, t, wq, lane);
+            continue;
+        }
         const int i = tl.q0 + r;                 // new-token index of the row
         const int qpos = i < sr.n ? sr.c + i : sr.L - 1;  // padding rows see every key
         // skipped blocks, from the table: bit u of a tile's mask = unit u
@@ -899,11 +1153,12 @@ __device__ __forceinline__ void run_softmax_p(const PrefillParams &P, int t, con
             const int tok = ((bt << 5) + lane) << g.lg_tbr;
             return __ballot_sync(0xffffffffu, tok < tl.kv_end && (e < 0 || e >= P.num_blocks));
         };
-        unsigned bb = bad_of(unit_entry(P, row, g, 0, tl.kv_end, lane), 0);
-        int e_nxt = unit_entry(P, row, g, 1, tl.kv_end, lane);
+        const int b0 = kt0 >> g.lg_tpb;  // table batch of the first tile
+        unsigned bb = bad_of(unit_entry(P, row, g, b0, tl.kv_end, lane), b0);
+        int e_nxt = unit_entry(P, row, g, b0 + 1, tl.kv_end, lane);
         float m_ref = -INFINITY, lsum = 0.f;
-        for (int j = 0; j < tl.nt; ++j, ++scount, ++pc) {
-            if (j > 0 && (j & tpb_mask) == 0) {
+        for (int j = kt0; j < end; ++j, ++scount, ++pc) {
+            if (j > kt0 && (j & tpb_mask) == 0) {
                 const int bt = j >> g.lg_tpb;
                 bb = bad_of(e_nxt, bt);
                 e_nxt = unit_entry(P, row, g, bt + 1, tl.kv_end, lane);
@@ -976,7 +1231,7 @@ __device__ __forceinline__ void run_softmax_p(const PrefillParams &P, int t, con
             const bool grow = mx > m_ref + kRescaleLog2;
             if (__any_sync(0xffffffffu, grow)) {
                 const float alpha = grow && m_ref != -INFINITY ? ex2(m_ref - mx) : 1.f;
-                if (j > 0) {
+                if (j > kt0) {
                     const int pq = pc - 1;
                     if (!__all_sync(0xffffffffu,
                                     mbar_wait(&B.pv_done[2 * t + pq % kNP],
@@ -1050,11 +1305,18 @@ __device__ __forceinline__ void run_softmax_p(const PrefillParams &P, int t, con
             break;
         }
         tc_fence_after();
-        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-        if (P.out_dtype == PA_F32)
-            store_rows<D, float>(P, sr, tl, tm_o, inv, stage, &B.o_free[t], wq, lane);
-        else
-            store_rows<D, T>(P, sr, tl, tm_o, inv, stage, &B.o_free[t], wq, lane);
+        if (slot < 0) {
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            if (P.out_dtype == PA_F32)
+                store_rows<D, float>(P, sr, tl, tm_o, inv, stage, &B.o_free[t], wq, lane);
+            else
+                store_rows<D, T>(P, sr, tl, tm_o, inv, stage, &B.o_free[t], wq, lane);
+        } else {
+            // a part of a split item: its O, maximum and sum to the workspace;
+            // the part that finishes second merges both
+            store_partial<D>(P, slot, part, t, tm_o, m_ref, lsum, stage, &B.o_free[t], wq, lane);
+            if (split_last(P, slot, t, split_old, lane)) merge_parts<D, T>(P, sr, tl, slot, t, wq, lane);
+        }
     }
     if (!ok) {
         *abort_flag = 1;
@@ -1129,9 +1391,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     if (warp < kSoftmaxWarps) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         pdl_wait();  // the plan, and through it the cache write of the chunk, is complete
-        run_softmax_p<D, T, kSplit>(P, warp >> 2, items,
-                                    smem + L::stage_off + (size_t)warp * kStageWarpBytes, tmem,
-                                    B, abort_flag, warp & 3, lane);
+        run_softmax_p<D, T, kSplit>(
+            P, warp >> 2, items, smem + L::stage_off + (size_t)warp * kStageWarpBytes, tmem, B,
+            abort_flag, reinterpret_cast<volatile unsigned *>(smem + L::split_off), warp & 3, lane);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
         pdl_wait();
@@ -1203,6 +1465,33 @@ bool item_grid(int num_seqs, int num_heads, int num_kv_heads, int max_query_len,
     return true;
 }
 
+// Workspace layout for a batch (byte offsets, 256-byte aligned).
+struct PWork {
+    int max_splits;
+    size_t entries, split_cnt, part_m, part_l, part_o, bytes;
+};
+
+size_t align256p(size_t x) { return (x + 255) / 256 * 256; }
+
+PWork work_layout(unsigned long long n_items, int head_dim) {
+    PWork w;
+    w.max_splits = (int)(n_items < (unsigned long long)kMaxSplits ? n_items : kMaxSplits);
+    const size_t ms = (size_t)w.max_splits;
+    size_t off = align256p(kWorkHeader * sizeof(uint32_t));
+    w.entries = off;
+    off = align256p(off + 2 * (size_t)n_items * sizeof(uint2));
+    w.split_cnt = off;
+    off = align256p(off + ms * 2 * sizeof(uint32_t));
+    w.part_m = off;
+    off = align256p(off + ms * 4 * kQM * sizeof(float));
+    w.part_l = off;
+    off = align256p(off + ms * 4 * kQM * sizeof(float));
+    w.part_o = off;
+    off = align256p(off + ms * 4 * kQM * (size_t)head_dim * sizeof(float));
+    w.bytes = off;
+    return w;
+}
+
 int sm_count() {
     static std::atomic<int> cached[kMaxDevicesP];
     int dev = 0;
@@ -1222,13 +1511,14 @@ int sm_count() {
 using namespace pa;
 
 extern "C" size_t pa_prefill_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
-                                            int max_query_len) {
+                                            int head_dim, int max_query_len) {
     int ix = 0, iy = 0;
     unsigned long long count = 0;
+    if (head_dim != 64 && head_dim != 128) return 0;
     if (!item_grid(num_seqs, num_heads, num_kv_heads, max_query_len, &ix, &iy, &count))
         return 0;
-    const unsigned long long bytes = (count + kWorkHeader) * sizeof(uint32_t);
-    return (size_t)((bytes + 255) / 256 * 256);
+    if (count >= (1ull << 31)) return 0;
+    return work_layout(count, head_dim).bytes;
 }
 
 extern "C" pa_status_t pa_prefill_attention(
@@ -1263,9 +1553,8 @@ extern "C" pa_status_t pa_prefill_attention(
         return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
-        workspace_bytes < pa_prefill_workspace_size(num_seqs, num_heads, num_kv_heads,
-                                                    max_query_len))
+    const PWork wl = work_layout(n_items, head_dim);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < wl.bytes)
         return PA_ERR_WORKSPACE;
     const int sms = sm_count();
     if (sms <= 0) return PA_ERR_CUDA;
@@ -1319,13 +1608,22 @@ extern "C" pa_status_t pa_prefill_attention(
     P.items_x = ix;
     P.items_y = iy;
     P.num_items = (unsigned)n_items;
-    P.work = static_cast<unsigned int *>(workspace);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    P.work = reinterpret_cast<unsigned int *>(ws);
+    P.entries = reinterpret_cast<uint2 *>(ws + wl.entries);
+    P.split_cnt = reinterpret_cast<unsigned int *>(ws + wl.split_cnt);
+    P.part_m = reinterpret_cast<float *>(ws + wl.part_m);
+    P.part_l = reinterpret_cast<float *>(ws + wl.part_l);
+    P.part_o = reinterpret_cast<float *>(ws + wl.part_o);
+    P.max_splits = wl.max_splits;
     P.head_dim = head_dim;
     P.num_blocks = num_blocks;
     P.scale_log2 = scale * 1.4426950408889634f;
     P.err = dev_error_word;
-    // persistent: one CTA per SM, never more CTAs than items
-    const unsigned grid = (unsigned)(n_items < (unsigned long long)sms ? n_items : sms);
+    // persistent: one CTA per SM, never more CTAs than entries (items and parts)
+    const unsigned long long n_entries = n_items + (unsigned long long)wl.max_splits;
+    const unsigned grid = (unsigned)(n_entries < (unsigned long long)sms ? n_entries : sms);
+    P.grid = grid;
     cudaStream_t st = (cudaStream_t)stream;
     if (head_dim == 64)
         return dtype == PA_F16 ? launch_prefill<64, __half>(P, grid, st)

@@ -176,10 +176,10 @@ def test_prefill_many_items_per_cta(H, Hkv, dtype):
     cases[11] = (700, 1)                     # decode rows among the chunks
     d = _problem(cases, H, Hkv, 128, dtype, 16, seed=H + Hkv)
     maxq = d["maxq"]
-    nbytes = pa.prefill_workspace_size(len(cases), H, Hkv, maxq)
+    nbytes = pa.prefill_workspace_size(len(cases), H, Hkv, 128, maxq)
     mt = -(-maxq // 128)
     ix, iy = (mt, H // 2) if (H // Hkv) % 2 == 0 else (-(-mt // 2), H)
-    assert nbytes >= 4 * (2 + len(cases) * ix * iy) and nbytes % 256 == 0
+    assert nbytes >= 16 * len(cases) * ix * iy and nbytes % 256 == 0
     assert len(cases) * ix * iy > 2 * 152
     ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
     scale = 1.0 / np.sqrt(128)
@@ -201,15 +201,20 @@ def test_prefill_many_items_per_cta(H, Hkv, dtype):
 def test_prefill_workspace_checks():
     cases = [(10, 20), (0, 5)]
     d = _problem(cases, 4, 2, 64, "f16", 16, seed=1)
-    need = pa.prefill_workspace_size(2, 4, 2, d["maxq"])
-    assert need == 256                       # 2 header words + 2 x 1 x 2 items, rounded up
-    assert pa.prefill_workspace_size(2, 5, 2, 10) == 0      # heads not a multiple of KV heads
+    need = pa.prefill_workspace_size(2, 4, 2, 64, d["maxq"])
+    assert need % 256 == 0 and need > 4 * 128 * 64 * 4    # room for split partials
+    assert pa.prefill_workspace_size(2, 5, 2, 64, 10) == 0     # heads not a multiple of KV heads
+    assert pa.prefill_workspace_size(2, 4, 2, 96, 10) == 0     # head_dim not built
     small = torch.empty(need, dtype=torch.uint8, device=DEV)[1:]    # misaligned
     with pytest.raises(pa.PaError) as ei:
         _run(d, 0.1, workspace=small)
     assert ei.value.status == 4
-    big = pa.prefill_workspace_size(2, 4, 2, 100_000)
-    assert big > need
+    short = torch.empty(need - 256, dtype=torch.uint8, device=DEV)  # too small
+    with pytest.raises(pa.PaError) as ei:
+        _run(d, 0.1, workspace=short)
+    assert ei.value.status == 4
+    assert pa.prefill_workspace_size(2, 4, 2, 64, 100_000) > need
+    assert pa.prefill_workspace_size(2, 4, 2, 128, 20) > need
 
 
 @pytest.mark.parametrize("scale", [0.0, -0.05])
@@ -222,3 +227,31 @@ def test_prefill_non_positive_scale(scale):
     torch.cuda.synchronize()
     want = _oracle(d, scale, "bf16")
     assert max_abs(out.cpu().numpy(), want) <= ATOL
+
+
+@pytest.mark.parametrize("H,Hkv,dtype,B", [(12, 2, "bf16", 16), (6, 6, "f16", 16),
+                                          (9, 3, "bf16", 8), (4, 4, "f16", 64)])
+def test_prefill_split_items(H, Hkv, dtype, B):
+    """Items with more K/V tiles than an SM's even share are split over their
+    keys; the two parts are merged exactly.  One long sequence among many short
+    ones; a sequence whose second query tile is short, so that with tiles
+    paired by tokens the second part has no keys for the first tile; decode
+    rows; a sequence with a bad block id (its keys skipped) stays out."""
+    rng = np.random.default_rng(H + Hkv + B)
+    cases = [(3100, 256), (64, 256), (900, 129), (2000, 1)]
+    cases += [(int(rng.integers(0, 40)), int(rng.integers(1, 64))) for _ in range(40)]
+    d = _problem(cases, H, Hkv, 128, dtype, B, seed=H * 3 + B)
+    scale = 1.0 / np.sqrt(128)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(d, scale, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want = _oracle(d, scale, dtype)
+    e = max_abs(out.cpu().numpy(), want)
+    print(f"split items H={H} Hkv={Hkv} {dtype} B={B}: max|gpu-oracle| = {e:.3e}")
+    assert e <= ATOL
+    # with the output in the input dtype, the merge rounds once, like the plain path
+    d2 = _problem(cases, H, Hkv, 128, dtype, B, seed=H * 3 + B)
+    o16 = _run(d2, scale, out_dtype=TDT[dtype])
+    torch.cuda.synchronize()
+    assert torch.equal(out.to(TDT[dtype]).view(torch.int16), o16.view(torch.int16))
