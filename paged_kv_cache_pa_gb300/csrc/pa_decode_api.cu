@@ -20,6 +20,7 @@
 
 #include "pa_decode.cuh"
 #include "pa_launch.cuh"
+#include "pa_tmap.cuh"
 
 namespace pa {
 
@@ -247,45 +248,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
 
 std::atomic<int> g_sm_count[64];
 
-// cuTensorMapEncodeTiled, looked up once through the runtime's driver entry
-// point (no link against the driver library).
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn tensor_map_encoder() {
-    static std::atomic<void *> fn{nullptr};
-    void *f = fn.load(std::memory_order_acquire);
-    if (!f) {
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || !f)
-            return nullptr;
-        fn.store(f, std::memory_order_release);
-    }
-    return reinterpret_cast<EncodeTiledFn>(f);
-}
-
 // 3-D view [head_dim / 64][rows][64] of a row-major [rows][head_dim] 16-bit
 // tensor (strides: a row is head_dim * 2 bytes, a 64-element half 128 bytes);
 // one box is box_rows rows of box_halves halves (all halves, or one),
 // 128-byte swizzle; reads past the last row return zeros.
 bool encode_rows(CUtensorMap *map, const void *base, pa_dtype_t dtype, unsigned long long rows,
                  int head_dim, int box_rows, int box_halves) {
-    EncodeTiledFn enc = tensor_map_encoder();
-    if (!enc) return false;
     const cuuint64_t dims[3] = {64u, (cuuint64_t)rows, (cuuint64_t)(head_dim / 64)};
     const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, 128u};
     const cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, (cuuint32_t)box_halves};
-    const cuuint32_t elem_strides[3] = {1u, 1u, 1u};
-    return enc(map,
-               dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-               3, const_cast<void *>(base), dims, strides, box, elem_strides,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_tiled(map, base, dtype, 3, dims, strides, box);
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

@@ -255,3 +255,27 @@ def test_prefill_split_items(H, Hkv, dtype, B):
     o16 = _run(d2, scale, out_dtype=TDT[dtype])
     torch.cuda.synchronize()
     assert torch.equal(out.to(TDT[dtype]).view(torch.int16), o16.view(torch.int16))
+
+
+def test_prefill_sequences_without_new_tokens():
+    """Sequences with no new tokens in the batch (n = 0, with or without a
+    cached context) contribute no rows and no work; a batch of only such
+    sequences is a no-op."""
+    cases = [(0, 0), (40, 0), (10, 30), (0, 0), (100, 70), (300, 0), (0, 1)]
+    d = _problem(cases, 8, 2, 128, "bf16", 16, seed=21)
+    scale = 1.0 / np.sqrt(128)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(d, scale, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want = _oracle(d, scale, "bf16")
+    assert out.shape[0] == 101
+    assert max_abs(out.cpu().numpy(), want) <= ATOL
+    empty = _problem([(0, 0), (25, 0)], 8, 2, 128, "bf16", 16, seed=22)
+    q = torch.zeros(0, 8, 128, dtype=torch.bfloat16, device=DEV)
+    o = pa.prefill_attention(q, empty["kc"], empty["vc"],
+                             torch.as_tensor(empty["tables"], device=DEV),
+                             torch.as_tensor(empty["qsl"], device=DEV),
+                             torch.as_tensor(empty["lens"], device=DEV), 0, 25, scale)
+    torch.cuda.synchronize()
+    assert o.shape == (0, 8, 128)
