@@ -172,72 +172,69 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
 // One CTA per (sequence, query head) of a multi-partition sequence:
 //   M = max_p m_p,  c_p = 2^(m_p - M),  L = sum_p l_p c_p,
 //   o = sum_p acc_p c_p / L.
-// The partition weights go to shared memory once; the weighted-value loads
-// are spread over all threads (head_dim/4 float4 columns x partition groups)
-// and reduced in shared memory.
+// One pass over the partials: the threads form partition groups of head_dim/4
+// float4 columns each; group g folds partitions g, g + NG, ... into a running
+// (M, L, o), rescaling it whenever the maximum grows, so a partition's m, l
+// and acc are loaded together instead of in three dependent rounds.  The
+// groups' states are then folded the same way through shared memory.
 constexpr int kMergeThreads = 128;
-constexpr int kMergeParts = 2048;  // weights kept in shared memory up to this many partitions
+constexpr int kMergeBatch = 4;  // partitions a thread loads before folding them
+
+// (M, L, o) <- the merge of (M, L, o) and (mp, lp, a); an empty state has
+// M = -inf (ex2(-inf) = 0 drops it).
+__device__ __forceinline__ void fold_state(float &M, float &L, float4 &o, float mp, float lp,
+                                           float4 a) {
+    const float Mn = fmaxf(M, mp);
+    if (Mn == -INFINITY) return;  // both empty
+    const float c0 = ex2(M - Mn), c1 = ex2(mp - Mn);
+    L = fmaf(L, c0, lp * c1);
+    o.x = fmaf(o.x, c0, a.x * c1);
+    o.y = fmaf(o.y, c0, a.y * c1);
+    o.z = fmaf(o.z, c0, a.z * c1);
+    o.w = fmaf(o.w, c0, a.w * c1);
+    M = Mn;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ DecodeParams P) {
     constexpr int C = D / 4;                   // float4 columns
     constexpr int NG = kMergeThreads / C;      // partition groups
-    __shared__ float s_c[kMergeParts];
-    __shared__ float s_red[kMergeThreads / 32];
+    __shared__ float s_m[NG], s_l[NG];
     __shared__ float4 s_acc[NG][C];
-    const int s = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
+    const int s = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     const int L = P.context_lens[s];  // an input: complete before this grid launched
     if (L <= P.part_tokens || L > P.max_context_len) return;  // one partition, or invalid
     const int np = (L + P.part_tokens - 1) / P.part_tokens;
     pdl_wait();  // partials from the attention kernel
     const size_t base = ((size_t)s * P.num_heads + h) * P.max_parts;
-
-    float M = -INFINITY;
-    for (int p = tid; p < np; p += kMergeThreads) M = fmaxf(M, P.part_m[base + p]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if (lane == 0) s_red[tid / 32] = M;
-    __syncthreads();
-    M = s_red[0];
-#pragma unroll
-    for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, s_red[w]);
-    const float Ms = M == -INFINITY ? 0.f : M;
-    __syncthreads();
-
-    float lsum = 0.f;
-    for (int p = tid; p < np; p += kMergeThreads) {
-        const float c = ex2(P.part_m[base + p] - Ms);
-        if (p < kMergeParts) s_c[p] = c;
-        lsum = fmaf(P.part_l[base + p], c, lsum);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-    if (lane == 0) s_red[tid / 32] = lsum;
-    __syncthreads();
-    float Lsum = 0.f;
-#pragma unroll
-    for (int w = 0; w < kMergeThreads / 32; ++w) Lsum += s_red[w];
-
     const int col = tid % C, grp = tid / C;
     const float4 *acc = reinterpret_cast<const float4 *>(P.part_acc + base * D) + col;
+
+    float M = -INFINITY, Lsum = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int p = grp; p < np; p += NG) {
-        const float c = p < kMergeParts ? s_c[p] : ex2(P.part_m[base + p] - Ms);
-        const float4 a = acc[(size_t)p * C];
-        o.x = fmaf(a.x, c, o.x);
-        o.y = fmaf(a.y, c, o.y);
-        o.z = fmaf(a.z, c, o.z);
-        o.w = fmaf(a.w, c, o.w);
+    for (int p0 = grp; p0 < np; p0 += kMergeBatch * NG) {
+        float mp[kMergeBatch], lp[kMergeBatch];
+        float4 a[kMergeBatch];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+            const int p = p0 + u * NG;
+            const bool in = p < np;
+            mp[u] = in ? P.part_m[base + p] : -INFINITY;
+            lp[u] = in ? P.part_l[base + p] : 0.f;
+            a[u] = in ? acc[(size_t)p * C] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) fold_state(M, Lsum, o, mp[u], lp[u], a[u]);
+    }
+    if (col == 0) {
+        s_m[grp] = M;
+        s_l[grp] = Lsum;
     }
     s_acc[grp][col] = o;
     __syncthreads();
     if (grp == 0) {
 #pragma unroll
-        for (int g = 1; g < NG; ++g) {
-            const float4 b = s_acc[g][col];
-            o.x += b.x; o.y += b.y; o.z += b.z; o.w += b.w;
-        }
+        for (int g = 1; g < NG; ++g) fold_state(M, Lsum, o, s_m[g], s_l[g], s_acc[g][col]);
         const size_t ob = ((size_t)s * P.num_heads + h) * D + col * 4;
         store_out(P.out, P.out_dtype, ob + 0, Lsum > 0.f ? o.x / Lsum : 0.f);
         store_out(P.out, P.out_dtype, ob + 1, Lsum > 0.f ? o.y / Lsum : 0.f);
