@@ -2,7 +2,8 @@
 (prompts, forks, appends with copy-on-write) produces the copy pairs, slots,
 tables and lengths of a decode step, which runs on the GPU and in the oracle
 on the same inputs; then a beam group is swapped out to pinned host memory
-and back into other block ids, and its attention output is unchanged."""
+and back into other block ids, and the batch's attention output is
+unchanged to the bit."""
 import numpy as np
 import pytest
 import torch
@@ -79,13 +80,14 @@ def test_manager_trace_drives_a_decode_step_and_a_swap(B):
     p_in = bm.swap_in(g1)
     assert set(p_in[:, 1].tolist()).isdisjoint(set((junk_slots // B).tolist()))
     pa.swap_blocks([kc], [vc], [hk], [hv], torch.as_tensor(p_in, device=DEV), error_word=err)
-    tables2, lens2 = bm.build_batch(g1, maxb)
-    assert not np.array_equal(tables2, tables[4:8])        # other block ids now
-    # same partition size as the full batch, so the same arithmetic in the same order
-    mx = int(lens.max())
-    assert pa.decode_partition_tokens(4, Hkv, mx) == pa.decode_partition_tokens(S, Hkv, mx)
-    out2 = pa.decode_attention(q[4:8].contiguous(), kc, vc, torch.as_tensor(tables2, device=DEV),
-                               torch.as_tensor(lens2, device=DEV), mx, scale, error_word=err)
+    tables2, lens2 = bm.build_batch(seqs, maxb)
+    assert np.array_equal(lens2, lens)
+    assert not np.array_equal(tables2[4:8], tables[4:8])   # other block ids now
+    assert np.array_equal(tables2[:4], tables[:4]) and np.array_equal(tables2[8:], tables[8:])
+    # the same batch with only block ids changed: the same arithmetic in the
+    # same order, so the same bits
+    out2 = pa.decode_attention(q, kc, vc, torch.as_tensor(tables2, device=DEV), l_d,
+                               int(lens.max()), scale, error_word=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    assert torch.equal(out2, out[4:8])
+    assert torch.equal(out2, out)

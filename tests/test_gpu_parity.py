@@ -164,6 +164,48 @@ def test_empty_sequences_give_zero_rows():
     assert max_abs(got, want) <= ATOL
 
 
+# ---------------------------------------------------------------------------
+# query groups on the tensor-core kernel: extreme batch shapes for the plan,
+# the item pipeline and the merge
+# ---------------------------------------------------------------------------
+
+def test_gqa_one_long_sequence():
+    """One sequence of 20000 tokens: every item is a partition of its two
+    KV heads, and the merge folds 40 partitions per head."""
+    wl = custom_workload([20000], 12, 2, 128, "bf16", seed=21)
+    got, want = _run_and_check(wl)
+    assert max_abs(got, want) <= ATOL
+
+
+def test_gqa_fewer_items_than_ctas():
+    """Four short sequences: most CTAs get no item at all."""
+    wl = custom_workload([1, 17, 40, 33], 8, 2, 64, "f16", seed=22)
+    got, want = _run_and_check(wl, poison=True)
+    assert max_abs(got, want) <= ATOL
+
+
+def test_gqa_empty_sequences_between():
+    """Empty sequences among long and short ones give zero rows and no
+    items."""
+    lens = [0, 300, 0, 0, 5000, 0, 1, 0, 2048, 17, 0]
+    wl = custom_workload(lens, 8, 2, 128, "f16", seed=23)
+    got, want = _run_and_check(wl, poison=True)
+    for s, L in enumerate(lens):
+        if L == 0:
+            assert np.all(got[s] == 0)
+    assert max_abs(got, want) <= ATOL
+
+
+def test_gqa_many_sequences():
+    """More sequences than the plan kernel's 1024 threads (it takes them in
+    tiles) and many more items than CTAs."""
+    rng = np.random.default_rng(24)
+    lens = rng.integers(0, 90, 2500)
+    wl = custom_workload(lens, 8, 2, 64, "bf16", seed=24)
+    got, want = _run_and_check(wl)
+    assert max_abs(got, want) <= ATOL
+
+
 def test_output_is_bit_reproducible():
     wl = synthetic.make("gqa")
     vals = synthetic.make_values(wl, device=DEV)
