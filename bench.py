@@ -62,14 +62,34 @@ WORKLOADS = {
 UNIT = "GB/s"
 
 
-def algorithmic_bytes(wl, out_elt=4):
-    """(attention bytes, cache-write bytes, copy bytes) of one step."""
+def kv_tokens(wl, shared_once=True):
+    """K/V tokens one step must read.  shared_once: each physical block's
+    tokens count once however many tables hold it (the bytes that have to
+    come from memory); otherwise every sequence's own L tokens (logical).
+    The two agree unless sequences share blocks."""
+    L = wl.context_lens.astype(np.int64)
+    if not shared_once or len(L) == 0:
+        return int(L.sum())
+    B = wl.block_size
+    nb = (L + B - 1) // B
+    tables = np.asarray(wl.block_tables)
+    j = np.arange(tables.shape[1])
+    valid = j[None, :] < nb[:, None]
+    toks = np.clip(L[:, None] - j[None, :] * B, 0, B)
+    best = np.zeros(int(wl.num_blocks), np.int64)
+    np.maximum.at(best, tables[valid].astype(np.int64), toks[valid])
+    return int(best.sum())
+
+
+def algorithmic_bytes(wl, out_elt=4, shared_once=True):
+    """(attention bytes, cache-write bytes, copy bytes) of one step; blocks
+    shared by several sequences count once unless shared_once is False."""
     S, H, Hkv, D, elt = wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, 2
     L = wl.context_lens.astype(np.int64)
     B = wl.block_size
     nb = (L + B - 1) // B
-    attn = int(L.sum()) * Hkv * D * elt * 2 + S * H * D * elt + S * H * D * out_elt + \
-        int(nb.sum()) * 4 + S * 4
+    attn = kv_tokens(wl, shared_once) * Hkv * D * elt * 2 + S * H * D * elt + \
+        S * H * D * out_elt + int(nb.sum()) * 4 + S * 4
     write = 2 * (S * Hkv * D * elt * 2) + S * 8
     copy = 2 * len(wl.copy_pairs) * Hkv * B * D * elt * 2
     return attn, write, copy
@@ -747,6 +767,7 @@ def main():
     ms_per_step = total_ms / K
 
     b_attn, b_write, b_copy = algorithmic_bytes(wl)
+    b_attn_logical = algorithmic_bytes(wl, shared_once=False)[0]
     b_step = b_attn + b_write + b_copy
     value = world * b_step / (ms_per_step * 1e-3) / 1e9
     # roofline: the attention call's algorithmic bytes over the timed region's
@@ -931,6 +952,12 @@ def main():
                           if wl.kv_bytes() > (256 << 20) else "K/V per step near or below L2 size"),
                    "parallelism": f"replicas x{world}", "launch": timed_launch},
         "seqs_per_s_per_layer": round(world * S / (ms_per_step * 1e-3), 1),
+        # blocks shared by several sequences (copy-on-write prefixes) are
+        # counted once above; here once per sequence that reads them
+        "logical": ({"attention_bytes": int(b_attn_logical),
+                     "GBps": round(world * (b_attn_logical + b_write + b_copy) /
+                                   (ms_per_step * 1e-3) / 1e9, 2)}
+                    if b_attn_logical != b_attn else None),
         "pct_of_peak": {"measured_copy": round(100 * value / world / peak, 2),
                         "spec_8000": round(100 * value / world / 8000.0, 2)},
         "roofline": {"bound": "hbm", "achieved": round(attn_gbs, 2), "peak": peak,

@@ -83,3 +83,18 @@ def test_algorithmic_bytes_closed_form():
     assert copy == 0
     b = synthetic.make("beams")
     assert bench.algorithmic_bytes(b)[2] == 2 * len(b.copy_pairs) * 40 * 16 * 128 * 2 * 2
+
+
+def test_shared_blocks_count_once():
+    """Two sequences of 20 tokens share their first block: 16 + 4 + 4 tokens
+    must come from memory, 40 are read logically."""
+    wl = synthetic._from_lengths("pair", np.array([20, 20]), 4, 2, 64, "f16", 1,
+                                 np.random.default_rng(1), pool_blocks=8)
+    wl.block_tables = np.array([[5, 1], [5, 2]], np.int32)
+    assert bench.kv_tokens(wl) == 24
+    assert bench.kv_tokens(wl, shared_once=False) == 40
+    b = synthetic.make("beams")
+    assert bench.kv_tokens(b) < bench.kv_tokens(b, shared_once=False)
+    for name in ("tiny", "gqa"):      # no sharing: the two counts agree
+        w = synthetic.make(name)
+        assert bench.kv_tokens(w) == bench.kv_tokens(w, shared_once=False)
