@@ -731,30 +731,74 @@ def main():
             timed_launch = f"eager (faster than a CUDA graph of {g_steps} steps here)"
         else:
             timed_launch += " (faster than eager launches here)"
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    # K steps back to back, events only at the two ends (an event between two
+    # kernels would cut their programmatic overlap); the steps replay a CUDA
+    # graph of g captured steps (g divides K), so short steps are not bound by
+    # the host's launch overhead
+    def back_to_back():
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        barrier()
+        t_start.record(stream)
+        if timed_graph is not None:
+            for _ in range(K // g_steps):
+                timed_graph.replay()
+        else:
+            for i in range(K):
+                step()
+        t_end.record(stream)
+        barrier()
+        return reduce_max(t_start.elapsed_time(t_end), dist, dev)
+
+    # K/V within a few L2 sizes: the timed steps are separated by an L2
+    # flush (a read of twice the L2, so no dirty lines are left to write
+    # back), each step timed alone between events; back to back is reported
+    # as the hot-L2 figure
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (126 << 20)
+    near_l2 = wl.kv_bytes() < 4 * l2_bytes
+    if near_l2:
+        flush_buf = torch.ones(l2_bytes, dtype=torch.float16, device=dev)  # 2 x L2 bytes
+        one_step = None
+        try:
+            one_step = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(one_step):
+                step()
+            one_step.replay()
+            torch.cuda.synchronize(dev)
+        except Exception:  # capture not possible here: eager launches
+            one_step = None
+            torch.cuda.synchronize(dev)
+        run_one = one_step.replay if one_step is not None else step
+        for _ in range(3):
+            flush_buf.sum()
+            run_one()
+
     sampler = ClockSampler(local_rank) if rank == 0 or world > 1 else None
     if sampler:
         sampler.start()
     barrier()
     wall0 = time.time()
-    # the timed region: K steps back to back, events only at its two ends
-    # (an event between two kernels would cut their programmatic overlap);
-    # the steps replay a CUDA graph of g captured steps (g divides K), so
-    # short steps are not bound by the host's launch overhead
-    t_start.record(stream)
-    if timed_graph is not None:
-        for _ in range(K // g_steps):
-            timed_graph.replay()
-    else:
+    if near_l2:
+        ca = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        cb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
         for i in range(K):
-            step()
-    t_end.record(stream)
-    barrier()
+            flush_buf.sum()
+            ca[i].record(stream)
+            run_one()
+            cb[i].record(stream)
+        barrier()
+        total_ms = reduce_max(sum(a.elapsed_time(b) for a, b in zip(ca, cb)), dist, dev)
+        timed_launch = ("each step timed alone after an L2 flush, " +
+                        ("a CUDA graph of one step" if one_step is not None else "eager launches"))
+    else:
+        total_ms = back_to_back()
     wall1 = time.time()
     clocks = sampler.stop(wall0, wall1) if sampler else None
-    total_ms = t_start.elapsed_time(t_end)
-    total_ms = reduce_max(total_ms, dist, dev)
+    hot = None
+    if near_l2:
+        hot_ms = back_to_back()
+        hot = {"ms_per_step": round(hot_ms / K, 4), "launch": "back to back, " + (
+            f"CUDA graph of {g_steps} steps" if timed_graph is not None else "eager")}
     # the attention call timed alone: K more eager steps with an event pair
     # around every call, on the launching stream (each call then also waits
     # for the host to submit its three launches; reported beside the roofline)
@@ -770,6 +814,8 @@ def main():
     b_attn_logical = algorithmic_bytes(wl, shared_once=False)[0]
     b_step = b_attn + b_write + b_copy
     value = world * b_step / (ms_per_step * 1e-3) / 1e9
+    if hot is not None:
+        hot["value"] = round(world * b_step / (hot["ms_per_step"] * 1e-3) / 1e9, 2)
     # roofline: the attention call's algorithmic bytes over the timed region's
     # step time, which also holds the cache write (and the copy-on-write copies
     # where the workload has them), so the duration is an upper bound
@@ -906,6 +952,8 @@ def main():
         e2e = {"value": round(world * b_step / (e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e_ms, 4), "steps": n_e2e, "launch": launch}
+        if near_l2:
+            e2e["l2"] = "steps back to back, no L2 flush (hot)"
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -949,7 +997,10 @@ def main():
                    "mean_context": round(float(wl.context_lens.mean()), 1),
                    "kv_bytes_per_step": int(wl.kv_bytes()),
                    "l2": ("inputs larger than L2 (K/V read per step >> 126 MB L2)"
-                          if wl.kv_bytes() > (256 << 20) else "K/V per step near or below L2 size"),
+                          if not near_l2 else
+                          f"K/V per step within a few L2 sizes: an L2 flush (a read of "
+                          f"{2 * l2_bytes >> 20} MiB) before every timed step; hot_l2 = "
+                          f"the same steps back to back"),
                    "parallelism": f"replicas x{world}", "launch": timed_launch},
         "seqs_per_s_per_layer": round(world * S / (ms_per_step * 1e-3), 1),
         # blocks shared by several sequences (copy-on-write prefixes) are
@@ -970,7 +1021,9 @@ def main():
                      "ms": round(ms_per_step, 4), "algorithmic_bytes": int(b_attn),
                      "isolated_call": {"ms_per_call": round(attn_ms, 4),
                                        "achieved": round(attn_gbs_isolated, 2),
-                                       "how": "eager, an event pair around each call"}},
+                                       "how": "eager, an event pair around each call" +
+                                              (", no L2 flush" if near_l2 else "")}},
+        "hot_l2": hot,
         "gpu_launches": int(K * launches_per_step),
         "clocks": clocks,
         "e2e": e2e,
