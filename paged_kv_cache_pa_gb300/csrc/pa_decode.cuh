@@ -352,6 +352,11 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
         }
         __syncwarp();
     }
+    // The claim issued last is never used.  The fence waits until it (and
+    // every claim before it) has been performed, so the counter is final
+    // before the next call's plan kernel, which may start once this trigger
+    // has fired in every CTA, resets it.
+    __threadfence();
     pdl_trigger();
 }
 

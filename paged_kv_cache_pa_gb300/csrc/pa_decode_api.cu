@@ -75,6 +75,16 @@ WsLayout ws_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
 // and zero the output rows of empty sequences.  Sequences are taken 1024 at
 // a time, one per thread; shared-memory counters are bumped once per warp
 // and size (warp-aggregated), so threads do not queue on one address.
+//
+// The work list is built before the programmatic-dependent-launch wait, so
+// it overlaps the kernel before this call on the stream (typically the cache
+// write); only the output rows wait for it.  Reading context_lens that early
+// is safe because it is an input: a kernel that wrote it has completed before
+// this grid starts, unless that kernel let dependents launch before writing
+// it.  Writing the work list that early is safe because the attention
+// kernels of earlier calls that share the workspace have finished with it:
+// their producers read it, and release the claim counter with a fence,
+// before they allow dependents to launch.
 constexpr int kPlanThreads = 1024;
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
@@ -82,7 +92,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
     int num_kv_heads, int num_heads, int head_dim, int4 *__restrict__ items, WsHeader *hdr,
     void *out, int out_dtype, unsigned int *err) {
     pdl_trigger();  // the attention CTAs may start their set-up now
-    pdl_wait();     // inputs written by earlier work on the stream are ready
     constexpr int kKeys = kMaxPartTokens / kBlock + 1;
     __shared__ int hist[kKeys];
     __shared__ int offs[kKeys];
@@ -91,7 +100,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
     const unsigned lt_mask = (1u << lane) - 1u;
     if (tid < kKeys) hist[tid] = 0;
     __syncthreads();
-    // pass 1: histogram of partition sizes (in blocks); zero empty rows
+    // pass 1: histogram of partition sizes (in blocks)
     for (int s0 = 0; s0 < num_seqs; s0 += kPlanThreads) {
         const int s = s0 + tid;
         int L = s < num_seqs ? lens[s] : 1;
@@ -109,15 +118,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
         const int key = live ? (L - (np - 1) * part_tokens + kBlock - 1) / kBlock : 0;
         const unsigned same = __match_any_sync(0xffffffffu, key);
         if (live && (same & lt_mask) == 0) atomicAdd(&hist[key], __popc(same));
-        // the warp zeroes the output rows of its empty sequences together
-        unsigned empty = __ballot_sync(0xffffffffu, s < num_seqs && L == 0);
-        while (empty) {
-            const int src = __ffs(empty) - 1;
-            empty &= empty - 1;
-            const size_t base = (size_t)(s0 + (tid & ~31) + src) * num_heads * head_dim;
-            for (int i = lane; i < num_heads * head_dim; i += 32)
-                store_out(out, out_dtype, base + i, 0.f);
-        }
     }
     __syncthreads();
     if (tid < 32) {  // exclusive scan over sizes, largest first
@@ -166,6 +166,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
         if (live && lane == leader) slot = atomicAdd(&offs[key], __popc(same));
         slot = __shfl_sync(0xffffffffu, slot, leader) + __popc(same & lt_mask);
         if (live) items[slot] = make_int4(s, np - 1, ntok, np);
+    }
+    pdl_wait();  // earlier work on the stream may still read out
+    // the warp zeroes the output rows of its empty sequences together
+    for (int s0 = 0; s0 < num_seqs; s0 += kPlanThreads) {
+        const int s = s0 + tid;
+        const int L = s < num_seqs ? lens[s] : 1;
+        unsigned empty = __ballot_sync(0xffffffffu, s < num_seqs && (L <= 0 || L > max_context_len));
+        while (empty) {
+            const int src = __ffs(empty) - 1;
+            empty &= empty - 1;
+            const size_t base = (size_t)(s0 + (tid & ~31) + src) * num_heads * head_dim;
+            for (int i = lane; i < num_heads * head_dim; i += 32)
+                store_out(out, out_dtype, base + i, 0.f);
+        }
     }
 }
 
