@@ -167,7 +167,12 @@ int pa_decode_partition_tokens(int num_seqs, int num_kv_heads, int max_context_l
  * k_cache, v_cache  device pools, layout above
  * block_tables  device int32 [num_seqs][max_blocks_per_seq]; entries past a
  *               sequence's ceil(L/16) blocks are never read
- * context_lens  device int32 [num_seqs], each in [0, max_context_len]
+ * context_lens  device int32 [num_seqs], each in [0, max_context_len]; read
+ *               as soon as the call's first kernel starts, which may be
+ *               before the kernel enqueued ahead of it has finished (the
+ *               call's kernels use programmatic dependent launch), so it
+ *               must not be written by a kernel that lets dependents launch
+ *               before writing it (ordinary kernels and copies are fine)
  * max_context_len  host-known upper bound on context_lens,
  *               <= 16 * max_blocks_per_seq
  * num_heads % num_kv_heads == 0, num_heads / num_kv_heads <= 8,
