@@ -216,6 +216,50 @@ def test_output_is_bit_reproducible():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
+@pytest.mark.parametrize("H,Hkv,D,dtype", [(8, 8, 128, "f16"), (12, 2, 128, "bf16")])
+def test_back_to_back_calls_share_a_workspace(H, Hkv, D, dtype):
+    """Calls enqueued back to back on one stream, alternating two batches of
+    different lengths (different work lists) and sharing one workspace,
+    each after a cache write as in a decode step: every output equals the
+    one the same batch gives alone, to the bit.  The plan kernel of a call
+    rewrites the work list while the kernel ahead of it may still run, so a
+    race with the previous call's attention would show here."""
+    rng = np.random.default_rng(31)
+    lens_a = rng.integers(1, 3000, 48)
+    lens_b = rng.integers(1, 600, 48)
+    lens_b[::7] = 2999                          # a few long ones: several partitions
+    wl = custom_workload(np.maximum(lens_a, lens_b), H, Hkv, D, dtype, seed=31)
+    vals = synthetic.make_values(wl, device=DEV)
+    tables = torch.as_tensor(wl.block_tables, device=DEV)
+    mx = int(wl.max_context_len)
+    la = torch.as_tensor(lens_a.astype(np.int32), device=DEV)
+    lb = torch.as_tensor(lens_b.astype(np.int32), device=DEV)
+    slots = torch.full((wl.num_seqs,), -1, dtype=torch.int64, device=DEV)  # a write of nothing
+    S = wl.num_seqs
+    nbytes = pa.decode_workspace_size(S, H, Hkv, D, mx)
+    err = _err_word()
+
+    def call(lens, ws, out):
+        pa.cache_write(vals["key"], vals["value"], vals["k_cache"], vals["v_cache"], slots,
+                       error_word=err)
+        pa.decode_attention(vals["q"], vals["k_cache"], vals["v_cache"], tables, lens, mx,
+                            wl.scale, out=out, workspace=ws, error_word=err)
+
+    ref = {}
+    for name, lens in (("a", la), ("b", lb)):
+        ref[name] = torch.empty(S, H, D, dtype=torch.float32, device=DEV)
+        call(lens, torch.empty(nbytes, dtype=torch.uint8, device=DEV), ref[name])
+        torch.cuda.synchronize()
+    shared = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    outs = [torch.empty(S, H, D, dtype=torch.float32, device=DEV) for _ in range(40)]
+    for i, out in enumerate(outs):
+        call(la if i % 2 == 0 else lb, shared, out)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for i, out in enumerate(outs):
+        assert torch.equal(out, ref["a" if i % 2 == 0 else "b"]), i
+
+
 # ---------------------------------------------------------------------------
 # other block sizes (pools of B tokens per block, the *_ex entry points)
 # ---------------------------------------------------------------------------
