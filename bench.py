@@ -275,7 +275,8 @@ def run_reference(args, wl, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * tot_t / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "opt13b-shaped decode step (S=256, H=Hkv=40, D=128, fp16)",
+        "config": {"workload": WORKLOADS.get(args.config, args.config),
+                   "parallelism": f"replicas x{world} (rank 0 runs the oracle)",
                    "sample_seqs_per_step": n, "distinct_samples": n_distinct},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
                          "kind": "oracle",
