@@ -62,7 +62,7 @@ typedef enum { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2 } pa_dtype_t;
 typedef enum {
     PA_OK = 0,
     PA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned base, bad enum */
-    PA_ERR_UNSUPPORTED = 2,   /* a size this build has no kernel for */
+    PA_ERR_UNSUPPORTED = 2,   /* a size no kernel of the library handles */
     PA_ERR_CUDA = 3,          /* a CUDA launch or attribute call failed */
     PA_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required */
     PA_ERR_TIMEOUT = 5,       /* reserved: reported through PA_ERRBIT_TIMEOUT */
