@@ -260,6 +260,36 @@ def test_back_to_back_calls_share_a_workspace(H, Hkv, D, dtype):
         assert torch.equal(out, ref["a" if i % 2 == 0 else "b"]), i
 
 
+def _fuzz_case(i):
+    """Seeded random shape i: query groups 1..8, KV heads 1..8, head_dim 64 /
+    128 / 256, fp16 / bf16, blocks of 8..256 tokens, 1..40 sequences with a
+    mix of empty, short and long contexts."""
+    rng = np.random.default_rng(7000 + i)
+    hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.integers(1, 9))
+    D = int(rng.choice([64, 128, 256]))
+    dtype = str(rng.choice(["f16", "bf16"]))
+    B = int(rng.choice([8, 16, 16, 32, 64, 128, 256]))
+    S = int(rng.integers(1, 41))
+    kind = rng.integers(0, 4, S)
+    lens = np.where(kind == 0, 0, np.where(kind == 1, rng.integers(1, 40, S),
+                                           rng.integers(40, 3000, S)))
+    if not lens.any():
+        lens[0] = int(rng.integers(1, 3000))
+    return lens, G * hkv, hkv, D, dtype, B
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_shapes(i):
+    lens, H, Hkv, D, dtype, B = _fuzz_case(i)
+    wl = custom_workload(lens, H, Hkv, D, dtype, seed=7000 + i, block_size=B)
+    got, want = _run_and_check(wl, poison=True)
+    for s, L in enumerate(lens):
+        if L == 0:
+            assert np.all(got[s] == 0)
+    assert max_abs(got, want) <= ATOL, (H, Hkv, D, dtype, B, len(lens))
+
+
 # ---------------------------------------------------------------------------
 # other block sizes (pools of B tokens per block, the *_ex entry points)
 # ---------------------------------------------------------------------------
