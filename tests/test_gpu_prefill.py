@@ -279,3 +279,38 @@ def test_prefill_sequences_without_new_tokens():
                              torch.as_tensor(empty["lens"], device=DEV), 0, 25, scale)
     torch.cuda.synchronize()
     assert o.shape == (0, 8, 128)
+
+
+def _random_prefill(i):
+    """Seeded random batch i: query groups 1..6, KV heads 1..4, head_dim 64 or
+    128, fp16 / bf16, blocks of 8..256 tokens, 1..9 sequences each with a
+    cached prefix of 0..2500 tokens and 0..600 new ones."""
+    rng = np.random.default_rng(9100 + i)
+    hkv = int(rng.integers(1, 5))
+    H = hkv * int(rng.integers(1, 7))
+    D = int(rng.choice([64, 128]))
+    dtype = str(rng.choice(["f16", "bf16"]))
+    B = int(rng.choice([8, 16, 16, 32, 64, 256]))
+    S = int(rng.integers(1, 10))
+    cases = [(int(rng.integers(0, 2501)) * int(rng.integers(0, 2)), int(rng.integers(0, 601)))
+             for _ in range(S)]
+    if all(n == 0 for _, n in cases):
+        cases[0] = (cases[0][0], 1)
+    return cases, H, hkv, D, dtype, B
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_prefill_random_batches(i):
+    cases, H, Hkv, D, dtype, B = _random_prefill(i)
+    d = _problem(cases, H, Hkv, D, dtype, B, seed=9100 + i)
+    scale = 1.0 / np.sqrt(D)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(d, scale, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want = _oracle(d, scale, dtype)
+    assert np.array_equal(codes(d["kc"]), d["host"]["kc"])
+    assert np.array_equal(codes(d["vc"]), d["host"]["vc"])
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    assert max_abs(got, want) <= ATOL, (cases, H, Hkv, D, dtype, B)
