@@ -331,11 +331,15 @@ pa_status_t pa_decode_attention_contiguous(void *out, pa_dtype_t out_dtype, cons
  * built into the library, which every GPU that loads the library keeps until
  * the process exits.  It calls no allocator (no cudaMalloc, cudaFree or
  * allocating library routine).
- *   - Sizes whose pa_decode_workspace_size exceeds PA_NOALLOC_WORKSPACE_BYTES
- *     are rejected with PA_ERR_WORKSPACE before anything is enqueued.
- *   - The first call on each device, made with that device current, looks up
- *     the array's device address (cudaGetSymbolAddress); make that first call
- *     before any stream capture.
+ *   - Arguments are checked exactly as pa_decode_attention checks them, in
+ *     the same order; otherwise valid sizes whose pa_decode_workspace_size
+ *     exceeds PA_NOALLOC_WORKSPACE_BYTES are then rejected with
+ *     PA_ERR_WORKSPACE.  Nothing is enqueued on any error.
+ *   - Every call looks up the array's device address (cudaGetSymbolAddress)
+ *     in the context current at the call, so a device reset or another
+ *     context on the same device is followed.  The first call in a context
+ *     loads the library's device code there; make that first call before any
+ *     stream capture.
  *   - All calls on a device share the array, which keeps the last call's
  *     contents; nothing in it needs to start at zero.  Calls that overlap on
  *     the GPU (e.g. on unordered streams) race on it: order them.

@@ -14,13 +14,11 @@
 // which this library's device code is loaded holds that memory until the
 // process exits.  All calls on a device share it, and it keeps whatever the
 // last call left there.  The decode path needs nothing in it to start at
-// zero: the plan kernel of each call rewrites the part it reads (the claim
-// counter and the work list) before use.  Two calls whose work overlaps on
-// the GPU (for example on two streams without ordering between them) race on
-// the array and give wrong results; order them on one stream.
+// zero: each call rewrites the part it reads (the claim counter and the work
+// list) before use.  Two calls whose work overlaps on the GPU (for example
+// on two streams without ordering between them) race on the array and give
+// wrong results; order them on one stream.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "pa.h"
 
@@ -28,12 +26,8 @@ namespace {
 
 // Device-side scratch for pa_decode_attention_noalloc.  In host code this name
 // is only a stand-in for the symbol: its device address comes from
-// cudaGetSymbolAddress, done once per device below.
+// cudaGetSymbolAddress, with the caller's device (and context) current.
 static __device__ __align__(256) unsigned char g_noalloc_workspace[PA_NOALLOC_WORKSPACE_BYTES];
-
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_workspace_addr[kMaxDevices];  // device address of the array, per device
 
 }  // namespace
 
@@ -43,26 +37,16 @@ extern "C" pa_status_t pa_decode_attention_noalloc(
     int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
     int num_blocks, float scale, pa_dtype_t dtype, unsigned int *dev_error_word,
     pa_stream_t stream) {
-    const size_t need = pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim,
-                                                 max_context_len);
-    if (need > (size_t)PA_NOALLOC_WORKSPACE_BYTES) return PA_ERR_WORKSPACE;
-
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+    // The array's address is looked up on every call, in the context current
+    // now: after a device reset, or under another context, the library's
+    // device code is loaded again and the array can move.  The first lookup
+    // in a context loads the library's device code there; later ones are a
+    // host-side table lookup.
     void *ws = nullptr;
-    {
-        // First call on this device, with the device current: look up the
-        // array's device address (this may load the library's device code).
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_workspace_addr[dev]) {
-            void *addr = nullptr;
-            if (cudaGetSymbolAddress(&addr, g_noalloc_workspace) != cudaSuccess || !addr)
-                return PA_ERR_CUDA;
-            g_workspace_addr[dev] = addr;
-        }
-        ws = g_workspace_addr[dev];
-    }
+    if (cudaGetSymbolAddress(&ws, g_noalloc_workspace) != cudaSuccess || !ws) return PA_ERR_CUDA;
+    // pa_decode_attention checks every argument first, in its own order, and
+    // returns PA_ERR_WORKSPACE only for otherwise valid sizes whose workspace
+    // exceeds the array.
     return pa_decode_attention(out, out_dtype, query, k_cache, v_cache, block_tables,
                                max_blocks_per_seq, context_lens, max_context_len, num_seqs,
                                num_heads, num_kv_heads, head_dim, num_blocks, scale, dtype, ws,

@@ -22,8 +22,9 @@ Shapes follow the pages' workloads:
   scattered blocks"]), batch 64, lengths uniform in [512, 4096].
 * ``beams``: 32 prompts x 6 beams, OPT-13B head shape, fp16, a 512-token
   prompt shared by the 6 beams of a group, 1..256 suffix tokens per group
-  grown by a seeded beam search through :mod:`block_manager`; each step
-  copies shared partial last blocks (copy-on-write) before writing.
+  grown by a seeded beam search through the host block ledger
+  (:class:`block_manager.BlockLedger`); each step copies shared partial last
+  blocks (copy-on-write) before writing.
 * ``long``: 8 sequences of 16384..32768 tokens, OPT-13B head shape, fp16,
   blocks drawn without replacement from a 196,608-block (60 GiB K+V) pool.
 
@@ -45,7 +46,7 @@ from typing import Dict, Optional
 
 import numpy as np
 
-from .block_manager import BLOCK_SIZE, BlockPool, Sequence, blocks_for
+from .block_manager import BLOCK_SIZE, BlockLedger, blocks_for
 
 CONFIGS = ("tiny", "opt13b", "gqa", "beams", "long")
 SEEDS = {name: 1001 + i for i, name in enumerate(CONFIGS)}
@@ -201,29 +202,30 @@ def make_beams(seed: Optional[int] = None, groups: int = 32, beams: int = 6,
     # blocks a step allocates before it frees the old beams
     per_group = 2 * beams * blocks_for(max_len) + blocks_for(prompt)
     pool_blocks = groups * per_group
-    pool = BlockPool(pool_blocks, free_order=rng.permutation(pool_blocks).tolist())
+    ledger = BlockLedger(pool_blocks, free_order=rng.permutation(pool_blocks).tolist())
     all_beams = []
     for g in range(groups):
-        root = Sequence(pool)
-        root.reserve(prompt)
-        group = [root] + [root.fork() for _ in range(beams - 1)]
+        root = ledger.new_sequence()
+        ledger.append(root, prompt)
+        group = [root] + [ledger.fork(root) for _ in range(beams - 1)]
         for _ in range(int(suffix[g]) - 1):
             for b in group:
-                b.reserve(1)
+                ledger.append(b, 1)
             parents = rng.integers(0, beams, beams)
-            new = [group[p].fork() for p in parents]
+            new = [ledger.fork(group[p]) for p in parents]
             for b in group:
-                b.free()
+                ledger.release(b)
             group = new
         all_beams.extend(group)
-    pool.take_copies()                       # history; not part of the step
-    slots = np.array([b.reserve(1)[0] for b in all_beams], np.int64)
-    pairs = np.array(pool.take_copies(), np.int64).reshape(-1, 2)
-    lens = np.array([b.n for b in all_beams], np.int32)
+    ledger.take_copies()                     # history; not part of the step
+    slots = np.array([ledger.append(b, 1)[0] for b in all_beams], np.int64)
+    pairs = np.array(ledger.take_copies(), np.int64).reshape(-1, 2)
+    lens = np.array([ledger.length(b) for b in all_beams], np.int32)
     maxb = blocks_for(max_len)
     tables = np.full((len(all_beams), maxb), -1, np.int32)
     for i, b in enumerate(all_beams):
-        tables[i, :len(b.table)] = b.table
+        t = ledger.table(b)
+        tables[i, :len(t)] = t
     used = np.unique(tables[tables >= 0]).astype(np.int64)
     logical = int(sum(blocks_for(int(L)) for L in lens))
     return Workload(name="beams", num_seqs=len(all_beams), num_heads=num_heads,

@@ -7,7 +7,7 @@ import pytest
 
 from conftest import golden
 from paged_kv_cache_pa_gb300 import PaError
-from paged_kv_cache_pa_gb300.block_manager import BlockPool, OutOfBlocks, Sequence, blocks_for
+from paged_kv_cache_pa_gb300.block_manager import BlockLedger, OutOfBlocks, blocks_for
 from paged_kv_cache_pa_gb300.manager import BlockManager, NoFreeBlocks
 
 
@@ -94,26 +94,26 @@ def test_cow_trace_two_samples():
 
 
 # ---------------------------------------------------------------------------
-# the same behaviour as the Python host shim on random traces
+# the same behaviour as the Python block ledger on random traces
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("seed,B", [(0, 16), (1, 16), (2, 8), (3, 4), (4, 64)])
-def test_random_trace_matches_the_python_shim(seed, B):
-    """Seeded random create / append / fork / free operations on both
-    managers: identical tables, lengths, slots, copy-on-write pairs, free
-    counts and reference counts after every operation, including the failed
-    appends when the pool runs dry."""
+def test_random_trace_matches_the_python_ledger(seed, B):
+    """Seeded random create / append / fork / free operations on the native
+    manager and the Python ledger: identical tables, lengths, slots,
+    copy-on-write pairs, free counts and reference counts after every
+    operation, including the refused appends when the pool runs dry."""
     rng = np.random.default_rng(seed)
     NB = 96
     bm = BlockManager(NB, block_size=B)
-    pool = BlockPool(NB, block_size=B)
-    live = {}                                      # native id -> python Sequence
+    led = BlockLedger(NB, block_size=B)
+    live = {}                                      # native id -> ledger id
     failures = 0
     for _ in range(600):
         op = rng.choice(["new", "append", "append", "append", "fork", "free"])
         if op == "new" or not live:
             s = bm.new_sequence()
-            live[s] = Sequence(pool)
+            live[s] = led.new_sequence()
             op, n = "append", int(rng.integers(1, 3 * B))
             target = s
         else:
@@ -121,34 +121,26 @@ def test_random_trace_matches_the_python_shim(seed, B):
             n = int(rng.integers(0, 2 * B)) if rng.random() < 0.3 else 1
         if op == "append":
             try:
-                want = live[target].reserve(n)
+                want = led.append(live[target], n)
             except OutOfBlocks:
+                # both refuse and both stay as they were
                 with pytest.raises(NoFreeBlocks):
                     bm.append(target, n)
-                # the shim may have changed state before running dry: rebuild
-                # the comparison from the native manager's unchanged state
-                live[target].table = bm.table(target)
-                live[target].n = bm.seq_len(target)
-                pool.refs = [bm.refcount(b) for b in range(NB)]
-                pool._queue = []
-                pool._heap = sorted(b for b in range(NB) if pool.refs[b] == 0)
-                assert len(bm.take_copies()) == 0      # nothing was queued
-                pool.copies = []
                 failures += 1
-                continue
-            got = bm.append(target, n)
-            assert got.tolist() == want
+            else:
+                got = bm.append(target, n)
+                assert got.tolist() == want
         elif op == "fork":
             c = bm.fork(target)
-            live[c] = live[target].fork()
+            live[c] = led.fork(live[target])
         elif op == "free":
             bm.free(target)
-            live.pop(target).free()
-        for s, py in live.items():
-            assert bm.table(s) == py.table and bm.seq_len(s) == py.n
-        assert bm.num_free_gpu == pool.num_free
-        assert [tuple(p) for p in bm.take_copies().tolist()] == pool.take_copies()
-        assert [bm.refcount(b) for b in range(NB)] == pool.refs
+            led.release(live.pop(target))
+        for s, ls in live.items():
+            assert bm.table(s) == led.table(ls) and bm.seq_len(s) == led.length(ls)
+        assert bm.num_free_gpu == led.num_free
+        assert [tuple(p) for p in bm.take_copies().tolist()] == led.take_copies()
+        assert [bm.refcount(b) for b in range(NB)] == led.refcounts()
     assert failures > 0                            # the trace ran the pool dry
 
 

@@ -7,7 +7,7 @@ import pytest
 
 from conftest import golden
 from paged_kv_cache_pa_gb300 import synthetic
-from paged_kv_cache_pa_gb300.block_manager import BlockPool, OutOfBlocks, Sequence, blocks_for
+from paged_kv_cache_pa_gb300.block_manager import BlockLedger, OutOfBlocks, blocks_for
 
 
 def _ints(v):
@@ -19,84 +19,105 @@ def test_interleaved_sequences_tables():
     B, NB, steps = int(g["block_size"][0][0]), int(g["pool_blocks"][0][0]), int(g["steps"][0][0])
     rows = {int(r[0]): r for r in g["seq"]}
     prompts = {i: int(r[r.index("prompt") + 1]) for i, r in rows.items()}
-    pool = BlockPool(NB, block_size=B)
-    seqs = [Sequence(pool) for _ in rows]
+    led = BlockLedger(NB, block_size=B)
+    seqs = [led.new_sequence() for _ in rows]
     for t in range(steps):
         for i, s in enumerate(seqs):
-            s.reserve(prompts[i] if t == 0 else 1)
+            led.append(s, prompts[i] if t == 0 else 1)
     for i, r in rows.items():
-        assert seqs[i].n == int(r[r.index("stored") + 1])
-        assert seqs[i].table == _ints(r[r.index("table") + 1:])
-    assert pool.num_free == int(g["free"][0][0])
-    assert pool.copies == []
+        assert led.length(seqs[i]) == int(r[r.index("stored") + 1])
+        assert led.table(seqs[i]) == _ints(r[r.index("table") + 1:])
+    assert led.num_free == int(g["free"][0][0])
+    assert led.take_copies() == []
 
 
 def test_parallel_sampling_copy_on_write():
     g = golden("parallel_sampling.txt")
     B = int(g["block_size"][0][0])
     prompt, samples, new = (int(g[k][0][0]) for k in ("prompt", "samples", "new_tokens"))
-    pool = BlockPool(64, block_size=B)
-    first = Sequence(pool)
-    first.reserve(prompt)
-    assert len(first.table) == int(g["prompt_blocks"][0][0])
-    assert first.fills()[-1][1] == int(g["last_block_fill"][0][0])
-    seqs = [first] + [first.fork() for _ in range(samples - 1)]
+    led = BlockLedger(64, block_size=B)
+    first = led.new_sequence()
+    led.append(first, prompt)
+    assert len(led.table(first)) == int(g["prompt_blocks"][0][0])
+    assert led.fills(first)[-1][1] == int(g["last_block_fill"][0][0])
+    seqs = [first] + [led.fork(first) for _ in range(samples - 1)]
     for _ in range(new - 1):          # the first new token is sampled from the prompt
         for s in seqs:
-            s.reserve(1)
-    in_use = pool.num_blocks - pool.num_free
+            led.append(s, 1)
+    in_use = led.num_blocks - led.num_free
     assert in_use == int(g["blocks_in_use"][0][0])
-    assert samples * blocks_for(seqs[0].n, B) == int(g["blocks_unshared"][0][0])
-    assert len(pool.copies) == int(g["cow_copies"][0][0])
+    assert samples * blocks_for(led.length(seqs[0]), B) == int(g["blocks_unshared"][0][0])
+    copies = led.take_copies()
+    assert len(copies) == int(g["cow_copies"][0][0])
     for row in g["table"]:
-        assert seqs[int(row[0])].table == _ints(row[1:])
+        assert led.table(seqs[int(row[0])]) == _ints(row[1:])
     # the copies are of the shared partial prompt block into fresh blocks
-    assert all(src == 2 for src, _ in pool.copies)
+    assert all(src == 2 for src, _ in copies)
 
 
 def test_figure6_block_table_walkthrough():
     g = golden("figure6_walkthrough.txt")
     B = int(g["block_size"][0][0])
-    pool = BlockPool(8, block_size=B, free_order=_ints(g["free_order"][0]))
-    seq = Sequence(pool)
+    led = BlockLedger(8, block_size=B, free_order=_ints(g["free_order"][0]))
+    seq = led.new_sequence()
 
     def fills():
-        return [f"{b}:{n}" for b, n in seq.fills()]
+        return [f"{b}:{n}" for b, n in led.fills(seq)]
 
-    seq.reserve(7)
+    led.append(seq, 7)
     assert fills() == g["after_prompt"][0]
-    seq.reserve(1)                                   # "fathers"
+    led.append(seq, 1)                               # "fathers"
     assert fills() == g["after_token8"][0]
-    slot = seq.reserve(1)[0]                         # "brought"
+    slot = led.append(seq, 1)[0]                     # "brought"
     assert fills() == g["after_token9"][0]
     assert slot == int(g["slot_token9"][0][0])
 
 
 def test_cow_trace_two_samples():
     g = golden("cow_trace.txt")
-    pool = BlockPool(16, block_size=int(g["block_size"][0][0]),
-                     free_order=_ints(g["free_order"][0]))
-    a1 = Sequence(pool)
-    a1.reserve(int(g["prompt"][0][0]))
-    a2 = a1.fork()
-    a1.reserve(1)
-    a2.reserve(1)
-    assert [tuple(p) for p in pool.copies] == [tuple(_ints(g["copies"][0]))]
-    assert a1.table == _ints(g["table_A1"][0])
-    assert a2.table == _ints(g["table_A2"][0])
+    led = BlockLedger(16, block_size=int(g["block_size"][0][0]),
+                      free_order=_ints(g["free_order"][0]))
+    a1 = led.new_sequence()
+    led.append(a1, int(g["prompt"][0][0]))
+    a2 = led.fork(a1)
+    led.append(a1, 1)
+    led.append(a2, 1)
+    assert [tuple(p) for p in led.take_copies()] == [tuple(_ints(g["copies"][0]))]
+    assert led.table(a1) == _ints(g["table_A1"][0])
+    assert led.table(a2) == _ints(g["table_A2"][0])
     for item in g["refs"][0]:
         b, r = item.split(":")
-        assert pool.refs[int(b)] == int(r)
+        assert led.refcount(int(b)) == int(r)
 
 
-def test_free_returns_blocks_and_out_of_blocks_raises():
-    pool = BlockPool(4)
-    s = Sequence(pool)
-    s.reserve(64)
+def test_free_returns_blocks_and_out_of_blocks_changes_nothing():
+    led = BlockLedger(4)
+    s = led.new_sequence()
+    led.append(s, 64)
+    t = led.new_sequence()
     with pytest.raises(OutOfBlocks):
-        Sequence(pool).reserve(1)
-    s.free()
-    assert pool.num_free == 4 and all(r == 0 for r in pool.refs)
+        led.append(t, 1)
+    assert led.table(t) == [] and led.length(t) == 0 and led.num_free == 0
+    led.release(s)
+    assert led.num_free == 4 and all(r == 0 for r in led.refcounts())
+
+
+def test_append_is_all_or_nothing():
+    """A shared partial last block plus spill blocks beyond the free count:
+    the append raises and leaves tables, counts and the copy list alone."""
+    led = BlockLedger(4, block_size=16)
+    a = led.new_sequence()
+    led.append(a, 40)                                # 3 blocks, the last partial
+    b = led.fork(a)
+    assert led.blocks_needed(b, 1) == 1              # copy of the shared partial block
+    assert led.blocks_needed(b, 40) == 3             # copy + two spill blocks
+    before = (led.table(a), led.table(b), led.num_free, led.refcounts())
+    with pytest.raises(OutOfBlocks):
+        led.append(b, 40)
+    assert (led.table(a), led.table(b), led.num_free, led.refcounts()) == before
+    assert led.take_copies() == []
+    assert led.append(b, 1) == [3 * 16 + 8]          # copy-on-write into block 3
+    assert led.table(b) == [0, 1, 3] and led.take_copies() == [(2, 3)]
 
 
 # ---------------------------------------------------------------------------
