@@ -27,6 +27,12 @@ all ranks' bytes / the slowest rank's time.
 
 --impl reference times the CPU oracle (plain C, fp64, all host cores) on a
 bounded sample of the same workload, same metric and unit.
+
+Besides the named workload, a default run adds a ``per_config`` object with
+the other decode workloads (grouped-query, long-context, shared-prefix beams,
+tiny), each timed the same way with its own roofline fraction, spread and CPU
+baseline; the chunked-prefill step with OPT-13B and grouped-query heads; and
+the paged-versus-contiguous time ratio at 16-token blocks.
 """
 from __future__ import annotations
 
@@ -120,7 +126,7 @@ def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_pa_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.startswith("pa_decode") or f == "pa_ptx.cuh":
+        if (f.startswith("pa_decode") and f != "pa_decode_noalloc.cu") or f == "pa_ptx.cuh":
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(f.encode())
                 h.update(fh.read())
@@ -337,9 +343,10 @@ def layout_sweep(args, wl, dev):
     base = res["contiguous"]["ms_per_call"]
     for v in res.values():
         v["time_vs_contiguous"] = round(v["ms_per_call"] / base, 4)
-    print(json.dumps({"layout_sweep": args.config, "workload": WORKLOADS.get(args.config),
-                      "steps": args.steps, "algorithmic_bytes": int(b_attn), "results": res}),
-          flush=True)
+    del q, kc, vc
+    torch.cuda.empty_cache()
+    return {"layout_sweep": args.config, "workload": WORKLOADS.get(args.config),
+            "steps": args.steps, "algorithmic_bytes": int(b_attn), "results": res}
 
 
 def block_size_sweep(args, wl, dev):
@@ -573,30 +580,375 @@ def prefill_bench(args, dev):
     except (OSError, KeyError, ValueError):
         peak = 1900.0
     tf = flops / (ms_attn * 1e-3) / 1e12
-    print(json.dumps({"prefill": args.config,
-                      "workload": f"chunked prefill: {batch_desc}, {H} query / {Hkv} KV "
-                                  f"heads, D={D}, {dtype}, block {B}, scattered blocks",
-                      "steps": n, "algorithmic_tflop": round(flops / 1e12, 4),
-                      "ms_attention": round(ms_attn, 4), "ms_step": round(ms_step, 4),
-                      "tflops": round(tf, 1), "peak_tflops": peak,
-                      "peak_kind": "measured dense bf16 matmul (burst)",
-                      "frac": round(tf / peak, 4)}), flush=True)
+    del kc, vc, q, key, val, out, ws
+    torch.cuda.empty_cache()
+    return {"prefill": args.config,
+            "workload": f"chunked prefill: {batch_desc}, {H} query / {Hkv} KV "
+                        f"heads, D={D}, {dtype}, block {B}, scattered blocks",
+            "steps": n, "algorithmic_tflop": round(flops / 1e12, 4),
+            "ms_attention": round(ms_attn, 4), "ms_step": round(ms_step, 4),
+            "tflops": round(tf, 1), "peak_tflops": peak,
+            "peak_kind": "measured dense bf16 matmul (burst)",
+            "frac": round(tf / peak, 4)}
+
+
+class DecodeStep:
+    """Device buffers and the step function of one decode workload: the
+    copy-on-write copies (if any), the cache write of each sequence's new
+    token, and decode attention over every context."""
+
+    def __init__(self, pa, synthetic, wl, dev, vals=None):
+        import torch
+        self.pa, self.wl, self.dev = pa, wl, dev
+        self.vals = vals if vals is not None else synthetic.make_values(wl, device=dev)
+        S, H, Hkv, D = wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim
+        self.tables = torch.as_tensor(wl.block_tables, device=dev)
+        self.lens = torch.as_tensor(wl.context_lens, device=dev)
+        self.slots = torch.as_tensor(wl.slot_mapping, device=dev)
+        self.pairs = torch.as_tensor(wl.copy_pairs, device=dev) if len(wl.copy_pairs) else None
+        self.out = torch.empty(S, H, D, dtype=torch.float32, device=dev)
+        self.ws = torch.empty(pa.decode_workspace_size(S, H, Hkv, D, wl.max_context_len),
+                              dtype=torch.uint8, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        merge = wl.max_context_len > pa.decode_partition_tokens(S, Hkv, wl.max_context_len)
+        # our kernels per step: [copy] + cache write + plan + attention + [merge]
+        self.launches = (self.pairs is not None) + 1 + 2 + int(merge)
+
+    def __call__(self, ev_a=None, ev_b=None):
+        pa, v = self.pa, self.vals
+        if self.pairs is not None:
+            pa.copy_blocks([v["k_cache"]], [v["v_cache"]], self.pairs, error_word=self.err)
+        pa.cache_write(v["key"], v["value"], v["k_cache"], v["v_cache"], self.slots,
+                       error_word=self.err)
+        if ev_a is not None:
+            ev_a.record()
+        pa.decode_attention(v["q"], v["k_cache"], v["v_cache"], self.tables, self.lens,
+                            self.wl.max_context_len, self.wl.scale, out=self.out,
+                            workspace=self.ws, error_word=self.err)
+        if ev_b is not None:
+            ev_b.record()
+
+
+def _pct(xs):
+    a = np.asarray(xs, np.float64)
+    return {"p10": round(float(np.percentile(a, 10)), 4),
+            "p50": round(float(np.percentile(a, 50)), 4),
+            "p90": round(float(np.percentile(a, 90)), 4)}
+
+
+def l2_size(dev):
+    import torch
+    return int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (126 << 20)
+
+
+def time_decode(step, K, warmup, dev, dist=None, no_graph=False, sampler=None, windows=10):
+    """Time K steps of ``step`` (a DecodeStep).
+
+    K/V far above L2: the K steps run back to back between two events (a
+    CUDA graph of up to 50 steps or eager launches, whichever a short sample
+    finds faster); ``windows`` more K-step windows give the spread.  K/V
+    within four L2 sizes: every step is timed alone between its own events
+    after an L2 flush (a read of twice the L2), and the spread is over those
+    K steps; the same steps back to back are the hot-L2 figure.  Also the
+    attention call alone, eager, an event pair around each call."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(warmup):
+        step()
+    barrier()
+    assert int(step.err.item()) == 0, f"device error word {int(step.err.item())}"
+
+    g_steps = max(d for d in range(1, min(K, 50) + 1) if K % d == 0)
+    timed_graph, timed_launch = None, "eager"
+    if not no_graph:
+        try:
+            g_ = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_):
+                for _ in range(g_steps):
+                    step()
+            g_.replay()
+            torch.cuda.synchronize(dev)
+            timed_graph, timed_launch = g_, f"CUDA graph of {g_steps} steps"
+        except Exception as exc:  # capture not possible here: eager launches
+            timed_graph = None
+            timed_launch = f"eager (graph capture failed: {type(exc).__name__})"
+            torch.cuda.synchronize(dev)
+    if timed_graph is not None:
+        # keep whichever launch method runs this step faster: graph replay
+        # saves the host's launch overhead, eager launches keep every
+        # programmatic overlap between the kernels
+        def sample(fn, n):
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier()
+            a_.record(stream)
+            for _ in range(n):
+                fn()
+            b_.record(stream)
+            barrier()
+            return a_.elapsed_time(b_) / n
+        reps = max(1, 200 // g_steps)
+        t_graph = reduce_max(sample(timed_graph.replay, reps) / g_steps, dist, dev)
+        t_eager = reduce_max(sample(step, reps * g_steps), dist, dev)
+        if t_eager <= t_graph:
+            timed_graph = None
+            timed_launch = f"eager (faster than a CUDA graph of {g_steps} steps here)"
+        else:
+            timed_launch += " (faster than eager launches here)"
+
+    # K steps back to back, events only at the two ends (an event between two
+    # kernels would cut their programmatic overlap)
+    def back_to_back():
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        barrier()
+        t_start.record(stream)
+        if timed_graph is not None:
+            for _ in range(K // g_steps):
+                timed_graph.replay()
+        else:
+            for _ in range(K):
+                step()
+        t_end.record(stream)
+        barrier()
+        return reduce_max(t_start.elapsed_time(t_end), dist, dev)
+
+    l2_bytes = l2_size(dev)
+    near_l2 = step.wl.kv_bytes() < 4 * l2_bytes
+    if near_l2:
+        flush_buf = torch.ones(l2_bytes, dtype=torch.float16, device=dev)  # 2 x L2 bytes
+        one_step = None
+        try:
+            one_step = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(one_step):
+                step()
+            one_step.replay()
+            torch.cuda.synchronize(dev)
+        except Exception:  # capture not possible here: eager launches
+            one_step = None
+            torch.cuda.synchronize(dev)
+        run_one = one_step.replay if one_step is not None else step
+        for _ in range(3):
+            flush_buf.sum()
+            run_one()
+
+    if sampler:
+        sampler.start()
+    barrier()
+    wall0 = time.time()
+    per_step = None
+    if near_l2:
+        ca = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        cb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        for i in range(K):
+            flush_buf.sum()
+            ca[i].record(stream)
+            run_one()
+            cb[i].record(stream)
+        barrier()
+        per_step = [a.elapsed_time(b) for a, b in zip(ca, cb)]
+        total_ms = reduce_max(sum(per_step), dist, dev)
+        timed_launch = ("each step timed alone after an L2 flush, " +
+                        ("a CUDA graph of one step" if one_step is not None else "eager launches"))
+    else:
+        total_ms = back_to_back()
+    wall1 = time.time()
+    clocks = sampler.stop(wall0, wall1) if sampler else None
+    if near_l2:
+        spread = dict(_pct(per_step), over=f"the {K} timed steps (ms per step)")
+        hot_ms = back_to_back()
+        hot = {"ms_per_step": round(hot_ms / K, 4), "launch": "back to back, " + (
+            f"CUDA graph of {g_steps} steps" if timed_graph is not None else "eager")}
+        del flush_buf
+    else:
+        wins = [total_ms / K] + [back_to_back() / K for _ in range(windows)]
+        spread = dict(_pct(wins), over=f"{len(wins)} windows of {K} steps back to back "
+                                       f"(ms per step; the first is the timed region)")
+        hot = None
+    # the attention call timed alone: K more eager steps with an event pair
+    # around every call (each call then also waits for the host to submit its
+    # launches)
+    evs_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    evs_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        step(evs_a[i], evs_b[i])
+    barrier()
+    attn_ms = sum(a.elapsed_time(b) for a, b in zip(evs_a, evs_b)) / K
+    assert int(step.err.item()) == 0, f"device error word {int(step.err.item())}"
+    return {"ms_per_step": total_ms / K, "launch": timed_launch, "near_l2": near_l2,
+            "l2_bytes": l2_bytes, "hot": hot, "spread": spread, "attn_ms": attn_ms,
+            "clocks": clocks, "graph": timed_graph, "g_steps": g_steps}
+
+
+def cpu_baseline(wl, vals, dev, core_seconds=10.0, max_bytes=0.6e9, max_reps=50):
+    """The oracle (plain C, fp64, all host cores) on the same device inputs:
+    all of the batch's sequences if their K/V fit ``max_bytes``, else a
+    seeded subset that does; passes repeat until ~``core_seconds`` of CPU
+    work."""
+    import torch
+    import oracle
+    oracle.build()
+    S = wl.num_seqs
+    per = wl.context_lens.astype(np.int64) * wl.num_kv_heads * wl.head_dim * 4
+    order = np.random.default_rng(0).permutation(S)
+    keep = order[np.cumsum(per[order]) <= max_bytes]
+    seqs = np.sort(keep if len(keep) else order[:1])
+    q_h = vals["q"].view(torch.int16).cpu().numpy().view(np.uint16)
+
+    def host_vals(sq, used):
+        idx = torch.as_tensor(np.asarray(used, np.int64), device=dev)
+        kc, vc = (vals[n].index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
+                  for n in ("k_cache", "v_cache"))
+        return q_h[sq], kc, vc
+    inputs = oracle_inputs(wl, seqs, host_vals=host_vals)
+    threads = oracle.default_threads()
+    t_cpu = b_cpu = 0.0
+    reps = 0
+    while reps < 1 or (t_cpu * threads < core_seconds and reps < max_reps):
+        t_cpu += oracle_time(wl, inputs, threads)
+        b_cpu += inputs[5]
+        reps += 1
+    what = (f"all {S} sequences of the batch" if len(seqs) == S else
+            f"{len(seqs)} of the batch's {S} sequences (seeded choice)")
+    return {"value": round(b_cpu / t_cpu / 1e9, 4), "unit": UNIT, "cores": threads,
+            "kind": "oracle", "seconds": round(t_cpu, 2),
+            "sample": f"{what}, attention only, {reps} pass(es)"}
+
+
+def step_numbers(wl, t, peak, world=1):
+    """Throughput figures of one timed workload."""
+    b_attn, b_write, b_copy = algorithmic_bytes(wl)
+    b_attn_logical = algorithmic_bytes(wl, shared_once=False)[0]
+    b_step = b_attn + b_write + b_copy
+    ms = t["ms_per_step"]
+    value = world * b_step / (ms * 1e-3) / 1e9
+    attn_gbs = b_attn / (ms * 1e-3) / 1e9
+    d = {"b_attn": b_attn, "b_write": b_write, "b_copy": b_copy, "b_step": b_step,
+         "value": value, "attn_gbs": attn_gbs, "frac": attn_gbs / peak,
+         "attn_gbs_isolated": b_attn / (t["attn_ms"] * 1e-3) / 1e9,
+         "logical": ({"attention_bytes": int(b_attn_logical),
+                      "GBps": round(world * (b_attn_logical + b_write + b_copy) /
+                                    (ms * 1e-3) / 1e9, 2)}
+                     if b_attn_logical != b_attn else None)}
+    return d
+
+
+def l2_note(t):
+    if not t["near_l2"]:
+        return "inputs larger than L2 (K/V read per step >> 126 MB L2)"
+    return (f"K/V per step within a few L2 sizes: an L2 flush (a read of "
+            f"{2 * t['l2_bytes'] >> 20} MiB) before every timed step; hot_l2 = the same "
+            f"steps back to back")
+
+
+def cow_copy_timing(pa, wl, dev, layer_counts=(1, 40), reps=20):
+    """The workload's copy-on-write pairs as one pa_copy_blocks launch over 1
+    and over 40 layers.  Each layer gets its own pool holding just the
+    blocks the pairs name (relabelled), so 40 layers fit in memory; every
+    timed call follows an L2 flush."""
+    import torch
+    pairs = np.asarray(wl.copy_pairs, np.int64)
+    if not len(pairs):
+        return None
+    ids = np.unique(pairs)
+    rel = np.searchsorted(ids, pairs)
+    Hkv, D, B = wl.num_kv_heads, wl.head_dim, wl.block_size
+    dt = torch.float16 if wl.dtype == "f16" else torch.bfloat16
+    L = max(layer_counts)
+    g = torch.Generator(device=dev).manual_seed(wl.seed)
+    kc = [torch.randn(len(ids), Hkv, B, D, generator=g, device=dev).to(dt) for _ in range(L)]
+    vc = [torch.randn(len(ids), Hkv, B, D, generator=g, device=dev).to(dt) for _ in range(L)]
+    p_d = torch.as_tensor(rel, device=dev)
+    flush = torch.ones(l2_size(dev), dtype=torch.float16, device=dev)
+    res = {"pairs": int(len(pairs))}
+    for n in layer_counts:
+        for _ in range(3):
+            pa.copy_blocks(kc[:n], vc[:n], p_d)
+        torch.cuda.synchronize(dev)
+        a = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+        b = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+        for i in range(reps):
+            flush.sum()
+            a[i].record()
+            pa.copy_blocks(kc[:n], vc[:n], p_d)
+            b[i].record()
+        torch.cuda.synchronize(dev)
+        ms = sum(x.elapsed_time(y) for x, y in zip(a, b)) / reps
+        nbytes = 2 * len(pairs) * n * Hkv * B * D * 2 * 2      # read + write, K and V
+        res[f"layers_{n}"] = {"ms": round(ms, 4), "bytes": int(nbytes),
+                              "GBps": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+    del kc, vc, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_config(name, args, pa, synthetic, dev, peak, rank=0, cpu=True):
+    """One workload's entry of the bench line's per_config object."""
+    import torch
+    wl = synthetic.make(name, seed=synthetic.SEEDS[name] + 100 * rank)
+    step = DecodeStep(pa, synthetic, wl, dev)
+    t = time_decode(step, args.steps, args.warmup, dev, no_graph=args.no_graph)
+    n = step_numbers(wl, t, peak)
+    entry = {
+        "workload": WORKLOADS[name], "ms_per_step": round(t["ms_per_step"], 4),
+        "value": round(n["value"], 2), "unit": UNIT,
+        "seqs_per_s_per_layer": round(wl.num_seqs / (t["ms_per_step"] * 1e-3), 1),
+        "launch": t["launch"], "l2": l2_note(t), "spread": t["spread"], "hot_l2": t["hot"],
+        "roofline": {"bound": "hbm", "achieved": round(n["attn_gbs"], 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(n["frac"], 4),
+                     "traffic": recorded_traffic(name),
+                     "algorithmic_bytes": int(n["b_attn"]),
+                     "isolated_call": {"ms_per_call": round(t["attn_ms"], 4),
+                                       "achieved": round(n["attn_gbs_isolated"], 2)}},
+        "logical": n["logical"],
+        "pct_of_spec_8000": round(100 * n["attn_gbs"] / 8000.0, 2),
+    }
+    if t["hot"] is not None:
+        entry["hot_l2"]["value"] = round(n["b_step"] / (t["hot"]["ms_per_step"] * 1e-3) / 1e9, 2)
+        entry["hot_l2"]["frac"] = round(n["b_attn"] / (t["hot"]["ms_per_step"] * 1e-3) / 1e9
+                                        / peak, 4)
+    if name == "beams":
+        entry["cow_copy"] = cow_copy_timing(pa, wl, dev)
+    if name == "tiny":
+        # the same chain of kernels on one sequence of one token: the floor
+        # a launch-bound step is measured against
+        rng = np.random.default_rng(7)
+        fw = synthetic._from_lengths("floor", [1], 8, 8, 64, "f16", 7, rng)
+        fstep = DecodeStep(pa, synthetic, fw, dev)
+        ft = time_decode(fstep, args.steps, args.warmup, dev, no_graph=args.no_graph)
+        entry["floor"] = {"ms_per_step": round(ft["ms_per_step"], 4),
+                          "hot_ms_per_step": ft["hot"]["ms_per_step"] if ft["hot"] else None,
+                          "what": "one sequence of one token (8 heads, D=64): the same "
+                                  "kernel chain with almost no work, timed the same way"}
+        del fstep
+    if cpu:
+        entry["cpu_baseline"] = cpu_baseline(wl, step.vals, dev, core_seconds=6.0)
+    del step, t
+    torch.cuda.empty_cache()
+    return entry
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="opt13b")
     ap.add_argument("--seqs", type=int, default=0,
                     help="batch size override (smaller cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-graph", action="store_true",
-                    help="e2e leg: launch the steps eagerly instead of replaying a CUDA graph")
+                    help="launch the steps eagerly instead of replaying a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the named workload (no per_config object)")
     ap.add_argument("--layout-sweep", action="store_true",
                     help="time the attention call with blocks scattered, blocks in order, and "
                          "on a contiguous (unpaged) cache; prints its own JSON line")
@@ -644,7 +996,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     if args.layout_sweep:
-        layout_sweep(args, wl, dev)
+        print(json.dumps(layout_sweep(args, wl, dev)), flush=True)
         return
     if args.block_size_sweep:
         block_size_sweep(args, wl, dev)
@@ -653,176 +1005,30 @@ def main():
         swap_sweep(args, dev)
         return
     if args.prefill:
-        prefill_bench(args, dev)
+        print(json.dumps(prefill_bench(args, dev)), flush=True)
         return
 
-    vals = synthetic.make_values(wl, device=dev)
+    peak, peak_kind = peaks()
+    step = DecodeStep(pa, synthetic, wl, dev)
+    vals = step.vals
     S, H, Hkv, D = wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim
-    tables = torch.as_tensor(wl.block_tables, device=dev)
-    lens = torch.as_tensor(wl.context_lens, device=dev)
-    slots = torch.as_tensor(wl.slot_mapping, device=dev)
-    pairs = torch.as_tensor(wl.copy_pairs, device=dev) if len(wl.copy_pairs) else None
-    out = torch.empty(S, H, D, dtype=torch.float32, device=dev)
-    ws = torch.empty(pa.decode_workspace_size(S, H, Hkv, D, wl.max_context_len),
-                     dtype=torch.uint8, device=dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    K = args.steps
+    sampler = ClockSampler(local_rank) if rank == 0 or world > 1 else None
+    t = time_decode(step, K, args.warmup, dev, dist=dist, no_graph=args.no_graph,
+                    sampler=sampler)
+    ms_per_step = t["ms_per_step"]
+    n = step_numbers(wl, t, peak, world)
+    b_attn, b_write, b_copy, b_step = n["b_attn"], n["b_write"], n["b_copy"], n["b_step"]
+    value = n["value"]
+    hot = t["hot"]
+    if hot is not None:
+        hot["value"] = round(world * b_step / (hot["ms_per_step"] * 1e-3) / 1e9, 2)
     stream = torch.cuda.current_stream(dev)
-    merge = wl.max_context_len > pa.decode_partition_tokens(S, Hkv, wl.max_context_len)
-    # our kernels per step: [copy] + cache write + plan + attention + [merge]
-    launches_per_step = (pairs is not None) + 1 + 2 + int(merge)
-
-    def step(ev_a=None, ev_b=None):
-        if pairs is not None:
-            pa.copy_blocks([vals["k_cache"]], [vals["v_cache"]], pairs, error_word=err)
-        pa.cache_write(vals["key"], vals["value"], vals["k_cache"], vals["v_cache"], slots,
-                       error_word=err)
-        if ev_a is not None:
-            ev_a.record(stream)
-        pa.decode_attention(vals["q"], vals["k_cache"], vals["v_cache"], tables, lens,
-                            wl.max_context_len, wl.scale, out=out, workspace=ws, error_word=err)
-        if ev_b is not None:
-            ev_b.record(stream)
 
     def barrier():
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize(dev)
-
-    for _ in range(args.warmup):
-        step()
-    barrier()
-    assert int(err.item()) == 0, f"device error word {int(err.item())}"
-
-    K = args.steps
-    g_steps = max(d for d in range(1, min(K, 50) + 1) if K % d == 0)
-    timed_graph, timed_launch = None, "eager"
-    if not args.no_graph:
-        try:
-            g_ = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_):
-                for _ in range(g_steps):
-                    step()
-            g_.replay()
-            torch.cuda.synchronize(dev)
-            timed_graph, timed_launch = g_, f"CUDA graph of {g_steps} steps"
-        except Exception as exc:  # capture not possible here: eager launches
-            timed_graph = None
-            timed_launch = f"eager (graph capture failed: {type(exc).__name__})"
-            torch.cuda.synchronize(dev)
-    if timed_graph is not None:
-        # keep whichever launch method runs this step faster: graph replay
-        # saves the host's launch overhead, eager launches keep every
-        # programmatic overlap between the kernels
-        def sample(fn, n):
-            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            barrier()
-            a_.record(stream)
-            for _ in range(n):
-                fn()
-            b_.record(stream)
-            barrier()
-            return a_.elapsed_time(b_) / n
-        reps = max(1, 200 // g_steps)
-        t_graph = sample(timed_graph.replay, reps) / g_steps
-        t_eager = sample(step, reps * g_steps)
-        t_graph = reduce_max(t_graph, dist, dev)
-        t_eager = reduce_max(t_eager, dist, dev)
-        if t_eager <= t_graph:
-            timed_graph = None
-            timed_launch = f"eager (faster than a CUDA graph of {g_steps} steps here)"
-        else:
-            timed_launch += " (faster than eager launches here)"
-    # K steps back to back, events only at the two ends (an event between two
-    # kernels would cut their programmatic overlap); the steps replay a CUDA
-    # graph of g captured steps (g divides K), so short steps are not bound by
-    # the host's launch overhead
-    def back_to_back():
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        barrier()
-        t_start.record(stream)
-        if timed_graph is not None:
-            for _ in range(K // g_steps):
-                timed_graph.replay()
-        else:
-            for i in range(K):
-                step()
-        t_end.record(stream)
-        barrier()
-        return reduce_max(t_start.elapsed_time(t_end), dist, dev)
-
-    # K/V within a few L2 sizes: the timed steps are separated by an L2
-    # flush (a read of twice the L2, so no dirty lines are left to write
-    # back), each step timed alone between events; back to back is reported
-    # as the hot-L2 figure
-    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (126 << 20)
-    near_l2 = wl.kv_bytes() < 4 * l2_bytes
-    if near_l2:
-        flush_buf = torch.ones(l2_bytes, dtype=torch.float16, device=dev)  # 2 x L2 bytes
-        one_step = None
-        try:
-            one_step = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(one_step):
-                step()
-            one_step.replay()
-            torch.cuda.synchronize(dev)
-        except Exception:  # capture not possible here: eager launches
-            one_step = None
-            torch.cuda.synchronize(dev)
-        run_one = one_step.replay if one_step is not None else step
-        for _ in range(3):
-            flush_buf.sum()
-            run_one()
-
-    sampler = ClockSampler(local_rank) if rank == 0 or world > 1 else None
-    if sampler:
-        sampler.start()
-    barrier()
-    wall0 = time.time()
-    if near_l2:
-        ca = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-        cb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-        for i in range(K):
-            flush_buf.sum()
-            ca[i].record(stream)
-            run_one()
-            cb[i].record(stream)
-        barrier()
-        total_ms = reduce_max(sum(a.elapsed_time(b) for a, b in zip(ca, cb)), dist, dev)
-        timed_launch = ("each step timed alone after an L2 flush, " +
-                        ("a CUDA graph of one step" if one_step is not None else "eager launches"))
-    else:
-        total_ms = back_to_back()
-    wall1 = time.time()
-    clocks = sampler.stop(wall0, wall1) if sampler else None
-    hot = None
-    if near_l2:
-        hot_ms = back_to_back()
-        hot = {"ms_per_step": round(hot_ms / K, 4), "launch": "back to back, " + (
-            f"CUDA graph of {g_steps} steps" if timed_graph is not None else "eager")}
-    # the attention call timed alone: K more eager steps with an event pair
-    # around every call, on the launching stream (each call then also waits
-    # for the host to submit its three launches; reported beside the roofline)
-    evs_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    evs_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for i in range(K):
-        step(evs_a[i], evs_b[i])
-    barrier()
-    attn_ms = sum(a.elapsed_time(b) for a, b in zip(evs_a, evs_b)) / K
-    ms_per_step = total_ms / K
-
-    b_attn, b_write, b_copy = algorithmic_bytes(wl)
-    b_attn_logical = algorithmic_bytes(wl, shared_once=False)[0]
-    b_step = b_attn + b_write + b_copy
-    value = world * b_step / (ms_per_step * 1e-3) / 1e9
-    if hot is not None:
-        hot["value"] = round(world * b_step / (hot["ms_per_step"] * 1e-3) / 1e9, 2)
-    # roofline: the attention call's algorithmic bytes over the timed region's
-    # step time, which also holds the cache write (and the copy-on-write copies
-    # where the workload has them), so the duration is an upper bound
-    attn_gbs = b_attn / (ms_per_step * 1e-3) / 1e9
-    attn_gbs_isolated = b_attn / (attn_ms * 1e-3) / 1e9
-    peak, peak_kind = peaks()
 
     # end to end through the Python API: every step's inputs go host -> device
     # in one copy from a pinned staging buffer and its output comes back to
@@ -831,17 +1037,19 @@ def main():
     # resident
     e2e = None
     if not args.no_e2e:
+        pairs = step.pairs
+        ws = step.ws
         host_parts = [vals["q"].cpu(), vals["key"].cpu(), vals["value"].cpu(),
                       torch.as_tensor(wl.slot_mapping), torch.as_tensor(wl.block_tables),
                       torch.as_tensor(wl.context_lens)]
         offs, total = [], 0
-        for t in host_parts:
+        for x in host_parts:
             offs.append(total)
-            total += (t.numel() * t.element_size() + 255) // 256 * 256
+            total += (x.numel() * x.element_size() + 255) // 256 * 256
         staging = torch.zeros(total, dtype=torch.uint8).pin_memory()
-        for t, o in zip(host_parts, offs):
-            nb = t.numel() * t.element_size()
-            staging[o:o + nb].copy_(t.contiguous().view(-1).view(torch.uint8))
+        for x, o in zip(host_parts, offs):
+            nb = x.numel() * x.element_size()
+            staging[o:o + nb].copy_(x.contiguous().view(-1).view(torch.uint8))
         h2d = int(total)
         d2h = S * H * D * 4
 
@@ -855,18 +1063,18 @@ def main():
         for _ in range(2):
             b_ = torch.empty(total, dtype=torch.uint8, device=dev)
             bufs.append(b_)
-            views.append([b_[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-                          for t, o in zip(host_parts, offs)])
+            views.append([b_[o:o + x.numel() * x.element_size()].view(x.dtype).view(x.shape)
+                          for x, o in zip(host_parts, offs)])
         ev = lambda: torch.cuda.Event()
         h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
 
-        def pipeline(n):
-            # n steps; step i's inputs and step i-1's output move on the copy
-            # stream while step i computes on `stream`
+        def pipeline(n_steps):
+            # step i's inputs and step i-1's output move on the copy stream
+            # while step i computes on `stream`
             cs = torch.cuda.current_stream(dev)
-            for i in range(n + 1):
+            for i in range(n_steps + 1):
                 b = i % 2
-                if i < n:
+                if i < n_steps:
                     with torch.cuda.stream(copy_stream):
                         if i >= 2:
                             copy_stream.wait_event(comp_done[b])   # step i-2 read bufs[b]
@@ -889,11 +1097,11 @@ def main():
                         hout[pb].copy_(outs[pb], non_blocking=True)
                         d2h_done[pb].record(copy_stream)
 
-        def e2e_steps(n, t_start=None, t_end=None):
+        def e2e_steps(n_steps, t_start=None, t_end=None):
             stream.synchronize()
             if t_start is not None:
                 t_start.record(copy_stream)
-            pipeline(n)
+            pipeline(n_steps)
             if t_end is not None:
                 t_end.record(copy_stream)
             copy_stream.synchronize()
@@ -953,36 +1161,40 @@ def main():
         e2e = {"value": round(world * b_step / (e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e_ms, 4), "steps": n_e2e, "launch": launch}
-        if near_l2:
+        if t["near_l2"]:
             e2e["l2"] = "steps back to back, no L2 flush (hot)"
+        del graph, bufs, views, outs
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        import oracle
-        oracle.build()
-        q_h = vals["q"].view(torch.int16).cpu().numpy().view(np.uint16)
-        cache = {}
+        cpu = cpu_baseline(wl, vals, dev, max_bytes=2.5e9)
+    launches = int(K * step.launches)
+    del step, vals
+    t.pop("graph", None)
+    torch.cuda.empty_cache()
 
-        def host_vals(seqs, used):
-            # copy only the blocks the sampled sequences read
-            key = (int(used[0]) if len(used) else -1, len(used))
-            if key not in cache:
-                idx = torch.as_tensor(np.asarray(used, np.int64), device=dev)
-                cache.clear()
-                cache[key] = tuple(vals[n].index_select(0, idx).view(torch.int16).cpu().numpy()
-                                   .view(np.uint16) for n in ("k_cache", "v_cache"))
-            kc, vc = cache[key]
-            return q_h[seqs], kc, vc
-        t_cpu = b_cpu = 0.0
-        reps, threads = 0, 1
-        while reps < 1 or (t_cpu * threads < 10.0 and reps < 50):   # ~10 s of CPU work
-            t, b, threads = cpu_oracle_run(wl, np.arange(S), host_vals=host_vals)
-            t_cpu += t
-            b_cpu += b
-            reps += 1
-        cpu = {"value": round(b_cpu / t_cpu / 1e9, 4), "unit": UNIT, "cores": threads,
-               "kind": "oracle", "seconds": round(t_cpu, 2),
-               "sample": f"all {S} sequences of the batch, attention only, {reps} pass(es)"}
+    # every other workload, the prefill step and the paged/contiguous ratio,
+    # measured the same way on this GPU (rank 0 only: one replica suffices)
+    per_config = None
+    if rank == 0 and not args.no_per_config and not args.seqs:
+        per_config = {}
+        for name in ("gqa", "long", "beams", "tiny"):
+            if name != args.config:
+                per_config[name] = measure_config(name, args, pa, synthetic, dev, peak,
+                                                  cpu=not args.no_cpu_baseline)
+        pf = {}
+        for heads in ("opt13b", "gqa"):
+            pargs = argparse.Namespace(**{**vars(args), "config": heads, "prefill_batch": "chunks",
+                                          "prefill_block_size": 16})
+            pf[heads] = prefill_bench(pargs, dev)
+        per_config["prefill"] = pf
+        largs = argparse.Namespace(**{**vars(args), "config": "opt13b"})
+        lay = layout_sweep(largs, synthetic.make("opt13b"), dev)
+        per_config["layout_b16_opt13b"] = {
+            "time_vs_contiguous": {k: v["time_vs_contiguous"] for k, v in lay["results"].items()},
+            "ms_per_call": {k: v["ms_per_call"] for k, v in lay["results"].items()},
+            "what": "the attention call alone, back to back, paged with 16-token blocks "
+                    "scattered or in order, against the same kernels on a contiguous cache"}
 
     if rank != 0:
         if dist is not None:
@@ -997,38 +1209,36 @@ def main():
                                (f" (cut to {S} sequences)" if args.seqs else ""),
                    "mean_context": round(float(wl.context_lens.mean()), 1),
                    "kv_bytes_per_step": int(wl.kv_bytes()),
-                   "l2": ("inputs larger than L2 (K/V read per step >> 126 MB L2)"
-                          if not near_l2 else
-                          f"K/V per step within a few L2 sizes: an L2 flush (a read of "
-                          f"{2 * l2_bytes >> 20} MiB) before every timed step; hot_l2 = "
-                          f"the same steps back to back"),
-                   "parallelism": f"replicas x{world}", "launch": timed_launch},
+                   "l2": l2_note(t),
+                   "parallelism": f"replicas x{world}", "launch": t["launch"]},
         "seqs_per_s_per_layer": round(world * S / (ms_per_step * 1e-3), 1),
         # blocks shared by several sequences (copy-on-write prefixes) are
         # counted once above; here once per sequence that reads them
-        "logical": ({"attention_bytes": int(b_attn_logical),
-                     "GBps": round(world * (b_attn_logical + b_write + b_copy) /
-                                   (ms_per_step * 1e-3) / 1e9, 2)}
-                    if b_attn_logical != b_attn else None),
+        "logical": n["logical"],
+        "spread": t["spread"],
         "pct_of_peak": {"measured_copy": round(100 * value / world / peak, 2),
                         "spec_8000": round(100 * value / world / 8000.0, 2)},
-        "roofline": {"bound": "hbm", "achieved": round(attn_gbs, 2), "peak": peak,
-                     "peak_kind": f"{peak_kind} HBM copy GB/s", "unit": "GB/s",
-                     "frac": round(attn_gbs / peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(n["attn_gbs"], 2), "peak": peak,
+                     "peak_kind": f"{peak_kind} HBM copy GB/s (reads + writes; a read-only "
+                                  f"stream such as decode can exceed it, so frac is against a "
+                                  f"lower bound of the read peak)",
+                     "unit": "GB/s", "frac": round(n["frac"], 4),
+                     "frac_of_spec_8000": round(n["attn_gbs"] / 8000.0, 4),
                      "traffic": recorded_traffic(args.config),
                      "kernel": "pa_decode_attention (plan + attention + merge kernels)",
                      "duration": "timed-region step time (cache write + attention call"
                                  + (" + copy-on-write copies" if b_copy else "") + ")",
                      "ms": round(ms_per_step, 4), "algorithmic_bytes": int(b_attn),
-                     "isolated_call": {"ms_per_call": round(attn_ms, 4),
-                                       "achieved": round(attn_gbs_isolated, 2),
+                     "isolated_call": {"ms_per_call": round(t["attn_ms"], 4),
+                                       "achieved": round(n["attn_gbs_isolated"], 2),
                                        "how": "eager, an event pair around each call" +
-                                              (", no L2 flush" if near_l2 else "")}},
+                                              (", no L2 flush" if t["near_l2"] else "")}},
         "hot_l2": hot,
-        "gpu_launches": int(K * launches_per_step),
-        "clocks": clocks,
+        "gpu_launches": launches,
+        "clocks": t["clocks"],
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:
