@@ -610,9 +610,10 @@ class DecodeStep:
         self.ws = torch.empty(pa.decode_workspace_size(S, H, Hkv, D, wl.max_context_len),
                               dtype=torch.uint8, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-        merge = wl.max_context_len > pa.decode_partition_tokens(S, Hkv, wl.max_context_len)
-        # our kernels per step: [copy] + cache write + plan + attention + [merge]
-        self.launches = (self.pairs is not None) + 1 + 2 + int(merge)
+        # our kernels per step: [copy] + cache write + the attention call's
+        # (plan, one or two attention kernels, [merge])
+        self.launches = (self.pairs is not None) + 1 + pa.decode_kernel_launches(
+            S, H, Hkv, D, wl.max_context_len)
 
     def __call__(self, ev_a=None, ev_b=None):
         pa, v = self.pa, self.vals
@@ -1225,7 +1226,7 @@ def main():
                      "unit": "GB/s", "frac": round(n["frac"], 4),
                      "frac_of_spec_8000": round(n["attn_gbs"] / 8000.0, 4),
                      "traffic": recorded_traffic(args.config),
-                     "kernel": "pa_decode_attention (plan + attention + merge kernels)",
+                     "kernel": "pa_decode_attention (plan, attention and merge kernels)",
                      "duration": "timed-region step time (cache write + attention call"
                                  + (" + copy-on-write copies" if b_copy else "") + ")",
                      "ms": round(ms_per_step, 4), "algorithmic_bytes": int(b_attn),

@@ -143,6 +143,17 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
 int pa_decode_partition_tokens(int num_seqs, int num_kv_heads, int max_context_len);
 
 /*
+ * pa_decode_kernel_launches -- how many kernels pa_decode_attention (and its
+ * _ex and _noalloc forms) enqueues for these sizes: the plan, one attention
+ * kernel or, when shared-prefix items may form with one query head per KV
+ * head, two (the tensor-core kernel for the shared prefixes, the CUDA-core
+ * kernel for the rest), and the merge when a sequence may have more than one
+ * partition.  0 for invalid sizes.  Host only, no CUDA calls.
+ */
+int pa_decode_kernel_launches(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                              int max_context_len);
+
+/*
  * pa_decode_attention -- one decode step of attention over a paged KV cache.
  *
  * Defines: for sequence s and query head h, with KV head hk = h / G,
@@ -167,12 +178,13 @@ int pa_decode_partition_tokens(int num_seqs, int num_kv_heads, int max_context_l
  * k_cache, v_cache  device pools, layout above
  * block_tables  device int32 [num_seqs][max_blocks_per_seq]; entries past a
  *               sequence's ceil(L/16) blocks are never read
- * context_lens  device int32 [num_seqs], each in [0, max_context_len]; read
- *               as soon as the call's first kernel starts, which may be
- *               before the kernel enqueued ahead of it has finished (the
- *               call's kernels use programmatic dependent launch), so it
- *               must not be written by a kernel that lets dependents launch
- *               before writing it (ordinary kernels and copies are fine)
+ * context_lens  device int32 [num_seqs], each in [0, max_context_len]
+ *               context_lens and block_tables are read as soon as the
+ *               call's first kernel starts, which may be before the kernel
+ *               enqueued ahead of it has finished (the call's kernels use
+ *               programmatic dependent launch), so they must not be written
+ *               by a kernel that lets dependents launch before writing them
+ *               (ordinary kernels and copies are fine)
  * max_context_len  host-known upper bound on context_lens,
  *               <= 16 * max_blocks_per_seq
  * num_heads % num_kv_heads == 0, num_heads / num_kv_heads <= 8,
@@ -184,9 +196,21 @@ int pa_decode_partition_tokens(int num_seqs, int num_kv_heads, int max_context_l
  * dev_error_word  device, may be NULL: PA_ERRBIT_BLOCK_OOB (the block is
  *               skipped), PA_ERRBIT_CONTEXT_LEN (the sequence gets a zero
  *               row), PA_ERRBIT_TIMEOUT
- * Enqueues two or three kernels, chained with programmatic dependent launch:
- * a plan kernel (the work list), the attention kernel, and a merge kernel
- * when a sequence may span more than one context partition.
+ * Shared prefixes: when consecutive sequences' tables start with the same
+ * block ids (beam search, parallel sampling, a common prompt), the blocks
+ * that are full in all of them are read once for the run, with every
+ * member's query, and merged with each member's own remainder; the result
+ * is each sequence's own attention either way.  Detection looks only at the
+ * ids, for head_dim <= 128, num_heads / num_kv_heads <= 4,
+ * 2 <= num_seqs <= 4096 and max_context_len >= 256.
+ * [Efficient Memory Management ..., "Shared prefix" and "Beam search": one
+ * physical copy of shared blocks serves every sequence that maps them]
+ *
+ * Enqueues, chained with programmatic dependent launch: a plan kernel (the
+ * work lists), one attention kernel (or two: shared prefixes on the
+ * tensor-core kernel and the rest on the CUDA-core kernel when
+ * num_heads == num_kv_heads), and a merge kernel when a sequence may have
+ * more than one partition; pa_decode_kernel_launches gives the count.
  */
 pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, const void *query,
                                 const void *k_cache, const void *v_cache,

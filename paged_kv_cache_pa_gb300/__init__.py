@@ -29,7 +29,8 @@ import threading
 from typing import Optional, Sequence
 
 __all__ = ["cache_write", "decode_attention", "decode_attention_contiguous",
-           "decode_workspace_size", "decode_partition_tokens", "copy_blocks",
+           "decode_workspace_size", "decode_partition_tokens", "decode_kernel_launches",
+           "copy_blocks",
            "status_string", "PaError", "library_path", "load_library", "BLOCK_SIZE",
            "ERRBIT_BLOCK_OOB", "ERRBIT_SLOT_OOB", "ERRBIT_CONTEXT_LEN", "ERRBIT_TIMEOUT",
            "MAX_LAYERS", "BLOCK_SIZES", "swap_blocks", "prefill_attention"]
@@ -52,6 +53,7 @@ _SIGNATURES = {
     "pa_cache_write_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pa_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
     "pa_decode_partition_tokens": (_I, [_I, _I, _I]),
+    "pa_decode_kernel_launches": (_I, [_I, _I, _I, _I, _I]),
     "pa_decode_attention": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I,
                                  ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P]),
     "pa_decode_attention_ex": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I,
@@ -162,6 +164,13 @@ def decode_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head
                           max_context_len: int) -> int:
     return int(load_library().pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads,
                                                        head_dim, max_context_len))
+
+
+def decode_kernel_launches(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                           max_context_len: int) -> int:
+    """Kernels one decode_attention call enqueues for these sizes."""
+    return int(load_library().pa_decode_kernel_launches(num_seqs, num_heads, num_kv_heads,
+                                                        head_dim, max_context_len))
 
 
 def decode_partition_tokens(num_seqs: int, num_kv_heads: int, max_context_len: int) -> int:

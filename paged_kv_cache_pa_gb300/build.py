@@ -6,6 +6,11 @@ Every .cu file under csrc/ is compiled with nvcc and every .cpp file (host
 code) with g++, in parallel, to _build/*.o, then linked into
 paged_kv_cache_pa_gb300/libpa_gb300.so (CUDA runtime linked statically).
 A stamp of the sources and flags skips the build when nothing changed.
+
+build(variant="shortwait") makes a test copy, libpa_gb300_shortwait.so (objects
+in _build_shortwait/), whose kernels give up their ordinary waits after a few
+non-blocking polls; the tests use it to run the give-up path on the GPU.  The
+product library is libpa_gb300.so.
 """
 from __future__ import annotations
 
@@ -38,9 +43,17 @@ def _nvcc() -> str:
     return "nvcc"
 
 
-def _stamp(sources) -> str:
+# variant -> (object folder, library, extra nvcc flags)
+VARIANTS = {
+    None: (BUILD, LIB, []),
+    "shortwait": (os.path.join(ROOT, "_build_shortwait"),
+                  os.path.join(PKG, "libpa_gb300_shortwait.so"), ["-DPA_TEST_WAIT_POLLS=4"]),
+}
+
+
+def _stamp(sources, extra) -> str:
     h = hashlib.sha256()
-    h.update(" ".join(CFLAGS + CXXFLAGS).encode())
+    h.update(" ".join(CFLAGS + CXXFLAGS + extra).encode())
     for path in sorted(sources + glob.glob(os.path.join(CSRC, "*.cuh")) +
                        glob.glob(os.path.join(INCLUDE, "*.h"))):
         with open(path, "rb") as f:
@@ -49,22 +62,23 @@ def _stamp(sources) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, variant=None) -> str:
+    build_dir, lib, extra = VARIANTS[variant]
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
-    stamp = _stamp(sources)
-    stamp_file = LIB + ".stamp"
-    if (not force and os.path.exists(LIB) and os.path.exists(stamp_file)
+    stamp = _stamp(sources, extra)
+    stamp_file = lib + ".stamp"
+    if (not force and os.path.exists(lib) and os.path.exists(stamp_file)
             and open(stamp_file).read() == stamp):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         if src.endswith(".cpp"):
             cmd = [os.environ.get("CXX", "g++")] + CXXFLAGS + ["-c", src, "-o", obj]
         else:
-            cmd = [nvcc] + CFLAGS + ["-c", src, "-o", obj]
+            cmd = [nvcc] + CFLAGS + extra + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"compile failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -75,15 +89,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if verbose:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp_file, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

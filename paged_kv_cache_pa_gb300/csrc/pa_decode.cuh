@@ -11,10 +11,17 @@
 // softmax per query head sharing a KV head].
 //
 // How (one persistent CTA family per SM, warp-specialised):
-//   * A work item is (sequence, context partition of <= part_tokens tokens,
-//     KV head).  A plan kernel lists the (sequence, partition) pairs longest
-//     first; CTAs take their first three items in a fixed order and claim
-//     the rest with one atomic each, so the tail is short.
+//   * A work item is (piece of a sequence's context of <= part_tokens
+//     tokens, KV head).  A plan kernel cuts every sequence's context into
+//     pieces and lists them longest first; CTAs take their first three
+//     items in a fixed order and claim the rest with one atomic each, so the
+//     tail is short.  Each item names its sequence, its first token, its
+//     token count and the partial-result slot (partition) it fills.
+//   * Runs of consecutive sequences whose block tables start with the same
+//     full blocks share that prefix: the plan makes the shared prefix one
+//     item whose query rows are all the run's queries (the tensor-core
+//     kernel in pa_decode_mma.cuh takes those), and each sequence's own
+//     remainder a plain item.  This kernel takes plain items only.
 //   * Warp 0 (producer) resolves the item's block-table slice once (one
 //     coalesced load, one entry per 16-token chunk; two for 8-token blocks)
 //     and streams each chunk's K and V rows -- 16 rows x head_dim, only the
@@ -33,9 +40,9 @@
 //     its own running (max, sum, acc[8]) per query head over the rows it saw;
 //     states are merged (shuffles, then shared memory) when the item ends.
 //     Each K/V byte is read from HBM once and serves all G query heads.
-//   * Output: a one-partition item writes the normalised row (fp32 or the
-//     input type, round to nearest even); otherwise (max, sum, acc) go to the
-//     workspace and the merge kernel combines the partitions.
+//   * Output: the only item of a sequence writes the normalised row (fp32 or
+//     the input type, round to nearest even); otherwise (max, sum, acc) go to
+//     the workspace and the merge kernel combines the sequence's partitions.
 // Scores are kept in base-2 units (q is pre-scaled by scale * log2 e) so the
 // exponentials are single ex2 instructions.
 #pragma once
@@ -64,15 +71,50 @@ struct alignas(16) StageMeta {
     int j, nblk, nvalid, flags;
 };
 
+// The plan writes up to two work lists: list 0 for the launch that takes
+// shared-prefix items (or every item), list 1 for the CUDA-core kernel's
+// plain items when a call runs both kernels.
 struct WsHeader {
-    unsigned int counter;   // items claimed beyond the first three rounds
-    unsigned int n_items;   // (sequence, partition, kv head) items in the plan
+    unsigned int counter[2];  // items claimed beyond the first three rounds, per list
+    unsigned int n_items[2];  // (piece, KV head) items in each list
 };
+
+// One entry per piece of a context, shared by its KV heads (item c of a list
+// is entry c / num_kv_heads, KV head c % num_kv_heads):
+//   x  the sequence (a shared-prefix item: the first sequence of its run)
+//   y  the piece's first token, z its tokens (> 0)
+//   w  bits 0..14: the partition (partial-result slot) the piece fills;
+//      bits 16..30: the sequence's number of partitions, or for a
+//      shared-prefix item the number of sequences in its run; bit 31: set
+//      for a shared-prefix item
+constexpr unsigned kGroupBit = 0x80000000u;
+constexpr int kMaxParts = 0x7fff;
+__host__ __device__ __forceinline__ int item_part(int w) { return w & 0x7fff; }
+__host__ __device__ __forceinline__ int item_count(int w) { return (w >> 16) & 0x7fff; }
+__host__ __device__ __forceinline__ bool item_is_group(int w) {
+    return ((unsigned)w & kGroupBit) != 0u;
+}
+__host__ __device__ __forceinline__ int make_item_w(int part, int count, bool group) {
+    return (int)((unsigned)part | ((unsigned)count << 16) | (group ? kGroupBit : 0u));
+}
+
+// Query rows of a shared-prefix item: the tmap_qs box holds Gb heads (G
+// rounded up to a power of two, so every box has 8 rows) of 8 / Gb
+// sequences; row r is head r / (8 / Gb) of the KV head's group and sequence
+// r % (8 / Gb) of the run.  Rows of heads >= G belong to no item row.
+__host__ __device__ __forceinline__ int group_box_heads(int G) {
+    return G <= 1 ? 1 : (G <= 2 ? 2 : 4);
+}
+__host__ __device__ __forceinline__ int group_seqs_per_box(int G) {
+    return 8 / group_box_heads(G);
+}
 
 struct DecodeParams {
     // Tensor maps of the query and the pools (tensor-core kernel only):
     // 3-D views [head_dim/64][rows][64], whole-row boxes, 128-byte swizzle.
-    CUtensorMap tmap_q, tmap_k, tmap_v;
+    // tmap_qs views the query as [head_dim/64][heads][sequences][64] with a
+    // box of G heads x 8/G sequences: the query rows of a shared-prefix item.
+    CUtensorMap tmap_q, tmap_k, tmap_v, tmap_qs;
     void *out;
     int out_dtype;  // PA_F16, PA_BF16 or PA_F32
     const void *q;
@@ -89,8 +131,11 @@ struct DecodeParams {
     int num_seqs, num_heads, num_kv_heads, G, head_dim, num_blocks;
     float scale_log2;  // scale * log2(e)
     int part_tokens, max_parts;
+    int list;          // the work list this launch takes (0 or 1)
+    int grouping;      // 1: the plan may form shared-prefix items
     WsHeader *hdr;
-    int4 *items;  // (s, p, ntok, nparts) per (sequence, partition)
+    int4 *items;       // the list this launch takes (entries as above)
+    int *nparts;       // per sequence: its partitions (0: empty or invalid)
     float *part_m, *part_l, *part_acc;
     unsigned int *err;
 };
@@ -172,9 +217,9 @@ struct Tuning {
 struct ItemPipe {
     const DecodeParams *P;
     unsigned n_items, Hkv;
-    int PB, lane;
+    int lane;
     unsigned cX, cY, cZ, raw;  // item indices; raw: lane 0's pending claim
-    int4 eX, eY, eZ;           // entries (s, p, ntok, nparts)
+    int4 eX, eY, eZ;           // entries (s, first token, tokens, w)
     int2 tX, tY;               // block-table entries of this lane's chunk of X and Y
 
     __device__ __forceinline__ int4 entry(unsigned c) const {
@@ -189,7 +234,7 @@ struct ItemPipe {
         int2 r = make_int2(-1, -1);
         if (c < n_items && lane < nchunk) {
             const int32_t *row = P->block_tables + (size_t)e.x * P->max_blocks_per_seq;
-            const int i = (e.y * PB + lane) * kBlock >> P->block_shift;
+            const int i = (e.y + lane * kBlock) >> P->block_shift;
             r.x = __ldg(&row[i]);
             if (P->block_size < kBlock && e.z - lane * kBlock > P->block_size)
                 r.y = __ldg(&row[i + 1]);
@@ -197,13 +242,12 @@ struct ItemPipe {
         return r;
     }
     __device__ __forceinline__ unsigned claim() const {
-        return lane == 0 ? 3u * gridDim.x + atomicAdd(&P->hdr->counter, 1u) : 0u;
+        return lane == 0 ? 3u * gridDim.x + atomicAdd(&P->hdr->counter[P->list], 1u) : 0u;
     }
     __device__ __forceinline__ void init(const DecodeParams &params, unsigned n, int lane_) {
         P = &params;
         n_items = n;
         Hkv = (unsigned)params.num_kv_heads;
-        PB = params.part_tokens / kBlock;
         lane = lane_;
         cX = blockIdx.x;
         cY = blockIdx.x + gridDim.x;
@@ -236,7 +280,7 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
                                              StageMeta *meta, uint64_t *full, uint64_t *empty,
                                              volatile int *abort_flag, int lane) {
     pdl_wait();  // the plan kernel's items and counter are ready
-    const unsigned n_items = P.hdr->n_items;
+    const unsigned n_items = P.hdr->n_items[P.list];
     const unsigned Hkv = (unsigned)P.num_kv_heads;
     const int G = P.G;
     const uint64_t policy = l2_evict_first_policy();
@@ -259,7 +303,8 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
         const int4 eA = items.eX;
         const int2 tA = items.tX;
 
-        const int s = eA.x, part = eA.y, ntok = eA.z, nparts = eA.w;
+        const int s = eA.x, t_item = eA.y, ntok = eA.z;
+        const int part = item_part(eA.w), nparts = item_count(eA.w);
         const int hk = (int)(cA % Hkv);
         const int nblk = (ntok + kBlock - 1) / kBlock;
         // Lane j prepares chunk j's copies once per item (all chunks at once),
@@ -274,7 +319,7 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
         if (lane == 0 && badmask && P.err) atomicOr(P.err, PA_ERRBIT_BLOCK_OOB);
         size_t off0 = 0, off1 = 0;  // element offsets of the rows in either pool
         if (nv > 0 && !bad) {
-            const int t0 = part * P.part_tokens + lane * kBlock;  // the chunk's first token
+            const int t0 = t_item + lane * kBlock;  // the chunk's first token
             if (P.contig_rows) {
                 off0 = (((size_t)s * Hkv + hk) * P.contig_rows + (size_t)t0) * D;
             } else {
@@ -346,9 +391,8 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
         }
         // let the copies already issued land before the CTA can exit
         if (lane == 0) {
-            volatile int never = 0;
             const uint32_t first = k > (uint32_t)R ? k - R : 0u;
-            for (uint32_t kk = first; kk < k; ++kk) mbar_wait(&full[kk % R], (kk / R) & 1u, &never);
+            for (uint32_t kk = first; kk < k; ++kk) mbar_drain_wait(&full[kk % R], (kk / R) & 1u);
         }
         __syncwarp();
     }
@@ -607,13 +651,19 @@ __global__ void __launch_bounds__(kThreads, MINB) paged_decode_kernel(const __gr
 // (pa_decode_mma.cuh); single-head groups and head_dim 256 on the CUDA cores.
 inline bool uses_tensor_cores(int G, int head_dim) { return G >= 2 && head_dim <= 128; }
 
+// Which attention kernel a launch uses: the one the query group selects
+// (tensor cores for G = 2..8 at head_dim <= 128, else CUDA cores), or the
+// tensor-core kernel whatever G is (shared-prefix items of a G = 1 call).
+constexpr int kKernelByGroup = 0;
+constexpr int kKernelTensorCore = 1;
+
 // Host-side launcher for one head_dim (defined in pa_decode_d{64,128,256}.cu).
 pa_status_t launch_decode_d64(const DecodeParams &P, pa_dtype_t dtype, int grid_cap,
-                              cudaStream_t stream);
+                              cudaStream_t stream, int kernel);
 pa_status_t launch_decode_d128(const DecodeParams &P, pa_dtype_t dtype, int grid_cap,
-                               cudaStream_t stream);
+                               cudaStream_t stream, int kernel);
 pa_status_t launch_decode_d256(const DecodeParams &P, pa_dtype_t dtype, int grid_cap,
-                               cudaStream_t stream);
+                               cudaStream_t stream, int kernel);
 
 // Number of streaming multiprocessors of the current device (cached).
 int current_sm_count();

@@ -3,9 +3,10 @@
 // the host-side checks and launches.
 //
 // Context split: a sequence longer than part_tokens is cut into partitions of
-// part_tokens tokens; every (sequence, partition, KV head) is an independent
-// work item whose partial softmax state (max m, sum l, weighted values acc)
-// is merged exactly afterwards by the merge kernel:
+// part_tokens tokens, and a prefix that a run of sequences shares is a
+// partition of its own; every (piece, KV head) is an independent work item
+// whose partial softmax state (max m, sum l, weighted values acc) is merged
+// exactly afterwards by the merge kernel:
 //     M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  o = sum_p acc_p 2^(m_p - M) / L
 // [vLLM Internals ..., "The kernel pays for the indirection": a grid axis over
 // partitions; Paged Attention: Managing the KV Cache Like Virtual Memory,
@@ -28,6 +29,15 @@ namespace {
 
 constexpr int kMinPartTokens = 64;
 constexpr long long kTargetItems = 2048;  // ~ 152 SMs x resident CTAs x a few items each
+// Shared prefixes: runs of at most 8 / G consecutive sequences (G <= 4) whose
+// tables start with the same blocks, at least kMinSharedTokens of them full,
+// among at most kMaxGroupSeqs sequences (the plan keeps per-sequence state in
+// shared memory).
+constexpr int kMinSharedTokens = 64;
+constexpr int kMaxGroupSeqs = 4096;
+// Below this longest context the tokens a shared prefix could save do not
+// pay for the work of finding it (and, for G = 1, a second kernel).
+constexpr int kMinGroupContext = 256;
 
 int choose_part_tokens(int num_seqs, int num_kv_heads, int max_context_len) {
     int p = kMaxPartTokens;
@@ -40,21 +50,41 @@ int choose_part_tokens(int num_seqs, int num_kv_heads, int max_context_len) {
     return p;
 }
 
+// Sequences per shared-prefix run for these sizes (0: no shared-prefix
+// items): the tensor-core kernel's 8 query rows hold G heads (rounded up to
+// a power of two) of 8 / that many sequences.
+int group_seqs(int num_seqs, int G, int head_dim, int max_context_len) {
+    if (head_dim > 128 || G > 4 || num_seqs < 2 || num_seqs > kMaxGroupSeqs) return 0;
+    if (max_context_len < kMinGroupContext) return 0;
+    return group_seqs_per_box(G);
+}
+
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-    int part_tokens, max_parts;
-    size_t items_off, m_off, l_off, acc_off, bytes;
+    int part_tokens, max_parts, group_seqs;
+    long long list_cap;  // entries per list
+    size_t items0_off, items1_off, nparts_off, m_off, l_off, acc_off, bytes;
 };
 
 WsLayout ws_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                    int max_context_len) {
     WsLayout w;
     w.part_tokens = choose_part_tokens(num_seqs, num_kv_heads, max_context_len);
-    w.max_parts = max_context_len > 0 ? (max_context_len + w.part_tokens - 1) / w.part_tokens : 1;
+    w.group_seqs = group_seqs(num_seqs, num_heads / num_kv_heads, head_dim, max_context_len);
+    const int np = max_context_len > 0 ? (max_context_len + w.part_tokens - 1) / w.part_tokens : 1;
+    // a sequence in a run has the shared prefix's pieces and its own: at most
+    // one partition more than its length alone needs
+    w.max_parts = np + (w.group_seqs ? 1 : 0);
+    // own pieces: <= np per sequence; shared-prefix pieces: <= np per run
+    w.list_cap = (long long)num_seqs * np + (w.group_seqs ? (long long)(num_seqs / 2 + 1) * np : 0);
     size_t off = align256(sizeof(WsHeader));
-    w.items_off = off;
-    off = align256(off + (size_t)num_seqs * w.max_parts * sizeof(int4));
+    w.items0_off = off;
+    off = align256(off + (size_t)w.list_cap * sizeof(int4));
+    w.items1_off = off;
+    off = align256(off + (size_t)(w.group_seqs ? w.list_cap : 1) * sizeof(int4));
+    w.nparts_off = off;
+    off = align256(off + (size_t)num_seqs * sizeof(int));
     if (w.max_parts > 1) {
         const size_t n = (size_t)num_seqs * num_heads * w.max_parts;
         w.m_off = off;
@@ -70,115 +100,356 @@ WsLayout ws_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
     return w;
 }
 
-// One CTA: count (sequence, partition) pairs by size, lay them out longest
-// first (a counting sort on the number of blocks), reset the claim counter,
-// and zero the output rows of empty sequences.  Sequences are taken 1024 at
-// a time, one per thread; shared-memory counters are bumped once per warp
-// and size (warp-aggregated), so threads do not queue on one address.
+// ---------------------------------------------------------------------------
+// Plan kernel (one CTA of 1024 threads).
 //
-// The work list is built before the programmatic-dependent-launch wait, so
-// it overlaps the kernel before this call on the stream (typically the cache
-// write); only the output rows wait for it.  Reading context_lens that early
-// is safe because it is an input: a kernel that wrote it has completed before
-// this grid starts, unless that kernel let dependents launch before writing
-// it.  Writing the work list that early is safe because the attention
-// kernels of earlier calls that share the workspace have finished with it:
-// their producers read it, and release the claim counter with a fence,
-// before they allow dependents to launch.
+//  1. Shared prefixes (when enabled): for each sequence s >= 1, the number of
+//     leading blocks that are full in both s and s - 1 and hold the same
+//     block ids in both tables.  Equal ids at equal positions hold the same
+//     tokens, so those tokens' attention terms differ only in the query.
+//     Sequence s joins s - 1's run when they share >= kMinSharedTokens; runs
+//     are cut into groups of at most group_seqs sequences, and a group's
+//     shared length is the smallest of its consecutive pairs' (a multiple of
+//     16 tokens).
+//  2. Every sequence's context is cut into pieces: a group's shared prefix
+//     [0, T) once for the group (a shared-prefix item), and each sequence's
+//     own range [T, L) (T = 0 outside groups), each into part_tokens pieces
+//     and a shorter last piece.  A sequence's partitions are numbered prefix
+//     pieces first.
+//  3. The pieces are laid out longest first (a counting sort on their size
+//     in 16-token chunks): shared-prefix pieces in list 0, the others in
+//     list 0 or, when the call runs the CUDA-core kernel beside the
+//     tensor-core one, in list 1.
+//  4. After the programmatic-dependent-launch wait: the per-sequence counts
+//     of partitions, and zero output rows for empty sequences.
+//
+// Steps 1-3 run before the wait, so they overlap the kernel before this call
+// on the stream (the cache write of a decode step): context_lens and
+// block_tables are inputs, complete before the call (a kernel that wrote
+// them has finished, unless it let dependents launch before writing), and
+// the work lists are free -- the attention kernels of earlier calls that
+// share the workspace read them in their producers, which release the claim
+// counters with a fence before they allow dependents to launch.  The
+// partition counts are written after the wait because the epilogue and the
+// merge of an earlier call may still read them until that call completes.
+// ---------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;
+constexpr int kSeqPerThread = kMaxGroupSeqs / kPlanThreads;
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(
-    const int32_t *__restrict__ lens, int num_seqs, int max_context_len, int part_tokens,
-    int num_kv_heads, int num_heads, int head_dim, int4 *__restrict__ items, WsHeader *hdr,
-    void *out, int out_dtype, unsigned int *err) {
+struct PlanParams {
+    const int32_t *lens;
+    const int32_t *tables;
+    int max_blocks_per_seq, block_shift;
+    int num_seqs, max_context_len, part_tokens;
+    int num_kv_heads, num_heads, head_dim;
+    int group_seqs;  // 0: no shared-prefix items
+    int split;       // 1: plain pieces go to list 1
+    int4 *items0, *items1;
+    int *nparts;
+    WsHeader *hdr;
+    void *out;
+    int out_dtype;
+    unsigned int *err;
+};
+
+// Shared memory of the plan: the fixed part, then (shared prefixes only) the
+// per-sequence arrays, sized by the host for the call's num_seqs.
+struct PlanShared {
+    int hist[2][kMaxPartTokens / kBlock + 1];
+    int offs[2][kMaxPartTokens / kBlock + 1];
+    int red[32];
+    int *shared_tok;   // [num_seqs] tokens s shares with s - 1 (0: none)
+    int *pre;          // [num_seqs] scan scratch
+    short *run_start;  // [num_seqs] first sequence of s's run
+};
+constexpr size_t plan_smem_bytes(int num_seqs, bool grouping) {
+    return sizeof(PlanShared) + (grouping ? (size_t)num_seqs * (4 + 4 + 2) + 16 : 0);
+}
+
+__device__ __forceinline__ int valid_len(const PlanParams &A, int s) {
+    const int L = A.lens[s];
+    return (L < 0 || L > A.max_context_len) ? 0 : L;
+}
+
+// Block-wide exclusive sum of one value per thread (red: 32 ints of shared
+// memory); returns this thread's prefix.
+__device__ __forceinline__ int block_exclusive_sum(int v, int *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += u;
+    }
+    __syncthreads();  // red may still be read from an earlier use
+    if (lane == 31) red[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int x = red[lane];
+        int y = x;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, y, off);
+            if (lane >= off) y += u;
+        }
+        red[lane] = y - x;
+    }
+    __syncthreads();
+    return red[warp] + incl - v;
+}
+
+// Group of sequence s: (first sequence, sequences, shared tokens); n = 1 and
+// T = 0 outside a group.
+struct Group {
+    int first, n, T;
+};
+__device__ __forceinline__ Group group_of(const PlanParams &A, const PlanShared &sh, int s) {
+    Group g = {s, 1, 0};
+    if (!A.group_seqs) return g;
+    const int rs = sh.run_start[s];
+    const int first = rs + (s - rs) / A.group_seqs * A.group_seqs;
+    int n = 1, T = INT_MAX;
+    while (n < A.group_seqs && first + n < A.num_seqs && sh.shared_tok[first + n] > 0) {
+        T = min(T, sh.shared_tok[first + n]);
+        ++n;
+    }
+    if (n >= 2) {
+        g.first = first;
+        g.n = n;
+        g.T = T;
+    }
+    return g;
+}
+
+// Pieces of a range of len tokens: full part_tokens pieces and a shorter last one.
+__device__ __forceinline__ int pieces_of(int len, int PT) { return (len + PT - 1) / PT; }
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams A) {
     pdl_trigger();  // the attention CTAs may start their set-up now
+    extern __shared__ __align__(16) unsigned char plan_smem[];
+    PlanShared &sh = *reinterpret_cast<PlanShared *>(plan_smem);
+    if (threadIdx.x == 0) {
+        int *p = reinterpret_cast<int *>(plan_smem + sizeof(PlanShared));
+        sh.shared_tok = p;
+        sh.pre = p + A.num_seqs;
+        sh.run_start = reinterpret_cast<short *>(p + 2 * A.num_seqs);
+    }
     constexpr int kKeys = kMaxPartTokens / kBlock + 1;
-    __shared__ int hist[kKeys];
-    __shared__ int offs[kKeys];
-    const int PB = part_tokens / kBlock;
+    const int PT = A.part_tokens, PB = PT / kBlock;
     const int tid = threadIdx.x, lane = tid & 31;
-    const unsigned lt_mask = (1u << lane) - 1u;
-    if (tid < kKeys) hist[tid] = 0;
+    const int S = A.num_seqs;
+    if (tid < 2 * kKeys) (&sh.hist[0][0])[tid] = 0;
     __syncthreads();
-    // pass 1: histogram of partition sizes (in blocks)
-    for (int s0 = 0; s0 < num_seqs; s0 += kPlanThreads) {
-        const int s = s0 + tid;
-        int L = s < num_seqs ? lens[s] : 1;
-        const bool bad = L < 0 || L > max_context_len;
-        if (bad && s < num_seqs && err) atomicOr(err, PA_ERRBIT_CONTEXT_LEN);
-        if (bad) L = 0;
-        const bool live = s < num_seqs && L > 0;
-        const int np = live ? (L + part_tokens - 1) / part_tokens : 0;
-        // full partitions: one add per warp
-        int full = np > 1 ? np - 1 : 0;
+
+    // ---- 1. shared prefixes ------------------------------------------------
+    if (A.group_seqs) {
+        const int min_blocks = kMinSharedTokens >> A.block_shift;
+        // leading full blocks worth comparing, 0 where the first ids differ
+        int jm[kSeqPerThread];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) full += __shfl_xor_sync(0xffffffffu, full, off);
-        if (lane == 0 && full) atomicAdd(&hist[PB], full);
-        // last partitions: one add per distinct size in the warp
-        const int key = live ? (L - (np - 1) * part_tokens + kBlock - 1) / kBlock : 0;
-        const unsigned same = __match_any_sync(0xffffffffu, key);
-        if (live && (same & lt_mask) == 0) atomicAdd(&hist[key], __popc(same));
-    }
-    __syncthreads();
-    if (tid < 32) {  // exclusive scan over sizes, largest first
-        const int key = PB - tid;
-        const int v = (tid < PB) ? hist[key] : 0;
-        int incl = v;
+        for (int i = 0; i < kSeqPerThread; ++i) {
+            const int s = tid * kSeqPerThread + i;
+            int j = 0;
+            if (s >= 1 && s < S) {
+                j = min(valid_len(A, s), valid_len(A, s - 1)) >> A.block_shift;
+                if (j < min_blocks) j = 0;
+                if (j > A.max_blocks_per_seq) j = A.max_blocks_per_seq;
+                if (j > 0) {
+                    const int32_t *r1 = A.tables + (size_t)s * A.max_blocks_per_seq;
+                    const int32_t *r0 = r1 - A.max_blocks_per_seq;
+                    if (__ldg(r1) != __ldg(r0)) j = 0;
+                }
+            }
+            jm[i] = j;
+            if (s < S) sh.shared_tok[s] = j;  // first mismatch so far: none
+        }
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < kSeqPerThread; ++i) sum += jm[i];
+        int base = block_exclusive_sum(sum, sh.red);
+#pragma unroll
+        for (int i = 0; i < kSeqPerThread; ++i) {
+            const int s = tid * kSeqPerThread + i;
+            if (s < S) sh.pre[s] = base;
+            base += jm[i];
+        }
+        __syncthreads();
+        const int total = sh.pre[S - 1] + sh.shared_tok[S - 1];
+        // compare every (sequence, block) candidate pair, flattened over all
+        // threads so the loads are independent; keep each sequence's first
+        // differing block
+        for (int idx = tid; idx < total; idx += kPlanThreads) {
+            int lo = 0, hi = S - 1;  // the last s with pre[s] <= idx
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (sh.pre[mid] <= idx) lo = mid;
+                else hi = mid - 1;
+            }
+            const int s = lo, j = idx - sh.pre[s];
+            const int32_t *r1 = A.tables + (size_t)s * A.max_blocks_per_seq;
+            if (__ldg(r1 + j) != __ldg(r1 - A.max_blocks_per_seq + j))
+                atomicMin(&sh.shared_tok[s], j);
+        }
+        __syncthreads();
+        // blocks -> tokens (whole 16-token chunks), below the minimum -> none
+#pragma unroll
+        for (int i = 0; i < kSeqPerThread; ++i) {
+            const int s = tid * kSeqPerThread + i;
+            if (s < S) {
+                const int t = (sh.shared_tok[s] << A.block_shift) & ~(kBlock - 1);
+                sh.shared_tok[s] = t >= kMinSharedTokens ? t : 0;
+            }
+        }
+        __syncthreads();
+        // run starts: the last s' <= s that does not share with s' - 1 (an
+        // inclusive max-scan)
+        int last = -1;
+#pragma unroll
+        for (int i = 0; i < kSeqPerThread; ++i) {
+            const int s = tid * kSeqPerThread + i;
+            if (s < S && sh.shared_tok[s] == 0) last = s;
+        }
+        int incl = last;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int u = __shfl_up_sync(0xffffffffu, incl, off);
-            if (tid >= off) incl += u;
+            if (lane >= off) incl = max(incl, u);
         }
-        if (tid < PB) offs[key] = incl - v;
-        if (tid == 31) {
-            hdr->counter = 0u;
-            hdr->n_items = (unsigned)incl * (unsigned)num_kv_heads;
-        }
-    }
-    __syncthreads();
-    // pass 2: place every (sequence, partition)
-    for (int s0 = 0; s0 < num_seqs; s0 += kPlanThreads) {
-        const int s = s0 + tid;
-        const int L0 = s < num_seqs ? lens[s] : 0;
-        const bool live = s < num_seqs && L0 > 0 && L0 <= max_context_len;
-        const int L = live ? L0 : 0;
-        const int np = live ? (L + part_tokens - 1) / part_tokens : 0;
-        // full partitions of the warp: contiguous range from one add
-        const int full = np > 1 ? np - 1 : 0;
-        int incl = full;
+        if (lane == 31) sh.red[tid >> 5] = incl;
+        __syncthreads();
+        int carry = -1;
+        for (int w = 0; w < (tid >> 5); ++w) carry = max(carry, sh.red[w]);
+        int prev = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) prev = -1;
+        int rs = max(carry, prev);
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += u;
+        for (int i = 0; i < kSeqPerThread; ++i) {
+            const int s = tid * kSeqPerThread + i;
+            if (s < S) {
+                if (sh.shared_tok[s] == 0) rs = s;
+                sh.run_start[s] = (short)rs;
+            }
         }
-        const int total = __shfl_sync(0xffffffffu, incl, 31);
-        int base = 0;
-        if (lane == 31 && total) base = atomicAdd(&offs[PB], total);
-        base = __shfl_sync(0xffffffffu, base, 31) + incl - full;
-        for (int p = 0; p < full; ++p)
-            items[base + p] = make_int4(s, p, part_tokens, np);
-        // last partition: rank among the warp's lanes with the same size
-        const int ntok = live ? L - (np - 1) * part_tokens : 0;
-        const int key = live ? (ntok + kBlock - 1) / kBlock : 0;
-        const unsigned same = __match_any_sync(0xffffffffu, key);
-        const int leader = __ffs(same) - 1;
-        int slot = 0;
-        if (live && lane == leader) slot = atomicAdd(&offs[key], __popc(same));
-        slot = __shfl_sync(0xffffffffu, slot, leader) + __popc(same & lt_mask);
-        if (live) items[slot] = make_int4(s, np - 1, ntok, np);
+        __syncthreads();
     }
-    pdl_wait();  // earlier work on the stream may still read out
-    // the warp zeroes the output rows of its empty sequences together
-    for (int s0 = 0; s0 < num_seqs; s0 += kPlanThreads) {
+
+    // ---- 2, 3. pieces, counted then placed longest first ------------------
+    // One pass counts (place = false), the other writes (place = true).
+    // Thread-strided over sequences, 1024 at a time; each thread handles its
+    // sequence's own range and, for a group's first sequence, the prefix.
+    // A range of len tokens is len / PT full pieces and one of len % PT.
+    const int own_list = A.split ? 1 : 0;
+    const int L_first = tid < S ? valid_len(A, tid) : 0;  // this thread's first sequence
+    for (int pass = 0; pass < 2; ++pass) {
+        const bool place = pass == 1;
+        for (int s0 = 0; s0 < S; s0 += kPlanThreads) {
+            const int s = s0 + tid;
+            const int L = s0 == 0 ? L_first : (s < S ? valid_len(A, s) : 0);
+            Group g = {s, 1, 0};
+            if (A.group_seqs && L > 0) g = group_of(A, sh, s);
+            // segment 0: the group's shared prefix (its first sequence only);
+            // segment 1: the sequence's own range
+            for (int seg = A.group_seqs ? 0 : 1; seg < 2; ++seg) {
+                int len, t0, pbase, list, cnt;
+                bool grp;
+                if (seg == 0) {
+                    grp = true;
+                    len = (L > 0 && g.n >= 2 && g.first == s) ? g.T : 0;
+                    t0 = 0;
+                    pbase = 0;
+                    list = 0;
+                    cnt = g.n;
+                } else {
+                    grp = false;
+                    len = L > 0 ? L - g.T : 0;
+                    t0 = g.T;
+                    pbase = pieces_of(g.T, PT);
+                    list = own_list;
+                    cnt = pbase + pieces_of(len, PT);
+                }
+                const int nf = len / PT, rem = len - nf * PT;
+                const int key = (rem + kBlock - 1) / kBlock;  // 0: no short piece
+                if (!place) {
+                    // full pieces: one add per warp; the short piece: one add
+                    int full = nf;
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1)
+                        full += __shfl_xor_sync(0xffffffffu, full, off);
+                    if (lane == 0 && full) atomicAdd(&sh.hist[list][PB], full);
+                    if (key) atomicAdd(&sh.hist[list][key], 1);
+                } else {
+                    // full pieces of the warp: a contiguous range from one add
+                    int incl = nf;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const int u = __shfl_up_sync(0xffffffffu, incl, off);
+                        if (lane >= off) incl += u;
+                    }
+                    int base = 0;
+                    if (lane == 31 && incl) base = atomicAdd(&sh.offs[list][PB], incl);
+                    base = __shfl_sync(0xffffffffu, base, 31) + incl - nf;
+                    int4 *items = list ? A.items1 : A.items0;
+                    const int first = grp ? g.first : s;
+                    for (int k = 0; k < nf; ++k)
+                        items[base + k] = make_int4(first, t0 + k * PT, PT,
+                                                    make_item_w(pbase + k, cnt, grp));
+                    if (key) {
+                        const int slot = atomicAdd(&sh.offs[list][key], 1);
+                        items[slot] = make_int4(first, t0 + nf * PT, rem,
+                                                make_item_w(pbase + nf, cnt, grp));
+                    }
+                }
+            }
+        }
+        if (place) break;  // the placing pass is the last: nothing to order after it
+        __syncthreads();
+        if (tid < (A.split ? 64 : 32)) {  // exclusive scans over sizes, largest first
+            const int list = tid >> 5;
+            const int key = PB - lane;
+            const int v = (lane < PB) ? sh.hist[list][key] : 0;
+            int incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += u;
+            }
+            if (lane < PB) sh.offs[list][key] = incl - v;
+            if (lane == 31) {
+                A.hdr->counter[list] = 0u;
+                A.hdr->n_items[list] = (unsigned)incl * (unsigned)A.num_kv_heads;
+            }
+        }
+        if (tid == 32 && !A.split) {
+            A.hdr->counter[1] = 0u;
+            A.hdr->n_items[1] = 0u;
+        }
+        __syncthreads();
+    }
+
+    pdl_wait();  // earlier work on the stream may still read nparts and out
+    for (int s0 = 0; s0 < S; s0 += kPlanThreads) {
         const int s = s0 + tid;
-        const int L = s < num_seqs ? lens[s] : 1;
-        unsigned empty = __ballot_sync(0xffffffffu, s < num_seqs && (L <= 0 || L > max_context_len));
+        const int L0 = s >= S ? 1 : (s0 == 0 ? (L_first > 0 ? L_first : A.lens[s]) : A.lens[s]);
+        const bool bad = L0 < 0 || L0 > A.max_context_len;
+        if (s < S) {
+            if (bad && A.err) atomicOr(A.err, PA_ERRBIT_CONTEXT_LEN);
+            const int L = bad ? 0 : L0;
+            int np = 0;
+            if (L > 0) {
+                Group g = {s, 1, 0};
+                if (A.group_seqs) g = group_of(A, sh, s);
+                np = pieces_of(g.T, A.part_tokens) + pieces_of(L - g.T, A.part_tokens);
+            }
+            A.nparts[s] = np;
+        }
+        // the warp zeroes the output rows of its empty sequences together
+        unsigned empty = __ballot_sync(0xffffffffu, s < S && (L0 <= 0 || bad));
         while (empty) {
             const int src = __ffs(empty) - 1;
             empty &= empty - 1;
-            const size_t base = (size_t)(s0 + (tid & ~31) + src) * num_heads * head_dim;
-            for (int i = lane; i < num_heads * head_dim; i += 32)
-                store_out(out, out_dtype, base + i, 0.f);
+            const size_t base = (size_t)(s0 + (tid & ~31) + src) * A.num_heads * A.head_dim;
+            for (int i = lane; i < A.num_heads * A.head_dim; i += 32)
+                store_out(A.out, A.out_dtype, base + i, 0.f);
         }
     }
 }
@@ -217,9 +488,21 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     __shared__ float4 s_acc[NG][C];
     const int s = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     const int L = P.context_lens[s];  // an input: complete before this grid launched
-    if (L <= P.part_tokens || L > P.max_context_len) return;  // one partition, or invalid
-    const int np = (L + P.part_tokens - 1) / P.part_tokens;
-    pdl_wait();  // partials from the attention kernel
+    if (L <= 0 || L > P.max_context_len) return;  // empty or invalid: a zero row
+    // One partition for sure: no split, and no shared prefix.  A sequence can
+    // share a prefix only with a neighbour whose first block id equals its
+    // own (tables are inputs too, complete before this grid launched).
+    if (L <= P.part_tokens) {
+        if (!P.grouping || L <= kMinSharedTokens) return;
+        const int32_t *row = P.block_tables + (size_t)s * P.max_blocks_per_seq;
+        const int b0 = __ldg(row);
+        const bool prev = s > 0 && __ldg(row - P.max_blocks_per_seq) == b0;
+        const bool next = s + 1 < P.num_seqs && __ldg(row + P.max_blocks_per_seq) == b0;
+        if (!prev && !next) return;
+    }
+    pdl_wait();  // partials from the attention kernels; the plan's counts
+    const int np = P.grouping ? P.nparts[s] : (L + P.part_tokens - 1) / P.part_tokens;
+    if (np <= 1) return;
     const size_t base = ((size_t)s * P.num_heads + h) * P.max_parts;
     const int col = tid % C, grp = tid / C;
     const float4 *acc = reinterpret_cast<const float4 *>(P.part_acc + base * D) + col;
@@ -271,6 +554,21 @@ bool encode_rows(CUtensorMap *map, const void *base, pa_dtype_t dtype, unsigned 
     return encode_tiled(map, base, dtype, 3, dims, strides, box);
 }
 
+// 4-D view [head_dim / 64][heads][sequences][64] of the query
+// [sequences][heads][head_dim]; one box is group_box_heads(G) heads of
+// group_seqs_per_box(G) consecutive sequences (8 rows), all halves: the
+// query rows of a shared-prefix item.
+bool encode_group_query(CUtensorMap *map, const void *q, pa_dtype_t dtype, int num_seqs,
+                        int num_heads, int head_dim, int G) {
+    const cuuint64_t dims[4] = {64u, (cuuint64_t)num_seqs, (cuuint64_t)num_heads,
+                                (cuuint64_t)(head_dim / 64)};
+    const cuuint64_t strides[3] = {(cuuint64_t)num_heads * head_dim * 2,
+                                   (cuuint64_t)head_dim * 2, 128u};
+    const cuuint32_t box[4] = {64u, (cuuint32_t)group_seqs_per_box(G),
+                               (cuuint32_t)group_box_heads(G), (cuuint32_t)(head_dim / 64)};
+    return encode_tiled(map, q, dtype, 4, dims, strides, box);
+}
+
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // log2 of a supported pool block size (8 .. 256 tokens, a power of two), or -1
@@ -308,6 +606,17 @@ extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_
 extern "C" int pa_decode_partition_tokens(int num_seqs, int num_kv_heads, int max_context_len) {
     if (num_seqs < 0 || num_kv_heads <= 0 || max_context_len < 0) return 0;
     return choose_part_tokens(num_seqs, num_kv_heads, max_context_len);
+}
+
+extern "C" int pa_decode_kernel_launches(int num_seqs, int num_heads, int num_kv_heads,
+                                         int head_dim, int max_context_len) {
+    if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        max_context_len < 0 || num_heads % num_kv_heads != 0)
+        return 0;
+    const WsLayout w = ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len);
+    const bool tc = uses_tensor_cores(num_heads / num_kv_heads, head_dim);
+    const bool merge = w.max_parts > 1 && (max_context_len > w.part_tokens || w.group_seqs);
+    return 1 + ((w.group_seqs && !tc) ? 2 : 1) + (merge ? 1 : 0);
 }
 
 namespace {
@@ -353,10 +662,19 @@ pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, cons
     const WsLayout w = ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len);
     if (workspace_bytes < w.bytes) return PA_ERR_WORKSPACE;
 
+    if (w.max_parts > kMaxParts) return PA_ERR_UNSUPPORTED;
+    const int G = num_heads / num_kv_heads;
+    // shared-prefix items need block tables; with G = 1 they run on the
+    // tensor-core kernel and the plain items on the CUDA-core kernel
+    const int grouping = contig_rows == 0 ? w.group_seqs : 0;
+    const bool tc = uses_tensor_cores(G, head_dim);
+    const bool split = grouping && !tc;
+    const bool merge = w.max_parts > 1 && (max_context_len > w.part_tokens || grouping);
+
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     DecodeParams P;
     memset(&P, 0, sizeof(P));
-    if (uses_tensor_cores(num_heads / num_kv_heads, head_dim)) {
+    if (tc || grouping) {
         // a 16-token chunk per box (all halves), or for 8-token blocks one
         // block's 8 rows of one 64-element half
         const bool eight = contig_rows == 0 && block_size < kBlock;
@@ -366,6 +684,9 @@ pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, cons
                          head_dim, 8, head_dim / 64) ||
             !encode_rows(&P.tmap_k, k_cache, dtype, pool_rows, head_dim, box_rows, box_halves) ||
             !encode_rows(&P.tmap_v, v_cache, dtype, pool_rows, head_dim, box_rows, box_halves))
+            return PA_ERR_CUDA;
+        if (grouping &&
+            !encode_group_query(&P.tmap_qs, query, dtype, num_seqs, num_heads, head_dim, G))
             return PA_ERR_CUDA;
     }
     P.out = out;
@@ -383,37 +704,71 @@ pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, cons
     P.num_seqs = num_seqs;
     P.num_heads = num_heads;
     P.num_kv_heads = num_kv_heads;
-    P.G = num_heads / num_kv_heads;
+    P.G = G;
     P.head_dim = head_dim;
     P.num_blocks = num_blocks;
     P.scale_log2 = scale * 1.4426950408889634f;
     P.part_tokens = w.part_tokens;
     P.max_parts = w.max_parts;
+    P.grouping = grouping ? 1 : 0;
     P.hdr = reinterpret_cast<WsHeader *>(ws);
-    P.items = reinterpret_cast<int4 *>(ws + w.items_off);
+    P.nparts = reinterpret_cast<int *>(ws + w.nparts_off);
     P.part_m = reinterpret_cast<float *>(ws + w.m_off);
     P.part_l = reinterpret_cast<float *>(ws + w.l_off);
     P.part_acc = reinterpret_cast<float *>(ws + w.acc_off);
     P.err = dev_error_word;
     cudaStream_t st = (cudaStream_t)stream;
 
-    if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, (const int32_t *)context_lens,
-                   num_seqs, max_context_len, w.part_tokens, num_kv_heads, num_heads, head_dim,
-                   P.items, P.hdr, out, (int)out_dtype, dev_error_word) != cudaSuccess)
+    PlanParams A;
+    memset(&A, 0, sizeof(A));
+    A.lens = context_lens;
+    A.tables = block_tables;
+    A.max_blocks_per_seq = max_blocks_per_seq;
+    A.block_shift = block_shift;
+    A.num_seqs = num_seqs;
+    A.max_context_len = max_context_len;
+    A.part_tokens = w.part_tokens;
+    A.num_kv_heads = num_kv_heads;
+    A.num_heads = num_heads;
+    A.head_dim = head_dim;
+    A.group_seqs = grouping;
+    A.split = split ? 1 : 0;
+    A.items0 = reinterpret_cast<int4 *>(ws + w.items0_off);
+    A.items1 = reinterpret_cast<int4 *>(ws + w.items1_off);
+    A.nparts = P.nparts;
+    A.hdr = P.hdr;
+    A.out = out;
+    A.out_dtype = (int)out_dtype;
+    A.err = dev_error_word;
+    const size_t plan_smem = plan_smem_bytes(num_seqs, grouping != 0);
+    if (plan_smem > 48 * 1024) return PA_ERR_UNSUPPORTED;  // never: grouping caps num_seqs
+    if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), plan_smem, st, A) != cudaSuccess)
         return PA_ERR_CUDA;
 
-    long long cap = (long long)num_seqs * w.max_parts * num_kv_heads;
+    long long cap = w.list_cap * num_kv_heads;
     if (cap > INT_MAX) cap = INT_MAX;
+    auto launch = [&](int kernel) -> pa_status_t {
+        if (head_dim == 64) return launch_decode_d64(P, dtype, (int)cap, st, kernel);
+        if (head_dim == 128) return launch_decode_d128(P, dtype, (int)cap, st, kernel);
+        return launch_decode_d256(P, dtype, (int)cap, st, kernel);
+    };
     pa_status_t st_launch;
-    if (head_dim == 64)
-        st_launch = launch_decode_d64(P, dtype, (int)cap, st);
-    else if (head_dim == 128)
-        st_launch = launch_decode_d128(P, dtype, (int)cap, st);
-    else
-        st_launch = launch_decode_d256(P, dtype, (int)cap, st);
+    P.list = 0;
+    P.items = A.items0;
+    if (split) {
+        // list 0: shared-prefix items on the tensor-core kernel; list 1: the
+        // plain items on the CUDA-core kernel
+        st_launch = launch(kKernelTensorCore);
+        if (st_launch != PA_OK) return st_launch;
+        P.list = 1;
+        P.items = A.items1;
+        st_launch = launch(kKernelByGroup);
+    } else {
+        st_launch = launch(kKernelByGroup);
+    }
     if (st_launch != PA_OK) return st_launch;
 
-    if (w.max_parts > 1) {
+    if (merge) {
         if (num_heads > 65535) return PA_ERR_UNSUPPORTED;
         const dim3 grid((unsigned)num_seqs, (unsigned)num_heads);
         cudaError_t e;

@@ -4,7 +4,7 @@
 
 namespace pa {
 pa_status_t launch_decode_d256(const DecodeParams &P, pa_dtype_t dtype, int grid_cap,
-                               cudaStream_t stream) {
-    return dispatch_dtype<256>(P, dtype, grid_cap, stream);
+                               cudaStream_t stream, int kernel) {
+    return dispatch_dtype<256>(P, dtype, grid_cap, stream, kernel);
 }
 }  // namespace pa

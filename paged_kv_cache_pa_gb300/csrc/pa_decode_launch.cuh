@@ -78,9 +78,10 @@ pa_status_t launch_one_mma(const DecodeParams &P, int grid_cap, cudaStream_t str
 }
 
 template <int D, typename T>
-pa_status_t dispatch_group(const DecodeParams &P, int grid_cap, cudaStream_t stream) {
+pa_status_t dispatch_group(const DecodeParams &P, int grid_cap, cudaStream_t stream, int kernel) {
     const int G = P.G;
     if constexpr (D <= 128) {
+        if (kernel == kKernelTensorCore && G <= 8) return launch_one_mma<D, T>(P, grid_cap, stream);
         if (G == 1) return launch_one<D, 1, T>(P, grid_cap, stream);
         if (G <= 8) return launch_one_mma<D, T>(P, grid_cap, stream);
     } else {
@@ -95,9 +96,9 @@ pa_status_t dispatch_group(const DecodeParams &P, int grid_cap, cudaStream_t str
 
 template <int D>
 pa_status_t dispatch_dtype(const DecodeParams &P, pa_dtype_t dtype, int grid_cap,
-                           cudaStream_t stream) {
-    if (dtype == PA_F16) return dispatch_group<D, __half>(P, grid_cap, stream);
-    if (dtype == PA_BF16) return dispatch_group<D, __nv_bfloat16>(P, grid_cap, stream);
+                           cudaStream_t stream, int kernel) {
+    if (dtype == PA_F16) return dispatch_group<D, __half>(P, grid_cap, stream, kernel);
+    if (dtype == PA_BF16) return dispatch_group<D, __nv_bfloat16>(P, grid_cap, stream, kernel);
     return PA_ERR_INVALID_ARG;
 }
 

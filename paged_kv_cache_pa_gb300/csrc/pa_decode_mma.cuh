@@ -26,10 +26,20 @@
 // length are masked out of the scores and zeroed in the V tile before P V,
 // so stale or poisoned data never reaches the output.
 //
+// Shared-prefix items: the plan turns the blocks that a run of consecutive
+// sequences shares at the start of their tables into one item whose query
+// rows are the run's queries for the KV head's G query heads (8 / G
+// sequences at most, 2 for G = 3, G <= 4), loaded through a second tensor map that views
+// the query as [head_dim / 64][heads][sequences][64].  Each shared K/V tile
+// is then read once for the whole run; every sequence's own remainder is a
+// plain item, and the partitions are merged exactly afterwards
+// [Efficient Memory Management ..., "Shared prefix" and "Beam search": one
+// physical copy of the shared blocks serves every sequence that maps them].
+//
 // Item ends: each consumer warp hands its running state for the item to a
 // dedicated epilogue warp through one of two shared-memory buffers and goes
 // straight on to the next stage; the epilogue warp merges the four states and
-// writes the output row or the partition's partial state.
+// writes each query row's output or partition's partial state.
 //
 // Precision: P is rounded to the operand type in two parts, P = P_hi + P_lo,
 // and both are multiplied with V, so the weights carry ~16 significant bits
@@ -45,11 +55,16 @@ constexpr size_t kBoxBytes = 16 * 128;  // one chunk's 64-element box: 16 rows x
 constexpr size_t kHalfBoxBytes = 8 * 128;  // an 8-token block's box: 8 rows x 128 B
 constexpr size_t kQBoxBytes = 8 * 128;  // the query box: 8 rows x 128 B
 
-// Per-item hand-off from the consumer warps to the epilogue warp.
+// Per-item hand-off from the consumer warps to the epilogue warp.  count:
+// the sequence's partitions (plain item) or the run's sequences (group).
 struct alignas(16) ItemInfo {
-    int s, hk, p, nparts;
+    int s, hk, p, count;
     int flags, pad0, pad1, pad2;
 };
+
+constexpr int kGroupFlag = 2;  // StageMeta / ItemInfo flags: a shared-prefix item
+
+
 
 // threads of a CTA with W consumer warps: producer, W consumers, epilogue
 template <int W>
@@ -152,9 +167,10 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
         prefetch_tmap(&P.tmap_k);
         prefetch_tmap(&P.tmap_v);
         prefetch_tmap(&P.tmap_q);
+        if (P.grouping) prefetch_tmap(&P.tmap_qs);
     }
     pdl_wait();  // the plan kernel's items and counter are ready
-    const unsigned n_items = P.hdr->n_items;
+    const unsigned n_items = P.hdr->n_items[P.list];
     const unsigned Hkv = (unsigned)P.num_kv_heads;
     const int G = P.G;
     const uint64_t policy = l2_evict_first_policy();
@@ -169,12 +185,16 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
         const int4 eA = items.eX;
         const int2 tA = items.tX;
 
-        const int s = eA.x, part = eA.y, ntok = eA.z, nparts = eA.w;
+        const int s = eA.x, t_item = eA.y, ntok = eA.z;
+        const int part = item_part(eA.w), count = item_count(eA.w);
+        const bool group = item_is_group(eA.w);
         const int hk = (int)(cA % Hkv);
         const int nblk = (ntok + kBlock - 1) / kBlock;
         const int nst = (nblk + W - 1) / W;
         const bool split = !P.contig_rows && P.block_size < kBlock;  // 8-token blocks
-        const int t_item = part * P.part_tokens;  // the item's first token
+        // query bytes: 8 rows either way (G heads of s and the rows after
+        // them, or the run's box of heads x sequences)
+        const uint32_t q_tx = (uint32_t)(KB * kQBoxBytes);
         for (int st = 0; st < nst; ++st, ++k) {
             // Everything that does not depend on the ring is worked out before
             // waiting for the slot, so a freed slot is refilled at once.
@@ -195,7 +215,7 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
             const uint32_t kv = split ? (uint32_t)(2 * KB * kHalfBoxBytes) *
                                             (uint32_t)(nb - __popc(bad) + __popc(two & ~bad))
                                       : (uint32_t)(2 * (nb - __popc(bad)) * KB * kBoxBytes);
-            const uint32_t tx = kv + (st == 0 ? (uint32_t)(KB * kQBoxBytes) : 0u);
+            const uint32_t tx = kv + (st == 0 ? q_tx : 0u);
             // this lane's copy: its place in the stage, its row and half, K or V
             bool issue;
             int y, z = 0, is_v;
@@ -238,8 +258,9 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
             }
             if (lane == 0) {
                 StageMeta m;
-                m.s = s; m.hk = hk; m.p = part; m.nparts = nparts;
-                m.j = st; m.nblk = nst; m.nvalid = ntok - j0 * kBlock; m.flags = (int)(bad << 8);
+                m.s = s; m.hk = hk; m.p = part; m.nparts = count;
+                m.j = st; m.nblk = nst; m.nvalid = ntok - j0 * kBlock;
+                m.flags = (int)(bad << 8) | (group ? kGroupFlag : 0);
                 meta[slot] = m;
                 mbar_arrive_expect_tx(&full[slot], tx);
             }
@@ -251,9 +272,14 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
                 else
                     tma_load_3d(sk + o, &P.tmap_k, 0, y, z, &full[slot], policy);
             }
-            if (st == 0 && lane == 0)
-                tma_load_3d(sq + (size_t)slot * KB * kQBoxBytes, &P.tmap_q, 0,
-                            s * P.num_heads + hk * G, 0, &full[slot], policy);
+            if (st == 0 && lane == 0) {
+                if (group)
+                    tma_load_4d(sq + (size_t)slot * KB * kQBoxBytes, &P.tmap_qs, 0, s, hk * G, 0,
+                                &full[slot], policy);
+                else
+                    tma_load_3d(sq + (size_t)slot * KB * kQBoxBytes, &P.tmap_q, 0,
+                                s * P.num_heads + hk * G, 0, &full[slot], policy);
+            }
             __syncwarp();
         }
         if (aborted) break;
@@ -278,9 +304,8 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
         if (lane == 0) {
             *abort_flag = 1;
             if (P.err) atomicOr(P.err, PA_ERRBIT_TIMEOUT);
-            volatile int never = 0;
             const uint32_t first = k > (uint32_t)R ? k - R : 0u;
-            for (uint32_t kk = first; kk < k; ++kk) mbar_wait(&full[kk % R], (kk / R) & 1u, &never);
+            for (uint32_t kk = first; kk < k; ++kk) mbar_drain_wait(&full[kk % R], (kk / R) & 1u);
         }
         __syncwarp();
     }
@@ -441,7 +466,7 @@ __device__ __forceinline__ void run_consumer_mma(const DecodeParams &P, unsigned
         int buf;
         if (!take_buffer(buf)) return;
         float *acc_b = s_acc + (size_t)buf * W * 8 * D;
-        if (g < G) {
+        if (g < G || (mt.flags & kGroupFlag)) {  // a group item uses all 8 rows
             float *dst = acc_b + ((size_t)cw * 8 + g) * D + 2 * t;
 #pragma unroll
             for (int n = 0; n < NT; ++n)
@@ -453,8 +478,8 @@ __device__ __forceinline__ void run_consumer_mma(const DecodeParams &P, unsigned
         }
         if (cw == 0 && lane == 0) {
             ItemInfo it;
-            it.s = mt.s; it.hk = mt.hk; it.p = mt.p; it.nparts = mt.nparts;
-            it.flags = 0; it.pad0 = it.pad1 = it.pad2 = 0;
+            it.s = mt.s; it.hk = mt.hk; it.p = mt.p; it.count = mt.nparts;
+            it.flags = mt.flags & kGroupFlag; it.pad0 = it.pad1 = it.pad2 = 0;
             info[buf] = it;
         }
         mbar_arrive(&acc_full[buf]);  // every consumer thread: its writes are released
@@ -487,32 +512,49 @@ __device__ __forceinline__ void run_epilogue_mma(const DecodeParams &P, uint64_t
         if (it.flags & kEndFlag) return;
         const float *acc_b = s_acc + (size_t)buf * W * 8 * D;
         const float *m_b = s_m + buf * W * 8, *l_b = s_l + buf * W * 8;
-        for (int gg = 0; gg < G; ++gg) {
+        // row r's merge of the W consumer warps' states, then its output
+        // (one partition) or its partial state
+        auto emit = [&](int r, int s_row, int h, int nparts) {
             float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < W; ++w) M = fmaxf(M, m_b[w * 8 + gg]);
+            for (int w = 0; w < W; ++w) M = fmaxf(M, m_b[w * 8 + r]);
             const float Ms = M == -INFINITY ? 0.f : M;
             float cf[W], Lsum = 0.f;
 #pragma unroll
             for (int w = 0; w < W; ++w) {
-                cf[w] = ex2(m_b[w * 8 + gg] - Ms);
-                Lsum += l_b[w * 8 + gg] * cf[w];
+                cf[w] = ex2(m_b[w * 8 + r] - Ms);
+                Lsum += l_b[w * 8 + r] * cf[w];
             }
-            const int h = it.hk * G + gg;
-            const size_t pi = ((size_t)it.s * H + h) * P.max_parts + it.p;
+            const size_t pi = ((size_t)s_row * H + h) * P.max_parts + it.p;
             for (int d = lane; d < D; d += 32) {
                 float ov = 0.f;
 #pragma unroll
-                for (int w = 0; w < W; ++w) ov += acc_b[((size_t)w * 8 + gg) * D + d] * cf[w];
-                if (it.nparts == 1)
-                    store_out(P.out, P.out_dtype, ((size_t)it.s * H + h) * D + d,
+                for (int w = 0; w < W; ++w) ov += acc_b[((size_t)w * 8 + r) * D + d] * cf[w];
+                if (nparts == 1)
+                    store_out(P.out, P.out_dtype, ((size_t)s_row * H + h) * D + d,
                               Lsum > 0.f ? ov / Lsum : 0.f);
                 else
                     P.part_acc[pi * D + d] = ov;
             }
-            if (it.nparts > 1 && lane == 0) {
+            if (nparts > 1 && lane == 0) {
                 P.part_m[pi] = M;
                 P.part_l[pi] = Lsum;
+            }
+        };
+        if (!(it.flags & kGroupFlag)) {
+            // the G heads of one sequence, all with the item's partition count
+            for (int r = 0; r < G; ++r) emit(r, it.s, it.hk * G + r, it.count);
+        } else {
+            // a run's rows belong to different sequences: each row's own
+            // partition count decides between the output and a partial
+            const int nS = group_seqs_per_box(G);
+            int np_lane = 0;
+            if (lane < 8 && lane % nS < it.count) np_lane = P.nparts[it.s + lane % nS];
+            for (int r = 0; r < 8; ++r) {
+                const int gl = r / nS, sl = r % nS;
+                const int np_row = __shfl_sync(0xffffffffu, np_lane, r);
+                if (gl >= G || sl >= it.count) continue;  // no such row
+                emit(r, it.s + sl, it.hk * G + gl, np_row);
             }
         }
         __syncwarp();

@@ -9,9 +9,23 @@
 namespace pa {
 
 // A bounded wait gives up after this long (ns of %globaltimer) or this many
-// polls, whichever comes first, and reports PA_ERRBIT_TIMEOUT.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
-constexpr uint32_t kWaitLimitPolls = 1u << 28;
+// polls, whichever comes first, and reports PA_ERRBIT_TIMEOUT.  The wait
+// for a CTA's own copies and tensor-core work still in flight, before it
+// leaves, has the same limits in every build (kDrainLimit*).
+constexpr uint64_t kDrainLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kDrainLimitPolls = 1u << 28;
+#ifdef PA_TEST_WAIT_POLLS
+// Test build: every other wait polls without blocking (mbarrier.test_wait)
+// and gives up after PA_TEST_WAIT_POLLS polls, so it runs out on an ordinary
+// call and the give-up path can be checked on the GPU.
+constexpr uint64_t kWaitLimitNs = kDrainLimitNs;
+constexpr uint32_t kWaitLimitPolls = PA_TEST_WAIT_POLLS;
+constexpr bool kShortWaits = true;
+#else
+constexpr uint64_t kWaitLimitNs = kDrainLimitNs;
+constexpr uint32_t kWaitLimitPolls = kDrainLimitPolls;
+constexpr bool kShortWaits = false;
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -57,9 +71,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false if the
 // wait gave up (time or poll limit) or *abort became non-zero.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    if constexpr (kShortWaits) {
+        for (uint32_t polls = 0; polls < kWaitLimitPolls; ++polls)
+            if (mbar_test_wait(bar, parity)) return true;
+        return false;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t polls = 1; polls < kWaitLimitPolls; ++polls) {
@@ -68,6 +100,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
             if (*abort) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
         }
+    }
+    return false;
+}
+
+// The wait for a CTA's own copies or tensor-core work in flight before it
+// leaves: no abort flag, and the full limits in every build.
+__device__ __forceinline__ bool mbar_drain_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t polls = 1; polls < kDrainLimitPolls; ++polls) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((polls & 31u) == 0u && globaltimer_ns() - t0 > kDrainLimitNs) return false;
     }
     return false;
 }
@@ -107,6 +151,16 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, 
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
         ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
         "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// 4-D tiled bulk copy (TMA) through a tensor map; same rules as tma_load_3d.
+__device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, int x, int y, int z,
+                                            int w, uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-from paritylib import ATOL, codes, max_abs
+from paritylib import ATOL, codes, max_abs, prefill_oracle, prefill_problem, prefill_run
 
 pytestmark = pytest.mark.gpu
 
@@ -20,60 +20,9 @@ DEV = torch.device("cuda:0")
 TDT = {"f16": torch.float16, "bf16": torch.bfloat16}
 
 
-def _problem(cases, H, Hkv, D, dtype, B, seed, extra_blocks=3):
-    """(cached, new) per sequence -> device tensors and host copies.  Blocks
-    are scattered; every slot no context covers holds NaN."""
-    rng = np.random.default_rng(seed)
-    S = len(cases)
-    lens = np.array([c + n for c, n in cases], np.int32)
-    qsl = np.concatenate([[0], np.cumsum([n for _, n in cases])]).astype(np.int32)
-    nbs = [-(-int(L) // B) for L in lens]
-    NB = sum(nbs) + extra_blocks
-    perm = rng.permutation(NB)
-    maxb = max(max(nbs), 1)
-    tables = np.full((S, maxb), -1, np.int32)
-    pos = 0
-    for s, n in enumerate(nbs):
-        tables[s, :n] = perm[pos:pos + n]
-        pos += n
-    slots = np.concatenate([tables[s, np.arange(c, c + n) // B].astype(np.int64) * B +
-                            np.arange(c, c + n) % B for s, (c, n) in enumerate(cases)])
-    T = int(qsl[-1])
-    g = torch.Generator(device=DEV).manual_seed(seed)
-    dt = TDT[dtype]
-    kc = torch.randn(NB, Hkv, B, D, generator=g, device=DEV).to(dt)
-    vc = torch.randn(NB, Hkv, B, D, generator=g, device=DEV).to(dt)
-    cover = np.zeros((NB, B), bool)
-    for s, L in enumerate(lens):
-        for t in range(int(L)):
-            cover[tables[s, t // B], t % B] = True
-    cv = torch.as_tensor(cover, device=DEV)[:, None, :, None]
-    nan = torch.tensor(float("nan"), dtype=dt, device=DEV)
-    kc = torch.where(cv, kc, nan).contiguous()
-    vc = torch.where(cv, vc, nan).contiguous()
-    q = torch.randn(T, H, D, generator=g, device=DEV).to(dt)
-    key = torch.randn(T, Hkv, D, generator=g, device=DEV).to(dt)
-    val = torch.randn(T, Hkv, D, generator=g, device=DEV).to(dt)
-    d = dict(q=q, kc=kc, vc=vc, key=key, val=val, tables=tables, qsl=qsl, lens=lens,
-             slots=slots, maxq=max(n for _, n in cases), maxc=int(lens.max()))
-    d["host"] = {k: codes(d[k]) for k in ("q", "kc", "vc", "key", "val")}
-    return d
-
-
-def _run(d, scale, out_dtype=torch.float32, err=None, workspace=None):
-    pa.cache_write(d["key"], d["val"], d["kc"], d["vc"], torch.as_tensor(d["slots"], device=DEV),
-                   error_word=err)
-    return pa.prefill_attention(d["q"], d["kc"], d["vc"], torch.as_tensor(d["tables"], device=DEV),
-                                torch.as_tensor(d["qsl"], device=DEV),
-                                torch.as_tensor(d["lens"], device=DEV), d["maxq"], d["maxc"],
-                                scale, out_dtype=out_dtype, workspace=workspace, error_word=err)
-
-
-def _oracle(d, scale, dtype):
-    h = d["host"]
-    oracle.cache_write(h["key"], h["val"], h["kc"], h["vc"], d["slots"])
-    return oracle.prefill_attention(h["q"], h["kc"], h["vc"], d["tables"], d["qsl"], d["lens"],
-                                    scale, dtype)
+_problem = prefill_problem
+_run = prefill_run
+_oracle = prefill_oracle
 
 
 CASES = [(0, 1), (0, 64), (0, 65), (0, 200), (37, 1), (100, 16), (500, 130), (63, 64), (1, 127),
