@@ -133,6 +133,7 @@ struct DecodeParams {
     int part_tokens, max_parts;
     int list;          // the work list this launch takes (0 or 1)
     int grouping;      // 1: the plan may form shared-prefix items
+    int early_trigger; // 1: let the next kernel launch at once (it waits for this grid)
     WsHeader *hdr;
     int4 *items;       // the list this launch takes (entries as above)
     int *nparts;       // per sequence: its partitions (0: empty or invalid)
@@ -241,8 +242,13 @@ struct ItemPipe {
         }
         return r;
     }
-    __device__ __forceinline__ unsigned claim() const {
-        return lane == 0 ? 3u * gridDim.x + atomicAdd(&P->hdr->counter[P->list], 1u) : 0u;
+    // Lane 0 claims the next item beyond the three fixed rounds; no claim
+    // (the answer is past the end) once the list is known to be exhausted,
+    // so CTAs with nothing left do not queue on the counter.
+    __device__ __forceinline__ unsigned claim(bool live) const {
+        if (lane != 0) return 0u;
+        if (!live) return n_items;
+        return 3u * gridDim.x + atomicAdd(&P->hdr->counter[P->list], 1u);
     }
     __device__ __forceinline__ void init(const DecodeParams &params, unsigned n, int lane_) {
         P = &params;
@@ -255,7 +261,7 @@ struct ItemPipe {
         eX = entry(cX);
         eY = entry(cY);
         eZ = entry(cZ);
-        raw = claim();
+        raw = claim(3u * gridDim.x < n_items);
         tX = table(cX, eX);
         tY = table(cY, eY);
     }
@@ -265,7 +271,7 @@ struct ItemPipe {
         const int2 tZ = table(cZ, eZ);
         const unsigned cW = __shfl_sync(0xffffffffu, raw, 0);
         const int4 eW = entry(cW);
-        raw = claim();
+        raw = claim(cW < n_items);
         cX = cY; eX = eY; tX = tY;
         cY = cZ; eY = eZ; tY = tZ;
         cZ = cW; eZ = eW;
@@ -391,8 +397,10 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
         }
         // let the copies already issued land before the CTA can exit
         if (lane == 0) {
+            volatile int never = 0;
             const uint32_t first = k > (uint32_t)R ? k - R : 0u;
-            for (uint32_t kk = first; kk < k; ++kk) mbar_drain_wait(&full[kk % R], (kk / R) & 1u);
+            for (uint32_t kk = first; kk < k; ++kk)
+                mbar_drain_wait(&full[kk % R], (kk / R) & 1u, &never);
         }
         __syncwarp();
     }

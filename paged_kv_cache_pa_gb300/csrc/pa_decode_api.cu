@@ -133,8 +133,15 @@ WsLayout ws_layout(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
 // partition counts are written after the wait because the epilogue and the
 // merge of an earlier call may still read them until that call completes.
 // ---------------------------------------------------------------------------
+// The plan's block: one thread per sequence up to 1024 (at least 128), so a
+// small batch's barriers involve few warps; with shared prefixes each
+// thread keeps up to kSeqPerThread sequences' state (num_seqs <= 4096).
 constexpr int kPlanThreads = 1024;
 constexpr int kSeqPerThread = kMaxGroupSeqs / kPlanThreads;
+int plan_threads(int num_seqs) {
+    const int t = (num_seqs + 31) / 32 * 32;
+    return t < 128 ? 128 : (t > kPlanThreads ? kPlanThreads : t);
+}
 
 struct PlanParams {
     const int32_t *lens;
@@ -159,11 +166,10 @@ struct PlanShared {
     int offs[2][kMaxPartTokens / kBlock + 1];
     int red[32];
     int *shared_tok;   // [num_seqs] tokens s shares with s - 1 (0: none)
-    int *pre;          // [num_seqs] scan scratch
     short *run_start;  // [num_seqs] first sequence of s's run
 };
 constexpr size_t plan_smem_bytes(int num_seqs, bool grouping) {
-    return sizeof(PlanShared) + (grouping ? (size_t)num_seqs * (4 + 4 + 2) + 16 : 0);
+    return sizeof(PlanShared) + (grouping ? (size_t)num_seqs * (4 + 2) + 16 : 0);
 }
 
 __device__ __forceinline__ int valid_len(const PlanParams &A, int s) {
@@ -171,41 +177,15 @@ __device__ __forceinline__ int valid_len(const PlanParams &A, int s) {
     return (L < 0 || L > A.max_context_len) ? 0 : L;
 }
 
-// Block-wide exclusive sum of one value per thread (red: 32 ints of shared
-// memory); returns this thread's prefix.
-__device__ __forceinline__ int block_exclusive_sum(int v, int *red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += u;
-    }
-    __syncthreads();  // red may still be read from an earlier use
-    if (lane == 31) red[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const int x = red[lane];
-        int y = x;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, y, off);
-            if (lane >= off) y += u;
-        }
-        red[lane] = y - x;
-    }
-    __syncthreads();
-    return red[warp] + incl - v;
-}
-
 // Group of sequence s: (first sequence, sequences, shared tokens); n = 1 and
 // T = 0 outside a group.
 struct Group {
     int first, n, T;
 };
-__device__ __forceinline__ Group group_of(const PlanParams &A, const PlanShared &sh, int s) {
+__device__ __forceinline__ Group group_of(const PlanParams &A, const PlanShared &sh, int s,
+                                          bool grouped) {
     Group g = {s, 1, 0};
-    if (!A.group_seqs) return g;
+    if (!grouped) return g;
     const int rs = sh.run_start[s];
     const int first = rs + (s - rs) / A.group_seqs * A.group_seqs;
     int n = 1, T = INT_MAX;
@@ -231,8 +211,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     if (threadIdx.x == 0) {
         int *p = reinterpret_cast<int *>(plan_smem + sizeof(PlanShared));
         sh.shared_tok = p;
-        sh.pre = p + A.num_seqs;
-        sh.run_start = reinterpret_cast<short *>(p + 2 * A.num_seqs);
+        sh.run_start = reinterpret_cast<short *>(p + A.num_seqs);
     }
     constexpr int kKeys = kMaxPartTokens / kBlock + 1;
     const int PT = A.part_tokens, PB = PT / kBlock;
@@ -242,63 +221,83 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     __syncthreads();
 
     // ---- 1. shared prefixes ------------------------------------------------
+    bool grouped = false;  // the same in every thread: some run may form
+    int jm[kSeqPerThread];  // per sequence: leading full blocks worth comparing
     if (A.group_seqs) {
         const int min_blocks = kMinSharedTokens >> A.block_shift;
-        // leading full blocks worth comparing, 0 where the first ids differ
-        int jm[kSeqPerThread];
+        // lengths and first block ids of s and s - 1, in one round of loads
+        int len1[kSeqPerThread], len0[kSeqPerThread], id1[kSeqPerThread], id0[kSeqPerThread];
 #pragma unroll
         for (int i = 0; i < kSeqPerThread; ++i) {
             const int s = tid * kSeqPerThread + i;
-            int j = 0;
+            len1[i] = len0[i] = 0;
+            id1[i] = id0[i] = 0;
             if (s >= 1 && s < S) {
-                j = min(valid_len(A, s), valid_len(A, s - 1)) >> A.block_shift;
-                if (j < min_blocks) j = 0;
-                if (j > A.max_blocks_per_seq) j = A.max_blocks_per_seq;
-                if (j > 0) {
-                    const int32_t *r1 = A.tables + (size_t)s * A.max_blocks_per_seq;
-                    const int32_t *r0 = r1 - A.max_blocks_per_seq;
-                    if (__ldg(r1) != __ldg(r0)) j = 0;
-                }
+                const int32_t *r1 = A.tables + (size_t)s * A.max_blocks_per_seq;
+                len1[i] = A.lens[s];
+                len0[i] = A.lens[s - 1];
+                id1[i] = __ldg(r1);
+                id0[i] = __ldg(r1 - A.max_blocks_per_seq);
             }
+        }
+        // 0 where the first ids differ
+        bool any = false;
+#pragma unroll
+        for (int i = 0; i < kSeqPerThread; ++i) {
+            const bool ok1 = len1[i] >= 0 && len1[i] <= A.max_context_len;
+            const bool ok0 = len0[i] >= 0 && len0[i] <= A.max_context_len;
+            int j = (ok1 && ok0) ? min(len1[i], len0[i]) >> A.block_shift : 0;
+            if (j < max(min_blocks, 1) || id1[i] != id0[i]) j = 0;
+            if (j > A.max_blocks_per_seq) j = A.max_blocks_per_seq;
             jm[i] = j;
-            if (s < S) sh.shared_tok[s] = j;  // first mismatch so far: none
+            any |= j > 0;
         }
-        int sum = 0;
-#pragma unroll
-        for (int i = 0; i < kSeqPerThread; ++i) sum += jm[i];
-        int base = block_exclusive_sum(sum, sh.red);
-#pragma unroll
+        // nothing to compare anywhere (the usual batch): no runs, done
+        grouped = __syncthreads_or(any) != 0;
+    }
+    if (grouped) {
+        // Each thread compares its sequences' rows with the rows before them,
+        // 16 blocks a round with every load of the round in flight together
+        // (16-byte loads when the rows are 16-byte aligned), and keeps the
+        // leading equal blocks as tokens: whole 16-token chunks, none below
+        // the minimum.
+        constexpr int kRound = 16;
+        const bool vec = (reinterpret_cast<uintptr_t>(A.tables) & 15u) == 0 &&
+                         (A.max_blocks_per_seq & 3) == 0;
         for (int i = 0; i < kSeqPerThread; ++i) {
             const int s = tid * kSeqPerThread + i;
-            if (s < S) sh.pre[s] = base;
-            base += jm[i];
-        }
-        __syncthreads();
-        const int total = sh.pre[S - 1] + sh.shared_tok[S - 1];
-        // compare every (sequence, block) candidate pair, flattened over all
-        // threads so the loads are independent; keep each sequence's first
-        // differing block
-        for (int idx = tid; idx < total; idx += kPlanThreads) {
-            int lo = 0, hi = S - 1;  // the last s with pre[s] <= idx
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (sh.pre[mid] <= idx) lo = mid;
-                else hi = mid - 1;
-            }
-            const int s = lo, j = idx - sh.pre[s];
+            if (s >= S) break;
+            const int c = jm[i];
+            int first = c;  // blocks 0 .. first-1 are equal
             const int32_t *r1 = A.tables + (size_t)s * A.max_blocks_per_seq;
-            if (__ldg(r1 + j) != __ldg(r1 - A.max_blocks_per_seq + j))
-                atomicMin(&sh.shared_tok[s], j);
-        }
-        __syncthreads();
-        // blocks -> tokens (whole 16-token chunks), below the minimum -> none
+            const int32_t *r0 = r1 - A.max_blocks_per_seq;
+            for (int j0 = 0; j0 < c && first == c; j0 += kRound) {
+                int a[kRound], b[kRound];
+                if (vec) {
 #pragma unroll
-        for (int i = 0; i < kSeqPerThread; ++i) {
-            const int s = tid * kSeqPerThread + i;
-            if (s < S) {
-                const int t = (sh.shared_tok[s] << A.block_shift) & ~(kBlock - 1);
-                sh.shared_tok[s] = t >= kMinSharedTokens ? t : 0;
+                    for (int u = 0; u < kRound / 4; ++u) {
+                        const bool in = j0 + 4 * u < c;  // a whole int4 inside the row
+                        const int4 x = in ? __ldg(reinterpret_cast<const int4 *>(r1 + j0) + u)
+                                          : make_int4(0, 0, 0, 0);
+                        const int4 y = in ? __ldg(reinterpret_cast<const int4 *>(r0 + j0) + u)
+                                          : make_int4(0, 0, 0, 0);
+                        a[4 * u] = x.x; a[4 * u + 1] = x.y; a[4 * u + 2] = x.z; a[4 * u + 3] = x.w;
+                        b[4 * u] = y.x; b[4 * u + 1] = y.y; b[4 * u + 2] = y.z; b[4 * u + 3] = y.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < kRound; ++u) {
+                        const bool in = j0 + u < c;
+                        a[u] = in ? __ldg(r1 + j0 + u) : 0;
+                        b[u] = in ? __ldg(r0 + j0 + u) : 0;
+                    }
+                }
+#pragma unroll
+                for (int u = kRound - 1; u >= 0; --u)
+                    if (j0 + u < c && a[u] != b[u]) first = j0 + u;
             }
+            const int t = (first << A.block_shift) & ~(kBlock - 1);
+            sh.shared_tok[s] = t >= kMinSharedTokens ? t : 0;
         }
         __syncthreads();
         // run starts: the last s' <= s that does not share with s' - 1 (an
@@ -342,14 +341,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     const int L_first = tid < S ? valid_len(A, tid) : 0;  // this thread's first sequence
     for (int pass = 0; pass < 2; ++pass) {
         const bool place = pass == 1;
-        for (int s0 = 0; s0 < S; s0 += kPlanThreads) {
+        for (int s0 = 0; s0 < S; s0 += (int)blockDim.x) {
             const int s = s0 + tid;
             const int L = s0 == 0 ? L_first : (s < S ? valid_len(A, s) : 0);
             Group g = {s, 1, 0};
-            if (A.group_seqs && L > 0) g = group_of(A, sh, s);
+            if (grouped && L > 0) g = group_of(A, sh, s, grouped);
             // segment 0: the group's shared prefix (its first sequence only);
             // segment 1: the sequence's own range
-            for (int seg = A.group_seqs ? 0 : 1; seg < 2; ++seg) {
+            for (int seg = grouped ? 0 : 1; seg < 2; ++seg) {
                 int len, t0, pbase, list, cnt;
                 bool grp;
                 if (seg == 0) {
@@ -427,7 +426,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     }
 
     pdl_wait();  // earlier work on the stream may still read nparts and out
-    for (int s0 = 0; s0 < S; s0 += kPlanThreads) {
+    for (int s0 = 0; s0 < S; s0 += (int)blockDim.x) {
         const int s = s0 + tid;
         const int L0 = s >= S ? 1 : (s0 == 0 ? (L_first > 0 ? L_first : A.lens[s]) : A.lens[s]);
         const bool bad = L0 < 0 || L0 > A.max_context_len;
@@ -436,8 +435,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             const int L = bad ? 0 : L0;
             int np = 0;
             if (L > 0) {
-                Group g = {s, 1, 0};
-                if (A.group_seqs) g = group_of(A, sh, s);
+                const Group g = group_of(A, sh, s, grouped);
                 np = pieces_of(g.T, A.part_tokens) + pieces_of(L - g.T, A.part_tokens);
             }
             A.nparts[s] = np;
@@ -742,7 +740,8 @@ pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, cons
     A.err = dev_error_word;
     const size_t plan_smem = plan_smem_bytes(num_seqs, grouping != 0);
     if (plan_smem > 48 * 1024) return PA_ERR_UNSUPPORTED;  // never: grouping caps num_seqs
-    if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), plan_smem, st, A) != cudaSuccess)
+    if (launch_pdl(plan_kernel, dim3(1), dim3(plan_threads(num_seqs)), plan_smem, st, A) !=
+        cudaSuccess)
         return PA_ERR_CUDA;
 
     long long cap = w.list_cap * num_kv_heads;
@@ -753,17 +752,22 @@ pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, cons
         return launch_decode_d256(P, dtype, (int)cap, st, kernel);
     };
     pa_status_t st_launch;
-    P.list = 0;
-    P.items = A.items0;
     if (split) {
-        // list 0: shared-prefix items on the tensor-core kernel; list 1: the
-        // plain items on the CUDA-core kernel
+        // list 0: the shared-prefix items on the tensor-core kernel, which
+        // lets the next kernel launch at once; then list 1: the plain items
+        // on the CUDA-core kernel, whose CTAs start as soon as they fit
+        P.list = 0;
+        P.items = A.items0;
+        P.early_trigger = 1;
         st_launch = launch(kKernelTensorCore);
         if (st_launch != PA_OK) return st_launch;
+        P.early_trigger = 0;
         P.list = 1;
         P.items = A.items1;
         st_launch = launch(kKernelByGroup);
     } else {
+        P.list = 0;
+        P.items = A.items0;
         st_launch = launch(kKernelByGroup);
     }
     if (st_launch != PA_OK) return st_launch;

@@ -169,6 +169,12 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
         prefetch_tmap(&P.tmap_q);
         if (P.grouping) prefetch_tmap(&P.tmap_qs);
     }
+    // The shared-prefix launch of a G = 1 call lets the CUDA-core kernel
+    // after it launch at once: that kernel waits for this grid's completion
+    // before it reads anything, and its CTAs start as soon as they fit.
+    // (The next call's plan still runs after this grid completes: it waits
+    // for the kernels in between, which wait for this one.)
+    if (P.early_trigger) pdl_trigger();
     pdl_wait();  // the plan kernel's items and counter are ready
     const unsigned n_items = P.hdr->n_items[P.list];
     const unsigned Hkv = (unsigned)P.num_kv_heads;
@@ -304,8 +310,10 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
         if (lane == 0) {
             *abort_flag = 1;
             if (P.err) atomicOr(P.err, PA_ERRBIT_TIMEOUT);
+            volatile int never = 0;
             const uint32_t first = k > (uint32_t)R ? k - R : 0u;
-            for (uint32_t kk = first; kk < k; ++kk) mbar_drain_wait(&full[kk % R], (kk / R) & 1u);
+            for (uint32_t kk = first; kk < k; ++kk)
+                mbar_drain_wait(&full[kk % R], (kk / R) & 1u, &never);
         }
         __syncwarp();
     }

@@ -707,10 +707,12 @@ __device__ __forceinline__ void run_k_producer(const PrefillParams &P, unsigned 
     }
     // every copy issued lands before the CTA can exit
     if (lane == 0) {
+        volatile int never = 0;
         for (int t = 0; t < 2; ++t)
-            if (qa[t] > 0) mbar_drain_wait(&B.q_full[t], (uint32_t)(qa[t] - 1) & 1u);
+            if (qa[t] > 0) mbar_drain_wait(&B.q_full[t], (uint32_t)(qa[t] - 1) & 1u, &never);
         const int first = rc > L::RK ? rc - L::RK : 0;
-        for (int q = first; q < rc; ++q) mbar_drain_wait(&B.k_full[q % L::RK], (q / L::RK) & 1u);
+        for (int q = first; q < rc; ++q)
+            mbar_drain_wait(&B.k_full[q % L::RK], (q / L::RK) & 1u, &never);
     }
     __syncwarp();
 }
@@ -747,12 +749,13 @@ __device__ __forceinline__ void run_v_producer(const PrefillParams &P, unsigned 
     // every copy issued lands before the CTA can exit; a tile abandoned while
     // its copies went to v_land waits there, not on its stage
     if (lane == 0) {
-        if (land_pending) mbar_drain_wait(B.v_land, (uint32_t)land & 1u);
+        volatile int never = 0;
+        if (land_pending) mbar_drain_wait(B.v_land, (uint32_t)land & 1u, &never);
         // rc counts the tiles whose stage was armed (or, last of an item,
         // handed over after v_land)
         const int first = rc > L::RV ? rc - L::RV : 0;
         for (int q = first; q < rc; ++q)
-            mbar_drain_wait(&B.v_full[q % L::RV], (q / L::RV) & 1u);
+            mbar_drain_wait(&B.v_full[q % L::RV], (q / L::RV) & 1u, &never);
     }
     __syncwarp();
 }
@@ -1433,7 +1436,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             if (lane == 0) {
                 run_mma_p<D, kSplit>(P, t, pv, items, sq, sk, sv, tmem, B, abort_flag);
                 // every MMA it issued has completed before tensor memory is released
-                mbar_drain_wait(&B.o_done[2 * t + pv], 0);
+                volatile int never = 0;
+                mbar_drain_wait(&B.o_done[2 * t + pv], 0, &never);
             }
             __syncwarp();
         }

@@ -105,15 +105,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 }
 
 // The wait for a CTA's own copies or tensor-core work in flight before it
-// leaves: no abort flag, and the full limits in every build.
-__device__ __forceinline__ bool mbar_drain_wait(uint64_t *bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t polls = 1; polls < kDrainLimitPolls; ++polls) {
+// leaves: `never` is a flag nothing sets, and the limits are the full ones
+// in every build (in the ordinary build this is exactly mbar_wait).
+__device__ __forceinline__ bool mbar_drain_wait(uint64_t *bar, uint32_t parity,
+                                                volatile int *never) {
+    if constexpr (kShortWaits) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((polls & 31u) == 0u && globaltimer_ns() - t0 > kDrainLimitNs) return false;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t polls = 1; polls < kDrainLimitPolls; ++polls) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if ((polls & 31u) == 0u && globaltimer_ns() - t0 > kDrainLimitNs) return false;
+        }
+        return false;
+    } else {
+        return mbar_wait(bar, parity, never);
     }
-    return false;
 }
 
 // L2 policy for data read once (the K/V stream).
