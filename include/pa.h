@@ -85,6 +85,11 @@ typedef enum {
 #define PA_ERRBIT_SLOT_OOB    2u  /* a slot >= num_blocks * block size */
 #define PA_ERRBIT_CONTEXT_LEN 4u  /* context_lens[s] < 0 or > max_context_len */
 #define PA_ERRBIT_TIMEOUT     8u  /* a bounded wait inside a kernel gave up */
+/* Only in a library built with -DPA_DEBUG: a work item or partition index
+ * that the decode plan produced failed the kernels' consistency checks (a
+ * sequence, token range or partition slot out of range); the item is skipped.
+ * A production build never sets it. */
+#define PA_ERRBIT_INTERNAL   16u
 
 /*
  * pa_cache_write -- write each new token's key and value rows into the pool

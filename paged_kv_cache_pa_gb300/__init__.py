@@ -33,6 +33,7 @@ __all__ = ["cache_write", "decode_attention", "decode_attention_contiguous",
            "copy_blocks",
            "status_string", "PaError", "library_path", "load_library", "BLOCK_SIZE",
            "ERRBIT_BLOCK_OOB", "ERRBIT_SLOT_OOB", "ERRBIT_CONTEXT_LEN", "ERRBIT_TIMEOUT",
+           "ERRBIT_INTERNAL",
            "MAX_LAYERS", "BLOCK_SIZES", "swap_blocks", "prefill_attention"]
 
 BLOCK_SIZE = 16
@@ -40,6 +41,7 @@ BLOCK_SIZES = (8, 16, 32, 64, 128, 256)
 MAX_LAYERS = 128
 PA_F16, PA_BF16, PA_F32 = 0, 1, 2
 ERRBIT_BLOCK_OOB, ERRBIT_SLOT_OOB, ERRBIT_CONTEXT_LEN, ERRBIT_TIMEOUT = 1, 2, 4, 8
+ERRBIT_INTERNAL = 16  # PA_DEBUG builds only
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libpa_gb300.so")

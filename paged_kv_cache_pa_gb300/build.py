@@ -9,7 +9,10 @@ A stamp of the sources and flags skips the build when nothing changed.
 
 build(variant="shortwait") makes a test copy, libpa_gb300_shortwait.so (objects
 in _build_shortwait/), whose kernels give up their ordinary waits after a few
-non-blocking polls; the tests use it to run the give-up path on the GPU.  The
+non-blocking polls; the tests use it to run the give-up path on the GPU.
+build(variant="debug") makes libpa_gb300_debug.so (objects in _build_debug/):
+the decode kernels check every work item and partition count they take
+(PA_ERRBIT_INTERNAL), and every C-ABI compute call is an NVTX range.  The
 product library is libpa_gb300.so.
 """
 from __future__ import annotations
@@ -48,6 +51,8 @@ VARIANTS = {
     None: (BUILD, LIB, []),
     "shortwait": (os.path.join(ROOT, "_build_shortwait"),
                   os.path.join(PKG, "libpa_gb300_shortwait.so"), ["-DPA_TEST_WAIT_POLLS=4"]),
+    "debug": (os.path.join(ROOT, "_build_debug"),
+              os.path.join(PKG, "libpa_gb300_debug.so"), ["-DPA_DEBUG", "-DPA_NVTX"]),
 }
 
 

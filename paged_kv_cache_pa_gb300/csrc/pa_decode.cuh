@@ -215,6 +215,29 @@ struct Tuning {
 // after Z; every load is issued at least one item before its value is used,
 // so only the very first item waits for two dependent loads.
 // ---------------------------------------------------------------------------
+// PA_DEBUG builds check every work item the producers take: a real
+// sequence, a token range inside its context (inside every member's context
+// for a shared-prefix item), and a partition slot that exists.  An item that
+// fails is reported (PA_ERRBIT_INTERNAL) and skipped.
+#ifdef PA_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+__device__ __forceinline__ bool item_ok(const DecodeParams &P, const int4 &e) {
+    const int s = e.x, part = item_part(e.w), count = item_count(e.w);
+    if (s < 0 || s >= P.num_seqs || e.y < 0 || e.z <= 0 || e.z > kMaxPartTokens) return false;
+    if (part >= P.max_parts) return false;
+    if (item_is_group(e.w)) {
+        if (count < 2 || count > 8 || s + count > P.num_seqs) return false;
+        for (int i = 0; i < count; ++i)
+            if (e.y + e.z > P.context_lens[s + i]) return false;
+        return true;
+    }
+    if (count < 1 || count > P.max_parts || part >= count) return false;
+    return e.y + e.z <= P.context_lens[s];
+}
+
 struct ItemPipe {
     const DecodeParams *P;
     unsigned n_items, Hkv;
@@ -309,6 +332,13 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
         const int4 eA = items.eX;
         const int2 tA = items.tX;
 
+        if constexpr (kDebugChecks) {
+            if (!item_ok(P, eA)) {
+                if (lane == 0 && P.err) atomicOr(P.err, PA_ERRBIT_INTERNAL);
+                items.advance();
+                continue;
+            }
+        }
         const int s = eA.x, t_item = eA.y, ntok = eA.z;
         const int part = item_part(eA.w), nparts = item_count(eA.w);
         const int hk = (int)(cA % Hkv);

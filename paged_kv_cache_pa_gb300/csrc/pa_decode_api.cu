@@ -21,6 +21,7 @@
 
 #include "pa_decode.cuh"
 #include "pa_launch.cuh"
+#include "pa_nvtx.cuh"
 #include "pa_tmap.cuh"
 
 namespace pa {
@@ -500,6 +501,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     }
     pdl_wait();  // partials from the attention kernels; the plan's counts
     const int np = P.grouping ? P.nparts[s] : (L + P.part_tokens - 1) / P.part_tokens;
+    if constexpr (kDebugChecks) {
+        if (np > P.max_parts) {
+            if (tid == 0 && h == 0 && P.err) atomicOr(P.err, PA_ERRBIT_INTERNAL);
+            return;
+        }
+    }
     if (np <= 1) return;
     const size_t base = ((size_t)s * P.num_heads + h) * P.max_parts;
     const int col = tid % C, grp = tid / C;
@@ -795,6 +802,7 @@ extern "C" pa_status_t pa_decode_attention_ex(
     int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
     int num_blocks, int block_size, float scale, pa_dtype_t dtype, void *workspace,
     size_t workspace_bytes, unsigned int *dev_error_word, pa_stream_t stream) {
+    PA_NVTX_RANGE("pa_decode_attention_ex");
     return decode_impl(out, out_dtype, query, k_cache, v_cache, block_tables, max_blocks_per_seq,
                        0, context_lens, max_context_len, num_seqs, num_heads, num_kv_heads,
                        head_dim, num_blocks, block_size, scale, dtype, workspace,
@@ -810,6 +818,7 @@ extern "C" pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, cons
                                            pa_dtype_t dtype, void *workspace,
                                            size_t workspace_bytes, unsigned int *dev_error_word,
                                            pa_stream_t stream) {
+    PA_NVTX_RANGE("pa_decode_attention");
     return decode_impl(out, out_dtype, query, k_cache, v_cache, block_tables, max_blocks_per_seq,
                        0, context_lens, max_context_len, num_seqs, num_heads, num_kv_heads,
                        head_dim, num_blocks, PA_BLOCK_SIZE, scale, dtype, workspace,
@@ -821,6 +830,7 @@ extern "C" pa_status_t pa_decode_attention_contiguous(
     int max_rows, const int32_t *context_lens, int max_context_len, int num_seqs, int num_heads,
     int num_kv_heads, int head_dim, float scale, pa_dtype_t dtype, void *workspace,
     size_t workspace_bytes, unsigned int *dev_error_word, pa_stream_t stream) {
+    PA_NVTX_RANGE("pa_decode_attention_contiguous");
     if (max_rows <= 0) return PA_ERR_INVALID_ARG;
     return decode_impl(out, out_dtype, query, k_cache, v_cache, nullptr, 0, max_rows,
                        context_lens, max_context_len, num_seqs, num_heads, num_kv_heads,

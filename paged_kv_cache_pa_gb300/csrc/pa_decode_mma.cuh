@@ -191,6 +191,13 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
         const int4 eA = items.eX;
         const int2 tA = items.tX;
 
+        if constexpr (kDebugChecks) {
+            if (!item_ok(P, eA)) {
+                if (lane == 0 && P.err) atomicOr(P.err, PA_ERRBIT_INTERNAL);
+                items.advance();
+                continue;
+            }
+        }
         const int s = eA.x, t_item = eA.y, ntok = eA.z;
         const int part = item_part(eA.w), count = item_count(eA.w);
         const bool group = item_is_group(eA.w);

@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include "pa.h"
+#include "pa_nvtx.cuh"
 
 namespace {
 
@@ -37,6 +38,7 @@ extern "C" pa_status_t pa_decode_attention_noalloc(
     int max_context_len, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
     int num_blocks, float scale, pa_dtype_t dtype, unsigned int *dev_error_word,
     pa_stream_t stream) {
+    PA_NVTX_RANGE("pa_decode_attention_noalloc");
     // The array's address is looked up on every call, in the context current
     // now: after a device reset, or under another context, the library's
     // device code is loaded again and the array can move.  The first lookup

@@ -67,6 +67,7 @@
 
 #include "pa.h"
 #include "pa_launch.cuh"
+#include "pa_nvtx.cuh"
 #include "pa_ptx.cuh"
 #include "pa_tmap.cuh"
 #include "pa_umma.cuh"
@@ -1558,6 +1559,7 @@ extern "C" pa_status_t pa_prefill_attention(
     int num_tokens, int num_heads, int num_kv_heads, int head_dim, int num_blocks,
     int block_size, float scale, pa_dtype_t dtype, void *workspace, size_t workspace_bytes,
     unsigned int *dev_error_word, pa_stream_t stream) {
+    PA_NVTX_RANGE("pa_prefill_attention");
     const int shift = shift_of(block_size);
     if (shift < 0) return PA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || num_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 ||

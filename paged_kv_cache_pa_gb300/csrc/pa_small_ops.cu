@@ -23,6 +23,7 @@
 
 #include "pa.h"
 #include "pa_launch.cuh"
+#include "pa_nvtx.cuh"
 #include "pa_ptx.cuh"
 
 namespace {
@@ -154,6 +155,7 @@ extern "C" pa_status_t pa_cache_write_ex(const void *key, const void *value, voi
                                          int num_tokens, int num_blocks, int block_size,
                                          int num_kv_heads, int head_dim, pa_dtype_t dtype,
                                          unsigned int *dev_error_word, pa_stream_t stream) {
+    PA_NVTX_RANGE("pa_cache_write_ex");
     if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0) return PA_ERR_INVALID_ARG;
     const int shift = block_shift_of(block_size);
     if (shift < 0) return PA_ERR_UNSUPPORTED;
@@ -179,6 +181,7 @@ extern "C" pa_status_t pa_cache_write(const void *key, const void *value, void *
                                       int num_blocks, int num_kv_heads, int head_dim,
                                       pa_dtype_t dtype, unsigned int *dev_error_word,
                                       pa_stream_t stream) {
+    PA_NVTX_RANGE("pa_cache_write");
     return pa_cache_write_ex(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_blocks,
                              PA_BLOCK_SIZE, num_kv_heads, head_dim, dtype, dev_error_word,
                              stream);
@@ -189,6 +192,7 @@ extern "C" pa_status_t pa_copy_blocks_ex(void *const *k_caches, void *const *v_c
                                          int num_pairs, int num_blocks, int block_size,
                                          int num_kv_heads, int head_dim, pa_dtype_t dtype,
                                          unsigned int *dev_error_word, pa_stream_t stream) {
+    PA_NVTX_RANGE("pa_copy_blocks_ex");
     if (num_layers <= 0 || num_pairs < 0 || num_blocks <= 0 || num_kv_heads <= 0)
         return PA_ERR_INVALID_ARG;
     if (block_shift_of(block_size) < 0) return PA_ERR_UNSUPPORTED;
@@ -213,6 +217,7 @@ extern "C" pa_status_t pa_copy_blocks(void *const *k_caches, void *const *v_cach
                                       int num_blocks, int num_kv_heads, int head_dim,
                                       pa_dtype_t dtype, unsigned int *dev_error_word,
                                       pa_stream_t stream) {
+    PA_NVTX_RANGE("pa_copy_blocks");
     return pa_copy_blocks_ex(k_caches, v_caches, num_layers, block_pairs, num_pairs, num_blocks,
                              PA_BLOCK_SIZE, num_kv_heads, head_dim, dtype, dev_error_word,
                              stream);
@@ -225,6 +230,7 @@ extern "C" pa_status_t pa_swap_blocks(void *const *dst_k_caches, void *const *ds
                                       int num_dst_blocks, int num_src_blocks, int block_size,
                                       int num_kv_heads, int head_dim, pa_dtype_t dtype,
                                       unsigned int *dev_error_word, pa_stream_t stream) {
+    PA_NVTX_RANGE("pa_swap_blocks");
     if (num_layers <= 0 || num_pairs < 0 || num_dst_blocks <= 0 || num_src_blocks <= 0 ||
         num_kv_heads <= 0)
         return PA_ERR_INVALID_ARG;

@@ -71,3 +71,15 @@ def test_product_package_does_not_use_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
                 assert "pa_oracle" not in src, f
+
+
+def test_error_bits_match_the_header():
+    """The binding's error-word bits are the header's PA_ERRBIT_* values."""
+    import paged_kv_cache_pa_gb300 as pa
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    bits = {name: int(v) for name, v in re.findall(r"#define PA_ERRBIT_(\w+)\s+(\d+)u", text)}
+    assert set(bits) == {"BLOCK_OOB", "SLOT_OOB", "CONTEXT_LEN", "TIMEOUT", "INTERNAL"}
+    for name, v in bits.items():
+        assert getattr(pa, "ERRBIT_" + name) == v, name
+    assert len(set(bits.values())) == len(bits)
+    assert all(v & (v - 1) == 0 for v in bits.values())   # one bit each
