@@ -139,8 +139,8 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
                                 int max_context_len);
 
 /*
- * pa_decode_partition_tokens -- context-partition size (tokens, a multiple of
- * 16 between 64 and 512) that pa_decode_attention uses for these sizes.  A
+ * pa_decode_partition_tokens -- context-partition size (tokens: 256 or 512)
+ * that pa_decode_attention uses for these sizes.  A
  * sequence longer than this is split into partitions whose partial results
  * a merge kernel combines; the merge kernel is enqueued only when
  * max_context_len exceeds it.  Returns 0 for invalid sizes.

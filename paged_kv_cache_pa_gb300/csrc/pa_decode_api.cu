@@ -28,7 +28,9 @@ namespace pa {
 
 namespace {
 
-constexpr int kMinPartTokens = 64;
+// Below 256 tokens a piece is too short for its split to pay: the merge
+// launch costs more than the shorter longest item saves.
+constexpr int kMinPartTokens = 256;
 constexpr long long kTargetItems = 2048;  // ~ 152 SMs x resident CTAs x a few items each
 // Shared prefixes: runs of at most 8 / G consecutive sequences (G <= 4) whose
 // tables start with the same blocks, at least kMinSharedTokens of them full,
