@@ -455,16 +455,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     }
 }
 
-// One CTA per (sequence, query head) of a multi-partition sequence:
+// One CTA per (sequence, HPC query heads) of a multi-partition sequence:
 //   M = max_p m_p,  c_p = 2^(m_p - M),  L = sum_p l_p c_p,
 //   o = sum_p acc_p c_p / L.
-// One pass over the partials: the threads form partition groups of head_dim/4
-// float4 columns each; group g folds partitions g, g + NG, ... into a running
-// (M, L, o), rescaling it whenever the maximum grows, so a partition's m, l
-// and acc are loaded together instead of in three dependent rounds.  The
-// groups' states are then folded the same way through shared memory.
+// One pass over the partials: the TPH = 128 / HPC threads of a head cover its
+// head_dim / 4 float4 columns (CPT columns a thread) and, when there are more
+// threads than columns, form NG partition groups; group g folds partitions
+// g, g + NG, ... into a running (M, L, o), rescaling it whenever the maximum
+// grows, so a partition's m, l and acc are loaded together instead of in
+// three dependent rounds.  The groups' states are then folded the same way
+// through shared memory.  Several heads a CTA (HPC > 1) keep the grid small
+// when most sequences need no merge: those CTAs only read a length and leave,
+// and it is their launches, not the merges, that would cost the time.
 constexpr int kMergeThreads = 128;
 constexpr int kMergeBatch = 4;  // partitions a thread loads before folding them
+constexpr int kMergeMaxCtas = 2048;  // heads per CTA grow until the grid is no larger
 
 // (M, L, o) <- the merge of (M, L, o) and (mp, lp, a); an empty state has
 // M = -inf (ex2(-inf) = 0 drops it).
@@ -481,13 +486,19 @@ __device__ __forceinline__ void fold_state(float &M, float &L, float4 &o, float 
     M = Mn;
 }
 
-template <int D>
+template <int D, int HPC>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ DecodeParams P) {
-    constexpr int C = D / 4;                   // float4 columns
-    constexpr int NG = kMergeThreads / C;      // partition groups
-    __shared__ float s_m[NG], s_l[NG];
-    __shared__ float4 s_acc[NG][C];
-    const int s = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    constexpr int C = D / 4;                       // float4 columns of a head
+    constexpr int TPH = kMergeThreads / HPC;       // threads of a head
+    constexpr int CPT = C > TPH ? C / TPH : 1;     // columns a thread
+    constexpr int NG = TPH > C ? TPH / C : 1;      // partition groups of a head
+    static_assert(CPT * TPH == C * NG && (NG == 1 || CPT == 1), "merge shape");
+    __shared__ float s_m[HPC][NG], s_l[HPC][NG];
+    __shared__ float4 s_acc[HPC][NG][C];
+    const int s = blockIdx.x, tid = threadIdx.x;
+    const int hl = tid / TPH, th = tid % TPH;        // head within the CTA, thread within the head
+    const int h = blockIdx.y * HPC + hl;
+    const int grp = th / (C / CPT), c0 = (th % (C / CPT)) * CPT;  // partition group, first column
     const int L = P.context_lens[s];  // an input: complete before this grid launched
     if (L <= 0 || L > P.max_context_len) return;  // empty or invalid: a zero row
     // One partition for sure: no split, and no shared prefix.  A sequence can
@@ -505,45 +516,64 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     const int np = P.grouping ? P.nparts[s] : (L + P.part_tokens - 1) / P.part_tokens;
     if constexpr (kDebugChecks) {
         if (np > P.max_parts) {
-            if (tid == 0 && h == 0 && P.err) atomicOr(P.err, PA_ERRBIT_INTERNAL);
+            if (tid == 0 && blockIdx.y == 0 && P.err) atomicOr(P.err, PA_ERRBIT_INTERNAL);
             return;
         }
     }
     if (np <= 1) return;
-    const size_t base = ((size_t)s * P.num_heads + h) * P.max_parts;
-    const int col = tid % C, grp = tid / C;
-    const float4 *acc = reinterpret_cast<const float4 *>(P.part_acc + base * D) + col;
+    const bool live = h < P.num_heads;  // the last CTA of a row may hold fewer heads
+    const size_t base = ((size_t)s * P.num_heads + (live ? h : 0)) * P.max_parts;
+    const float4 *acc = reinterpret_cast<const float4 *>(P.part_acc + base * D) + c0;
 
     float M = -INFINITY, Lsum = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p0 = grp; p0 < np; p0 += kMergeBatch * NG) {
+    float4 o[CPT];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float Mc[CPT], Lc[CPT];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) {
+        Mc[c] = -INFINITY;
+        Lc[c] = 0.f;
+    }
+    for (int p0 = grp; live && p0 < np; p0 += kMergeBatch * NG) {
         float mp[kMergeBatch], lp[kMergeBatch];
-        float4 a[kMergeBatch];
+        float4 a[kMergeBatch][CPT];
 #pragma unroll
         for (int u = 0; u < kMergeBatch; ++u) {
             const int p = p0 + u * NG;
             const bool in = p < np;
             mp[u] = in ? P.part_m[base + p] : -INFINITY;
             lp[u] = in ? P.part_l[base + p] : 0.f;
-            a[u] = in ? acc[(size_t)p * C] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < CPT; ++c)
+                a[u][c] = in ? acc[(size_t)p * C + c] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int u = 0; u < kMergeBatch; ++u) fold_state(M, Lsum, o, mp[u], lp[u], a[u]);
-    }
-    if (col == 0) {
-        s_m[grp] = M;
-        s_l[grp] = Lsum;
-    }
-    s_acc[grp][col] = o;
-    __syncthreads();
-    if (grp == 0) {
+        for (int u = 0; u < kMergeBatch; ++u)
 #pragma unroll
-        for (int g = 1; g < NG; ++g) fold_state(M, Lsum, o, s_m[g], s_l[g], s_acc[g][col]);
-        const size_t ob = ((size_t)s * P.num_heads + h) * D + col * 4;
-        store_out(P.out, P.out_dtype, ob + 0, Lsum > 0.f ? o.x / Lsum : 0.f);
-        store_out(P.out, P.out_dtype, ob + 1, Lsum > 0.f ? o.y / Lsum : 0.f);
-        store_out(P.out, P.out_dtype, ob + 2, Lsum > 0.f ? o.z / Lsum : 0.f);
-        store_out(P.out, P.out_dtype, ob + 3, Lsum > 0.f ? o.w / Lsum : 0.f);
+            for (int c = 0; c < CPT; ++c) fold_state(Mc[c], Lc[c], o[c], mp[u], lp[u], a[u][c]);
+    }
+    M = Mc[0];
+    Lsum = Lc[0];  // every column folds the same (m, l): the same M and L
+    if constexpr (NG > 1) {  // (then CPT == 1)
+        if (c0 == 0) {
+            s_m[hl][grp] = M;
+            s_l[hl][grp] = Lsum;
+        }
+        s_acc[hl][grp][c0] = o[0];
+        __syncthreads();
+        if (grp != 0) return;
+#pragma unroll
+        for (int g = 1; g < NG; ++g) fold_state(M, Lsum, o[0], s_m[hl][g], s_l[hl][g], s_acc[hl][g][c0]);
+    }
+    if (!live) return;
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) {
+        const size_t ob = ((size_t)s * P.num_heads + h) * D + (size_t)(c0 + c) * 4;
+        store_out(P.out, P.out_dtype, ob + 0, Lsum > 0.f ? o[c].x / Lsum : 0.f);
+        store_out(P.out, P.out_dtype, ob + 1, Lsum > 0.f ? o[c].y / Lsum : 0.f);
+        store_out(P.out, P.out_dtype, ob + 2, Lsum > 0.f ? o[c].z / Lsum : 0.f);
+        store_out(P.out, P.out_dtype, ob + 3, Lsum > 0.f ? o[c].w / Lsum : 0.f);
     }
 }
 
@@ -783,14 +813,24 @@ pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, cons
 
     if (merge) {
         if (num_heads > 65535) return PA_ERR_UNSUPPORTED;
-        const dim3 grid((unsigned)num_seqs, (unsigned)num_heads);
-        cudaError_t e;
-        if (head_dim == 64)
-            e = launch_pdl(merge_kernel<64>, grid, dim3(kMergeThreads), 0, st, P);
-        else if (head_dim == 128)
-            e = launch_pdl(merge_kernel<128>, grid, dim3(kMergeThreads), 0, st, P);
-        else
-            e = launch_pdl(merge_kernel<256>, grid, dim3(kMergeThreads), 0, st, P);
+        // heads a CTA: 1, 2, 4 or 8, the fewest that keep the grid within
+        // kMergeMaxCtas CTAs
+        int hpc = 1;
+        while (hpc < 8 && (long long)num_seqs * ((num_heads + hpc - 1) / hpc) > kMergeMaxCtas)
+            hpc *= 2;
+        const dim3 grid((unsigned)num_seqs, (unsigned)((num_heads + hpc - 1) / hpc));
+        cudaError_t e = cudaErrorInvalidValue;
+        auto go = [&](auto kern) { e = launch_pdl(kern, grid, dim3(kMergeThreads), 0, st, P); };
+        if (head_dim == 64) {
+            if (hpc == 1) go(merge_kernel<64, 1>); else if (hpc == 2) go(merge_kernel<64, 2>);
+            else if (hpc == 4) go(merge_kernel<64, 4>); else go(merge_kernel<64, 8>);
+        } else if (head_dim == 128) {
+            if (hpc == 1) go(merge_kernel<128, 1>); else if (hpc == 2) go(merge_kernel<128, 2>);
+            else if (hpc == 4) go(merge_kernel<128, 4>); else go(merge_kernel<128, 8>);
+        } else {
+            if (hpc == 1) go(merge_kernel<256, 1>); else if (hpc == 2) go(merge_kernel<256, 2>);
+            else if (hpc == 4) go(merge_kernel<256, 4>); else go(merge_kernel<256, 8>);
+        }
         if (e != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;
