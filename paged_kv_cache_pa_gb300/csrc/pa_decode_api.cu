@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
 // and it is their launches, not the merges, that would cost the time.
 constexpr int kMergeThreads = 128;
 constexpr int kMergeBatch = 4;  // partitions a thread loads before folding them
-constexpr int kMergeMaxCtas = 2048;  // heads per CTA grow until the grid is no larger
+constexpr int kMergeMaxCtas = 3072;  // heads per CTA grow until the grid is no larger
 
 // (M, L, o) <- the merge of (M, L, o) and (mp, lp, a); an empty state has
 // M = -inf (ex2(-inf) = 0 drops it).
