@@ -225,7 +225,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
 
     // ---- 1. shared prefixes ------------------------------------------------
     bool grouped = false;  // the same in every thread: some run may form
-    int jm[kSeqPerThread];  // per sequence: leading full blocks worth comparing
     if (A.group_seqs) {
         const int min_blocks = kMinSharedTokens >> A.block_shift;
         // lengths and first block ids of s and s - 1, in one round of loads
@@ -252,25 +251,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             int j = (ok1 && ok0) ? min(len1[i], len0[i]) >> A.block_shift : 0;
             if (j < max(min_blocks, 1) || id1[i] != id0[i]) j = 0;
             if (j > A.max_blocks_per_seq) j = A.max_blocks_per_seq;
-            jm[i] = j;
+            const int s = tid * kSeqPerThread + i;
+            if (s < S) sh.shared_tok[s] = j;  // blocks worth comparing, until compared
             any |= j > 0;
         }
         // nothing to compare anywhere (the usual batch): no runs, done
         grouped = __syncthreads_or(any) != 0;
     }
     if (grouped) {
-        // Each thread compares its sequences' rows with the rows before them,
-        // 16 blocks a round with every load of the round in flight together
-        // (16-byte loads when the rows are 16-byte aligned), and keeps the
-        // leading equal blocks as tokens: whole 16-token chunks, none below
-        // the minimum.
+        // Each thread compares the rows of sequences tid, tid + blockDim.x, ...
+        // with the rows before them (every thread has a sequence before any
+        // has a second), 16 blocks a round with every load of the round in
+        // flight together (16-byte loads when the rows are 16-byte aligned),
+        // and keeps the leading equal blocks as tokens: whole 16-token
+        // chunks, none below the minimum.
         constexpr int kRound = 16;
         const bool vec = (reinterpret_cast<uintptr_t>(A.tables) & 15u) == 0 &&
                          (A.max_blocks_per_seq & 3) == 0;
-        for (int i = 0; i < kSeqPerThread; ++i) {
-            const int s = tid * kSeqPerThread + i;
-            if (s >= S) break;
-            const int c = jm[i];
+        for (int s = tid; s < S; s += (int)blockDim.x) {
+            const int c = sh.shared_tok[s];
             int first = c;  // blocks 0 .. first-1 are equal
             const int32_t *r1 = A.tables + (size_t)s * A.max_blocks_per_seq;
             const int32_t *r0 = r1 - A.max_blocks_per_seq;
