@@ -120,6 +120,35 @@ def test_partition_edges_at_512():
     assert max_abs(got, want) <= ATOL
 
 
+def _merge_hpc(S, H):
+    """Query heads a merge CTA takes for these sizes (the host's rule)."""
+    hpc = 1
+    while hpc < 8 and S * -(-H // hpc) > 3072:
+        hpc *= 2
+    return hpc
+
+
+@pytest.mark.parametrize("S,H,Hkv,D,dtype,hpc", [
+    (1600, 8, 8, 64, "f16", 8),     # CUDA-core kernel, one thread a column group
+    (800, 16, 16, 128, "bf16", 8),  # two float4 columns a thread
+    (400, 20, 20, 256, "f16", 4),   # head_dim 256: two columns a thread
+    (100, 40, 40, 128, "f16", 2),   # two partition groups a head
+    (128, 32, 8, 128, "bf16", 2),   # tensor-core kernel (4 query heads a KV head)
+])
+def test_merge_several_heads_a_cta(S, H, Hkv, D, dtype, hpc):
+    """Batches large enough that one merge CTA takes several query heads:
+    most sequences fit one partition (their CTAs leave at once), every
+    eleventh needs a merge of two partitions."""
+    assert _merge_hpc(S, H) == hpc
+    rng = np.random.default_rng(S + H + D)
+    lens = rng.integers(1, 33, S)
+    lens[::11] = rng.integers(520, 1000, len(lens[::11]))
+    wl = custom_workload(lens, H, Hkv, D, dtype, seed=S + D)
+    assert pa.decode_partition_tokens(S, Hkv, wl.max_context_len) == 512
+    got, want = _run_and_check(wl, whole_pool=False)
+    assert max_abs(got, want) <= ATOL
+
+
 def test_poisoned_padding_is_never_read():
     """NaN in every slot past each sequence's length and in every unused
     block: the output stays finite and equal to the oracle's."""
