@@ -153,7 +153,9 @@ int pa_decode_partition_tokens(int num_seqs, int num_kv_heads, int max_context_l
  * kernel or, when shared-prefix items may form with one query head per KV
  * head, two (the tensor-core kernel for the shared prefixes, the CUDA-core
  * kernel for the rest), and the merge when a sequence may have more than one
- * partition.  0 for invalid sizes.  Host only, no CUDA calls.
+ * partition.  1 (the attention kernel alone) for a batch of at most 256
+ * (sequence, KV head) pairs whose contexts fit one partition and that forms
+ * no shared-prefix items.  0 for invalid sizes.  Host only, no CUDA calls.
  */
 int pa_decode_kernel_launches(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                               int max_context_len);
@@ -215,7 +217,10 @@ int pa_decode_kernel_launches(int num_seqs, int num_heads, int num_kv_heads, int
  * work lists), one attention kernel (or two: shared prefixes on the
  * tensor-core kernel and the rest on the CUDA-core kernel when
  * num_heads == num_kv_heads), and a merge kernel when a sequence may have
- * more than one partition; pa_decode_kernel_launches gives the count.
+ * more than one partition.  A small batch (at most 256 (sequence, KV head)
+ * pairs, every context within one partition, no shared prefixes) skips the
+ * plan: the attention kernel takes the pairs directly.
+ * pa_decode_kernel_launches gives the count.
  */
 pa_status_t pa_decode_attention(void *out, pa_dtype_t out_dtype, const void *query,
                                 const void *k_cache, const void *v_cache,

@@ -134,6 +134,12 @@ struct DecodeParams {
     int list;          // the work list this launch takes (0 or 1)
     int grouping;      // 1: the plan may form shared-prefix items
     int early_trigger; // 1: let the next kernel launch at once (it waits for this grid)
+    // direct = 1: no plan ran, and the host launches the kernels' DIRECT
+    // form.  Item c is the whole context of (sequence c / Hkv, KV head
+    // c % Hkv) and CTA b takes items b, b + grid, ... (for small batches whose
+    // contexts fit one partition, with no shared prefixes); hdr, items and
+    // nparts are then unused.
+    int direct;
     WsHeader *hdr;
     int4 *items;       // the list this launch takes (entries as above)
     int *nparts;       // per sequence: its partitions (0: empty or invalid)
@@ -224,8 +230,10 @@ constexpr bool kDebugChecks = true;
 #else
 constexpr bool kDebugChecks = false;
 #endif
+template <bool DIRECT>
 __device__ __forceinline__ bool item_ok(const DecodeParams &P, const int4 &e) {
     const int s = e.x, part = item_part(e.w), count = item_count(e.w);
+    if (DIRECT && e.z == 0) return s >= 0 && s < P.num_seqs;  // an empty unit
     if (s < 0 || s >= P.num_seqs || e.y < 0 || e.z <= 0 || e.z > kMaxPartTokens) return false;
     if (part >= P.max_parts) return false;
     if (item_is_group(e.w)) {
@@ -238,6 +246,17 @@ __device__ __forceinline__ bool item_ok(const DecodeParams &P, const int4 &e) {
     return e.y + e.z <= P.context_lens[s];
 }
 
+// Without a plan, the producer of an empty or invalid unit (s, hk) writes its
+// G output rows as zeros, and flags an invalid length once per sequence.
+__device__ __forceinline__ void zero_unit_rows(const DecodeParams &P, int s, int hk, int lane) {
+    const int L = P.context_lens[s];
+    if (lane == 0 && hk == 0 && (L < 0 || L > P.max_context_len) && P.err)
+        atomicOr(P.err, PA_ERRBIT_CONTEXT_LEN);
+    const size_t base = ((size_t)s * P.num_heads + (size_t)hk * P.G) * P.head_dim;
+    for (int i = lane; i < P.G * P.head_dim; i += 32) store_out(P.out, P.out_dtype, base + i, 0.f);
+}
+
+template <bool DIRECT>
 struct ItemPipe {
     const DecodeParams *P;
     unsigned n_items, Hkv;
@@ -247,7 +266,14 @@ struct ItemPipe {
     int2 tX, tY;               // block-table entries of this lane's chunk of X and Y
 
     __device__ __forceinline__ int4 entry(unsigned c) const {
-        return c < n_items ? P->items[c / Hkv] : make_int4(0, 0, 0, 0);
+        if (c >= n_items) return make_int4(0, 0, 0, 0);
+        if constexpr (DIRECT) {  // the unit's whole context; an empty or invalid one has no tokens
+            const int seq = (int)(c / Hkv);
+            const int L = P->context_lens[seq];
+            const int Lv = (L < 0 || L > P->max_context_len) ? 0 : L;
+            return make_int4(seq, 0, Lv, make_item_w(0, 1, false));
+        }
+        return P->items[c / Hkv];
     }
     // Lane j's chunk (tokens 16 j .. 16 j + 15 of the item): x = the block
     // holding its first token; y = the next block, read only for 8-token
@@ -267,9 +293,11 @@ struct ItemPipe {
     }
     // Lane 0 claims the next item beyond the three fixed rounds; no claim
     // (the answer is past the end) once the list is known to be exhausted,
-    // so CTAs with nothing left do not queue on the counter.
-    __device__ __forceinline__ unsigned claim(bool live) const {
+    // so CTAs with nothing left do not queue on the counter.  Without a plan
+    // the next item is simply the one a grid after `prev`.
+    __device__ __forceinline__ unsigned claim(bool live, unsigned prev) const {
         if (lane != 0) return 0u;
+        if constexpr (DIRECT) return prev + gridDim.x;
         if (!live) return n_items;
         return 3u * gridDim.x + atomicAdd(&P->hdr->counter[P->list], 1u);
     }
@@ -284,7 +312,7 @@ struct ItemPipe {
         eX = entry(cX);
         eY = entry(cY);
         eZ = entry(cZ);
-        raw = claim(3u * gridDim.x < n_items);
+        raw = claim(3u * gridDim.x < n_items, cZ);
         tX = table(cX, eX);
         tY = table(cY, eY);
     }
@@ -294,7 +322,7 @@ struct ItemPipe {
         const int2 tZ = table(cZ, eZ);
         const unsigned cW = __shfl_sync(0xffffffffu, raw, 0);
         const int4 eW = entry(cW);
-        raw = claim(cW < n_items);
+        raw = claim(cW < n_items, cW);
         cX = cY; eX = eY; tX = tY;
         cY = cZ; eY = eZ; tY = tZ;
         cZ = cW; eZ = eW;
@@ -304,12 +332,13 @@ struct ItemPipe {
 // ---------------------------------------------------------------------------
 // producer warp
 // ---------------------------------------------------------------------------
-template <int D, int GM, typename T, int R>
+template <int D, int GM, typename T, int R, bool DIRECT>
 __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv, T *sq,
                                              StageMeta *meta, uint64_t *full, uint64_t *empty,
                                              volatile int *abort_flag, int lane) {
     pdl_wait();  // the plan kernel's items and counter are ready
-    const unsigned n_items = P.hdr->n_items[P.list];
+    const unsigned n_items = DIRECT ? (unsigned)(P.num_seqs * P.num_kv_heads)
+                                    : P.hdr->n_items[P.list];
     const unsigned Hkv = (unsigned)P.num_kv_heads;
     const int G = P.G;
     const uint64_t policy = l2_evict_first_policy();
@@ -318,7 +347,7 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
     const T *qg = static_cast<const T *>(P.q);
     constexpr size_t kTile = (size_t)kBlock * D;
 
-    ItemPipe items;
+    ItemPipe<DIRECT> items;
     items.init(P, n_items, lane);
 
     uint32_t k = 0;      // stages issued so far
@@ -333,7 +362,7 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
         const int2 tA = items.tX;
 
         if constexpr (kDebugChecks) {
-            if (!item_ok(P, eA)) {
+            if (!item_ok<DIRECT>(P, eA)) {
                 if (lane == 0 && P.err) atomicOr(P.err, PA_ERRBIT_INTERNAL);
                 items.advance();
                 continue;
@@ -342,6 +371,13 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
         const int s = eA.x, t_item = eA.y, ntok = eA.z;
         const int part = item_part(eA.w), nparts = item_count(eA.w);
         const int hk = (int)(cA % Hkv);
+        if constexpr (DIRECT) {
+            if (ntok == 0) {  // an empty or invalid unit
+                zero_unit_rows(P, s, hk, lane);
+                items.advance();
+                continue;
+            }
+        }
         const int nblk = (ntok + kBlock - 1) / kBlock;
         // Lane j prepares chunk j's copies once per item (all chunks at once),
         // so the per-chunk loop below only waits, arms the barrier and issues.
@@ -650,7 +686,7 @@ __device__ __forceinline__ void run_consumer(const DecodeParams &P, const T *sk,
     }
 }
 
-template <int D, int GM, typename T, int R, int MINB>
+template <int D, int GM, typename T, int R, int MINB, bool DIRECT>
 __global__ void __launch_bounds__(kThreads, MINB) paged_decode_kernel(const __grid_constant__ DecodeParams P) {
     extern __shared__ __align__(128) unsigned char smem[];
     using L = Layout<D, GM, R>;
@@ -679,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, MINB) paged_decode_kernel(const __gr
     }
     __syncthreads();
     if (warp == 0)
-        run_producer<D, GM, T, R>(P, sk, sv, sq, meta, full, empty, abort_flag, lane);
+        run_producer<D, GM, T, R, DIRECT>(P, sk, sv, sq, meta, full, empty, abort_flag, lane);
     else
         run_consumer<D, GM, T, R>(P, sk, sv, sq, meta, full, empty, cbar, s_acc, s_m, s_l,
                                   abort_flag, warp - 1, lane);

@@ -41,6 +41,17 @@ constexpr int kMaxGroupSeqs = 4096;
 // Below this longest context the tokens a shared prefix could save do not
 // pay for the work of finding it (and, for G = 1, a second kernel).
 constexpr int kMinGroupContext = 256;
+// A batch of at most this many (sequence, KV head) units, whose contexts
+// each fit one partition and which forms no shared-prefix items, runs
+// without the plan: each unit is one item, and CTA b takes units b,
+// b + grid, ...  (right for any grid; at this size one item a CTA or less
+// on a GB300).  The plan kernel and its dependent launch would cost more
+// than such a batch's attention.
+constexpr long long kDirectMaxUnits = 256;
+
+bool plan_free(int num_seqs, int num_kv_heads, int max_parts, int grouping) {
+    return !grouping && max_parts == 1 && (long long)num_seqs * num_kv_heads <= kDirectMaxUnits;
+}
 
 int choose_part_tokens(int num_seqs, int num_kv_heads, int max_context_len) {
     int p = kMaxPartTokens;
@@ -652,6 +663,7 @@ extern "C" int pa_decode_kernel_launches(int num_seqs, int num_heads, int num_kv
     const WsLayout w = ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len);
     const bool tc = uses_tensor_cores(num_heads / num_kv_heads, head_dim);
     const bool merge = w.max_parts > 1 && (max_context_len > w.part_tokens || w.group_seqs);
+    if (plan_free(num_seqs, num_kv_heads, w.max_parts, w.group_seqs)) return 1;
     return 1 + ((w.group_seqs && !tc) ? 2 : 1) + (merge ? 1 : 0);
 }
 
@@ -776,13 +788,17 @@ pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, cons
     A.out = out;
     A.out_dtype = (int)out_dtype;
     A.err = dev_error_word;
-    const size_t plan_smem = plan_smem_bytes(num_seqs, grouping != 0);
-    if (plan_smem > 48 * 1024) return PA_ERR_UNSUPPORTED;  // never: grouping caps num_seqs
-    if (launch_pdl(plan_kernel, dim3(1), dim3(plan_threads(num_seqs)), plan_smem, st, A) !=
-        cudaSuccess)
-        return PA_ERR_CUDA;
+    const bool direct = plan_free(num_seqs, num_kv_heads, w.max_parts, grouping);
+    P.direct = direct ? 1 : 0;
+    if (!direct) {
+        const size_t plan_smem = plan_smem_bytes(num_seqs, grouping != 0);
+        if (plan_smem > 48 * 1024) return PA_ERR_UNSUPPORTED;  // never: grouping caps num_seqs
+        if (launch_pdl(plan_kernel, dim3(1), dim3(plan_threads(num_seqs)), plan_smem, st, A) !=
+            cudaSuccess)
+            return PA_ERR_CUDA;
+    }
 
-    long long cap = w.list_cap * num_kv_heads;
+    long long cap = direct ? (long long)num_seqs * num_kv_heads : w.list_cap * num_kv_heads;
     if (cap > INT_MAX) cap = INT_MAX;
     auto launch = [&](int kernel) -> pa_status_t {
         if (head_dim == 64) return launch_decode_d64(P, dtype, (int)cap, st, kernel);

@@ -14,13 +14,13 @@ namespace pa {
 
 constexpr int kMaxDevices = 64;
 
-template <int D, int GM, typename T>
-pa_status_t launch_one(const DecodeParams &P, int grid_cap, cudaStream_t stream) {
+template <int D, int GM, typename T, bool DIRECT>
+pa_status_t launch_one_form(const DecodeParams &P, int grid_cap, cudaStream_t stream) {
     using Tn = Tuning<D, GM>;
     constexpr int R = Tn::kStages;
     constexpr int MINB = Tn::kMinBlocks;
     using L = Layout<D, GM, R>;
-    auto kern = paged_decode_kernel<D, GM, T, R, MINB>;
+    auto kern = paged_decode_kernel<D, GM, T, R, MINB, DIRECT>;
     static std::atomic<int> occ_cache[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
@@ -44,16 +44,23 @@ pa_status_t launch_one(const DecodeParams &P, int grid_cap, cudaStream_t stream)
     return PA_OK;
 }
 
+// The kernel's planned or plan-free (DIRECT) form, as P.direct says.
+template <int D, int GM, typename T>
+pa_status_t launch_one(const DecodeParams &P, int grid_cap, cudaStream_t stream) {
+    return P.direct ? launch_one_form<D, GM, T, true>(P, grid_cap, stream)
+                    : launch_one_form<D, GM, T, false>(P, grid_cap, stream);
+}
+
 // Consumer warps per CTA of the tensor-core kernel.
 constexpr int kMmaWarps = 4;
 
-template <int D, typename T, int W = kMmaWarps>
-pa_status_t launch_one_mma(const DecodeParams &P, int grid_cap, cudaStream_t stream) {
+template <int D, typename T, bool DIRECT, int W = kMmaWarps>
+pa_status_t launch_one_mma_form(const DecodeParams &P, int grid_cap, cudaStream_t stream) {
     using Tn = TuningMma<D, W>;
     constexpr int R = Tn::kStages;
     constexpr int MINB = Tn::kMinBlocks;
     using L = LayoutMma<D, R, W>;
-    auto kern = paged_decode_mma_kernel<D, T, R, MINB, W>;
+    auto kern = paged_decode_mma_kernel<D, T, R, MINB, W, DIRECT>;
     static std::atomic<int> occ_cache[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
@@ -75,6 +82,12 @@ pa_status_t launch_one_mma(const DecodeParams &P, int grid_cap, cudaStream_t str
         cudaSuccess)
         return PA_ERR_CUDA;
     return PA_OK;
+}
+
+template <int D, typename T>
+pa_status_t launch_one_mma(const DecodeParams &P, int grid_cap, cudaStream_t stream) {
+    return P.direct ? launch_one_mma_form<D, T, true>(P, grid_cap, stream)
+                    : launch_one_mma_form<D, T, false>(P, grid_cap, stream);
 }
 
 template <int D, typename T>

@@ -157,7 +157,7 @@ __device__ __forceinline__ uint32_t swz(int chunk, int row, size_t box_bytes) {
 // producer warp: same item pipeline as the CUDA-core kernel, four blocks per
 // stage, tiled TMA
 // ---------------------------------------------------------------------------
-template <int D, typename T, int R, int W>
+template <int D, typename T, int R, int W, bool DIRECT>
 __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned char *sk,
                                                  unsigned char *sv, unsigned char *sq,
                                                  StageMeta *meta, uint64_t *full, uint64_t *empty,
@@ -176,12 +176,13 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
     // for the kernels in between, which wait for this one.)
     if (P.early_trigger) pdl_trigger();
     pdl_wait();  // the plan kernel's items and counter are ready
-    const unsigned n_items = P.hdr->n_items[P.list];
+    const unsigned n_items = DIRECT ? (unsigned)(P.num_seqs * P.num_kv_heads)
+                                    : P.hdr->n_items[P.list];
     const unsigned Hkv = (unsigned)P.num_kv_heads;
     const int G = P.G;
     const uint64_t policy = l2_evict_first_policy();
 
-    ItemPipe items;
+    ItemPipe<DIRECT> items;
     items.init(P, n_items, lane);
 
     uint32_t k = 0;
@@ -192,7 +193,7 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
         const int2 tA = items.tX;
 
         if constexpr (kDebugChecks) {
-            if (!item_ok(P, eA)) {
+            if (!item_ok<DIRECT>(P, eA)) {
                 if (lane == 0 && P.err) atomicOr(P.err, PA_ERRBIT_INTERNAL);
                 items.advance();
                 continue;
@@ -202,6 +203,13 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
         const int part = item_part(eA.w), count = item_count(eA.w);
         const bool group = item_is_group(eA.w);
         const int hk = (int)(cA % Hkv);
+        if constexpr (DIRECT) {
+            if (ntok == 0) {  // an empty or invalid unit
+                zero_unit_rows(P, s, hk, lane);
+                items.advance();
+                continue;
+            }
+        }
         const int nblk = (ntok + kBlock - 1) / kBlock;
         const int nst = (nblk + W - 1) / W;
         const bool split = !P.contig_rows && P.block_size < kBlock;  // 8-token blocks
@@ -577,7 +585,7 @@ __device__ __forceinline__ void run_epilogue_mma(const DecodeParams &P, uint64_t
     }
 }
 
-template <int D, typename T, int R, int MINB, int W>
+template <int D, typename T, int R, int MINB, int W, bool DIRECT>
 __global__ void __launch_bounds__(threads_mma<W>(), MINB)
     paged_decode_mma_kernel(const __grid_constant__ DecodeParams P) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -613,7 +621,7 @@ __global__ void __launch_bounds__(threads_mma<W>(), MINB)
     }
     __syncthreads();
     if (warp == 0)
-        run_producer_mma<D, T, R, W>(P, sk, sv, sq, meta, full, empty, abort_flag, lane);
+        run_producer_mma<D, T, R, W, DIRECT>(P, sk, sv, sq, meta, full, empty, abort_flag, lane);
     else if (warp <= W)
         run_consumer_mma<D, T, R, W>(P, sk, sv, sq, meta, full, empty, acc_full, acc_empty, s_acc,
                                   s_m, s_l, info, abort_flag, warp - 1, lane);

@@ -194,6 +194,55 @@ def test_empty_sequences_give_zero_rows():
 
 
 # ---------------------------------------------------------------------------
+# small batches without the plan: at most 256 (sequence, KV head) pairs, each
+# context within one partition, no shared-prefix items; each pair is one item
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("S,H,Hkv,D,dtype,B,max_len,direct", [
+    (128, 2, 2, 64, "f16", 16, 255, True),      # G = 1, CUDA cores, 256 pairs
+    (129, 2, 2, 64, "f16", 16, 255, False),     # two pairs more: the plan runs
+    (32, 64, 8, 128, "bf16", 16, 0, True),      # G = 8, a whole partition
+    (256, 4, 1, 128, "f16", 16, 200, True),     # G = 4, one KV head
+    (42, 6, 6, 256, "f16", 16, 0, True),        # D = 256, a whole partition
+    (60, 8, 4, 128, "f16", 8, 255, True),       # G = 2 on 8-token blocks
+])
+def test_small_batches_without_the_plan(S, H, Hkv, D, dtype, B, max_len, direct):
+    if max_len == 0:                            # the longest context one partition holds
+        max_len = pa.decode_partition_tokens(S, Hkv, 512)
+    rng = np.random.default_rng(S * 31 + H)
+    lens = rng.integers(1, max_len + 1, size=S)
+    lens[0], lens[1], lens[2], lens[-1] = max_len, 0, 1, 0
+    wl = custom_workload(lens, H, Hkv, D, dtype, seed=S + D, block_size=B)
+    assert wl.max_context_len == max_len
+    assert (pa.decode_kernel_launches(S, H, Hkv, D, max_len) == 1) == direct
+    got, want = _run_and_check(wl)
+    assert np.all(got[lens == 0] == 0)
+    assert max_abs(got, want) <= ATOL
+
+
+def test_small_batch_bad_length_on_tensor_cores_is_flagged():
+    wl = custom_workload([40, 90, 7, 200, 150], 12, 2, 128, "bf16", seed=4)
+    assert pa.decode_kernel_launches(5, 12, 2, 128, wl.max_context_len) == 1
+    vals = synthetic.make_values(wl, device=DEV)
+    h = host_inputs(wl, vals)
+    tables = torch.as_tensor(wl.block_tables, device=DEV)
+    lens = torch.as_tensor(wl.context_lens, device=DEV)
+    lens[1] = -3                                       # negative
+    lens[3] = 10_000                                   # above max_context_len
+    err = _err_word()
+    out = pa.decode_attention(vals["q"], vals["k_cache"], vals["v_cache"], tables, lens,
+                              wl.max_context_len, wl.scale, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == pa.ERRBIT_CONTEXT_LEN
+    assert torch.all(out[1] == 0) and torch.all(out[3] == 0)
+    import oracle
+    want = oracle.decode_attention(h["q"], h["k_cache"], h["v_cache"], h["tables"],
+                                   wl.context_lens, wl.scale, wl.dtype)
+    keep = [0, 2, 4]
+    assert max_abs(out.cpu().numpy()[keep], want[keep]) <= ATOL
+
+
+# ---------------------------------------------------------------------------
 # query groups on the tensor-core kernel: extreme batch shapes for the plan,
 # the item pipeline and the merge
 # ---------------------------------------------------------------------------
