@@ -133,7 +133,14 @@ struct DecodeParams {
     int part_tokens, max_parts;
     int list;          // the work list this launch takes (0 or 1)
     int grouping;      // 1: the plan may form shared-prefix items
-    int early_trigger; // 1: let the next kernel launch at once (it waits for this grid)
+    int early_trigger; // 1: let the next kernel launch once the plan has completed
+    // after_sibling = 1: the CUDA-core launch of a call that runs both
+    // attention kernels.  It launches only once every CTA of the tensor-core
+    // launch before it has seen the plan complete (early_trigger), so it
+    // reads the plan's lists at once instead of waiting for that launch, and
+    // waits for it only before it ends: whatever waits for this grid (the
+    // merge) then sees both.
+    int after_sibling;
     // direct = 1: no plan ran, and the host launches the kernels' DIRECT
     // form.  Item c is the whole context of (sequence c / Hkv, KV head
     // c % Hkv) and CTA b takes items b, b + grid, ... (for small batches whose
@@ -273,7 +280,7 @@ struct ItemPipe {
             const int Lv = (L < 0 || L > P->max_context_len) ? 0 : L;
             return make_int4(seq, 0, Lv, make_item_w(0, 1, false));
         }
-        return P->items[c / Hkv];
+        return __ldcg(&P->items[c / Hkv]);  // at L2: written by the plan in this call
     }
     // Lane j's chunk (tokens 16 j .. 16 j + 15 of the item): x = the block
     // holding its first token; y = the next block, read only for 8-token
@@ -336,9 +343,9 @@ template <int D, int GM, typename T, int R, bool DIRECT>
 __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv, T *sq,
                                              StageMeta *meta, uint64_t *full, uint64_t *empty,
                                              volatile int *abort_flag, int lane) {
-    pdl_wait();  // the plan kernel's items and counter are ready
+    if (!P.after_sibling) pdl_wait();  // the plan kernel's items and counter are ready
     const unsigned n_items = DIRECT ? (unsigned)(P.num_seqs * P.num_kv_heads)
-                                    : P.hdr->n_items[P.list];
+                                    : __ldcg(&P.hdr->n_items[P.list]);
     const unsigned Hkv = (unsigned)P.num_kv_heads;
     const int G = P.G;
     const uint64_t policy = l2_evict_first_policy();
@@ -476,6 +483,7 @@ __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv
     // has fired in every CTA, resets it.
     __threadfence();
     pdl_trigger();
+    if (P.after_sibling) pdl_wait();  // this grid ends after the tensor-core launch
 }
 
 // ---------------------------------------------------------------------------

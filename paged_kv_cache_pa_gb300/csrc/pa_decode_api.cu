@@ -808,14 +808,17 @@ pa_status_t decode_impl(void *out, pa_dtype_t out_dtype, const void *query, cons
     pa_status_t st_launch;
     if (split) {
         // list 0: the shared-prefix items on the tensor-core kernel, which
-        // lets the next kernel launch at once; then list 1: the plain items
-        // on the CUDA-core kernel, whose CTAs start as soon as they fit
+        // lets the next kernel launch once the plan has completed; then list
+        // 1: the plain items on the CUDA-core kernel, whose CTAs start work
+        // as soon as they fit and wait for the tensor-core grid only at the
+        // end
         P.list = 0;
         P.items = A.items0;
         P.early_trigger = 1;
         st_launch = launch(kKernelTensorCore);
         if (st_launch != PA_OK) return st_launch;
         P.early_trigger = 0;
+        P.after_sibling = 1;
         P.list = 1;
         P.items = A.items1;
         st_launch = launch(kKernelByGroup);

@@ -169,15 +169,16 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
         prefetch_tmap(&P.tmap_q);
         if (P.grouping) prefetch_tmap(&P.tmap_qs);
     }
-    // The shared-prefix launch of a G = 1 call lets the CUDA-core kernel
-    // after it launch at once: that kernel waits for this grid's completion
-    // before it reads anything, and its CTAs start as soon as they fit.
-    // (The next call's plan still runs after this grid completes: it waits
-    // for the kernels in between, which wait for this one.)
-    if (P.early_trigger) pdl_trigger();
     pdl_wait();  // the plan kernel's items and counter are ready
+    // The shared-prefix launch of a G = 1 call lets the CUDA-core kernel
+    // after it launch once every CTA here has seen the plan complete: that
+    // kernel reads the plan's lists at once, its CTAs start work as soon as
+    // they fit, and it waits for this grid only before it ends.  (The next
+    // call's plan still runs after this grid completes: it waits for the
+    // kernels in between, which wait for this one.)
+    if (P.early_trigger) pdl_trigger();
     const unsigned n_items = DIRECT ? (unsigned)(P.num_seqs * P.num_kv_heads)
-                                    : P.hdr->n_items[P.list];
+                                    : __ldcg(&P.hdr->n_items[P.list]);
     const unsigned Hkv = (unsigned)P.num_kv_heads;
     const int G = P.G;
     const uint64_t policy = l2_evict_first_policy();

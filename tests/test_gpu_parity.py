@@ -157,9 +157,10 @@ def test_poisoned_padding_is_never_read():
     assert max_abs(got, want) <= ATOL
 
 
+@pytest.mark.parametrize("lens", [[1, 5, 77, 300, 700], [1, 5, 77, 200, 255]])  # the second: no plan
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_half_output_is_rounded_fp32_output(dtype):
-    wl = custom_workload([1, 5, 77, 300, 700], 8, 2, 128, dtype, seed=11)
+def test_half_output_is_rounded_fp32_output(dtype, lens):
+    wl = custom_workload(lens, 8, 2, 128, dtype, seed=11)
     tdt = torch.float16 if dtype == "f16" else torch.bfloat16
     vals = synthetic.make_values(wl, device=DEV)
     h = host_inputs(wl, vals)
@@ -615,12 +616,21 @@ def test_swap_bad_pair_is_flagged_and_pageable_memory_refused():
 # contiguous (unpaged) cache: the layout the block table replaces
 # ---------------------------------------------------------------------------
 
+# "short": every context within one partition and few enough (sequence, KV
+# head) pairs that the call runs without the plan, an empty sequence among them
+CONTIG_LENS = {"mixed": [1, 15, 16, 17, 100, 513, 1000, 1025],
+               "short": [1, 15, 16, 0, 17, 100, 200, 255]}
+
+
+@pytest.mark.parametrize("lens_kind", sorted(CONTIG_LENS))
 @pytest.mark.parametrize("H,Hkv,D,dtype", [(8, 8, 128, "f16"), (12, 2, 128, "bf16"),
                                            (8, 2, 64, "f16"), (4, 4, 256, "bf16")])
-def test_contiguous_cache_matches_oracle(H, Hkv, D, dtype):
+def test_contiguous_cache_matches_oracle(H, Hkv, D, dtype, lens_kind):
     import oracle
-    lens = np.array([1, 15, 16, 17, 100, 513, 1000, 1025], np.int32)
+    lens = np.array(CONTIG_LENS[lens_kind], np.int32)
     S = len(lens)
+    direct = pa.decode_kernel_launches(S, H, Hkv, D, int(lens.max())) == 1
+    assert direct == (lens_kind == "short")
     rows = int(-(-lens.max() // 16) * 16) + 16
     tdt = torch.float16 if dtype == "f16" else torch.bfloat16
     g = torch.Generator(device=DEV).manual_seed(H * 31 + D)
@@ -648,6 +658,7 @@ def test_contiguous_cache_matches_oracle(H, Hkv, D, dtype):
                                    dtype)
     got = out.cpu().numpy()
     assert np.all(np.isfinite(got))
+    assert np.all(got[lens == 0] == 0)
     assert max_abs(got, want) <= ATOL
 
 
