@@ -343,7 +343,10 @@ template <int D, int GM, typename T, int R, bool DIRECT>
 __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv, T *sq,
                                              StageMeta *meta, uint64_t *full, uint64_t *empty,
                                              volatile int *abort_flag, int lane) {
-    if (!P.after_sibling) pdl_wait();  // the plan kernel's items and counter are ready
+    // The plan kernel's lists and counter are ready after this wait.  A
+    // launch after the tensor-core one (after_sibling) only starts once they
+    // are, and waits at its end instead.
+    if (!P.after_sibling) pdl_wait();
     const unsigned n_items = DIRECT ? (unsigned)(P.num_seqs * P.num_kv_heads)
                                     : __ldcg(&P.hdr->n_items[P.list]);
     const unsigned Hkv = (unsigned)P.num_kv_heads;

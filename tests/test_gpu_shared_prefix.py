@@ -117,3 +117,48 @@ def test_shared_prefix_step_with_copy_on_write():
     assert int(err.item()) == 0
     want = oracle_step(wl, h)
     assert max_abs(out.cpu().numpy(), want) <= ATOL
+
+
+@pytest.mark.parametrize("H, Hkv, D, dtype", [(8, 8, 128, "f16"), (4, 2, 64, "bf16")])
+def test_shared_and_unshared_calls_back_to_back_on_one_workspace(H, Hkv, D, dtype):
+    """Calls enqueued back to back on one stream and one workspace,
+    alternating a batch with shared prefixes and the same sequences cut
+    below the sharing threshold (no shared-prefix items: different work
+    lists in both of the plan's lists).  With one query head per KV head a
+    call runs the tensor-core and the CUDA-core kernel, and the CUDA-core
+    kernel reads its list as soon as it launches, without waiting for the
+    tensor-core grid, so a stale or early list read would show here.
+    Every output must equal the one the same batch gives alone, to the bit;
+    the shared batch is also checked against the oracle."""
+    import paged_kv_cache_pa_gb300 as pa
+    rng = np.random.default_rng(41)
+    S = 24
+    lens = rng.integers(300, 1400, S)
+    share = [0 if s % 6 == 0 else int(rng.integers(10, 18)) for s in range(S)]
+    wl = shared_workload(lens, share, H, Hkv, D, dtype, seed=41)
+    _check(wl, poison=False)                        # the shared batch against the oracle
+    vals = synthetic.make_values(wl, device=DEV)
+    tables = torch.as_tensor(wl.block_tables, device=DEV)
+    mx = int(wl.max_context_len)
+    la = torch.as_tensor(wl.context_lens, device=DEV)
+    lb = torch.clamp(la, max=40)                    # shares at most 40 tokens: no runs form
+    nbytes = pa.decode_workspace_size(S, H, Hkv, D, mx)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+
+    def call(lens_t, ws, out):
+        pa.decode_attention(vals["q"], vals["k_cache"], vals["v_cache"], tables, lens_t, mx,
+                            wl.scale, out=out, workspace=ws, error_word=err)
+
+    ref = {}
+    for name, lens_t in (("a", la), ("b", lb)):
+        ref[name] = torch.empty(S, H, D, dtype=torch.float32, device=DEV)
+        call(lens_t, torch.empty(nbytes, dtype=torch.uint8, device=DEV), ref[name])
+        torch.cuda.synchronize()
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    outs = [torch.empty(S, H, D, dtype=torch.float32, device=DEV) for _ in range(40)]
+    for i, out in enumerate(outs):
+        call(la if i % 2 == 0 else lb, ws, out)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for i, out in enumerate(outs):
+        assert torch.equal(out, ref["a" if i % 2 == 0 else "b"]), i
