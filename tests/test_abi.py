@@ -83,3 +83,21 @@ def test_error_bits_match_the_header():
         assert getattr(pa, "ERRBIT_" + name) == v, name
     assert len(set(bits.values())) == len(bits)
     assert all(v & (v - 1) == 0 for v in bits.values())   # one bit each
+
+
+@pytest.mark.parametrize("S,H,Hkv,D,max_len,launches", [
+    (4, 8, 8, 64, 116, 1),        # small batch: the attention kernel alone, no plan
+    (128, 2, 2, 64, 255, 1),      # 256 (sequence, KV head) pairs, one partition each
+    (129, 2, 2, 64, 255, 2),      # 258 pairs: plan + attention
+    (32, 64, 8, 128, 256, 1),     # query groups of 8 (no shared-prefix items), 256 tokens
+    (32, 64, 8, 128, 257, 3),     # two partitions: plan + attention + merge
+    (4, 8, 8, 64, 300, 4),        # shared prefixes may form (G = 1): plan + both kernels + merge
+    (256, 40, 40, 128, 1227, 4),  # the OPT-13B-shaped batch
+    (64, 12, 2, 128, 3991, 3),    # the grouped-query batch
+    (0, 8, 8, 64, 100, 0),        # invalid sizes
+    (4, 12, 5, 64, 100, 0),
+])
+def test_kernel_launch_counts_follow_the_host_rules(lib, S, H, Hkv, D, max_len, launches):
+    """pa_decode_kernel_launches (host only): which kernels a call enqueues."""
+    import paged_kv_cache_pa_gb300 as pa
+    assert pa.decode_kernel_launches(S, H, Hkv, D, max_len) == launches
