@@ -11,8 +11,9 @@ range.
 On correct plans nothing may fail.  Each case runs a whole decode step
 through that library: the copy-on-write copies, the cache write and
 attention.  The step must leave the error word 0 and match the oracle.  The
-cases cover the CUDA-core and tensor-core kernels, partitions, shared
-prefixes, 8-token blocks and every head size.
+cases cover the CUDA-core and tensor-core kernels, with the plan and
+without it (small batches), partitions, shared prefixes, 8-token blocks and
+every head size.
 
 The library runs in a child process of its own.  Each library links its own
 copy of the CUDA runtime, so a process loads only one of them.
@@ -34,7 +35,8 @@ for p in (ROOT, HERE):
 
 pytestmark = pytest.mark.gpu
 
-CASES = ["gqa_partitions", "g1_cuda_cores", "shared_prefix", "beams", "block8", "d64", "d256"]
+CASES = ["gqa_partitions", "g1_cuda_cores", "gqa_no_plan", "shared_prefix", "beams", "block8",
+         "d64", "d256"]
 
 
 def _workload(case):
@@ -42,8 +44,10 @@ def _workload(case):
     from paritylib import custom_workload, shared_workload
     if case == "gqa_partitions":   # G = 6, tensor cores, several partitions
         return custom_workload([700, 1500, 33, 4000, 900, 2], 12, 2, 128, "bf16")
-    if case == "g1_cuda_cores":    # G = 1, CUDA cores
+    if case == "g1_cuda_cores":    # G = 1, CUDA cores, no plan (a small batch)
         return synthetic.make("tiny", num_seqs=16)
+    if case == "gqa_no_plan":      # G = 6 on the tensor cores, no plan, an empty sequence
+        return custom_workload([40, 90, 7, 200, 0, 150], 12, 2, 128, "bf16")
     if case == "shared_prefix":    # G = 1 with shared prefixes: both kernels
         return shared_workload([900, 950, 990, 400, 1300], [0, 50, 50, 0, 20], 4, 4, 128, "f16")
     if case == "beams":            # copy-on-write copies and shared prompts

@@ -35,7 +35,7 @@ from paritylib import (ATOL, custom_workload, host_inputs, max_abs, prefill_orac
 
 pytestmark = pytest.mark.gpu
 
-DECODE_CASES = ["cuda_cores", "tensor_cores", "shared_prefix"]
+DECODE_CASES = ["cuda_cores", "tensor_cores", "tensor_cores_no_plan", "shared_prefix"]
 PREFILL_CASES = {"prefill_f16": (8, 8, 128, "f16"), "prefill_bf16": (12, 2, 128, "bf16")}
 PREFILL_CHUNKS = [(0, 200), (300, 130), (37, 64), (0, 1)]
 
@@ -46,6 +46,8 @@ def _decode_workload(case):
         return synthetic.make("tiny", num_seqs=16)
     if case == "tensor_cores":     # G = 6: the tensor-core kernel, several partitions
         return custom_workload([700, 1500, 33, 4000, 900, 2], 12, 2, 128, "bf16")
+    if case == "tensor_cores_no_plan":  # G = 6, a batch small enough to skip the plan
+        return custom_workload([40, 90, 7, 200, 0, 150], 12, 2, 128, "bf16")
     # G = 1 with shared prefixes: both attention kernels in one call
     return shared_workload([900, 950, 990, 400, 1300], [0, 50, 50, 0, 20], 4, 4, 128, "f16")
 
