@@ -1225,7 +1225,8 @@ def main():
                                   f"lower bound of the read peak)",
                      "unit": "GB/s", "frac": round(n["frac"], 4),
                      "frac_of_spec_8000": round(n["attn_gbs"] / 8000.0, 4),
-                     "traffic": recorded_traffic(args.config),
+                     # the recorded figure is for the full-size batch
+                     "traffic": None if args.seqs else recorded_traffic(args.config),
                      "kernel": "pa_decode_attention (plan, attention and merge kernels)",
                      "duration": "timed-region step time (cache write + attention call"
                                  + (" + copy-on-write copies" if b_copy else "") + ")",

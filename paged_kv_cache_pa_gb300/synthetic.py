@@ -182,8 +182,11 @@ def make_long(seed: Optional[int] = None, num_seqs: int = 8,
 
 def make_beams(seed: Optional[int] = None, groups: int = 32, beams: int = 6,
                prompt: int = 512, max_suffix: int = 256, num_heads: int = 40,
-               head_dim: int = 128) -> Workload:
+               head_dim: int = 128, num_seqs: Optional[int] = None) -> Workload:
     """Beam groups sharing a prompt, grown by a seeded beam search.
+
+    ``num_seqs`` (a smaller case for profiling) sets ``groups`` to
+    num_seqs // beams, at least one.
 
     Every group prefills its prompt once and forks it ``beams - 1`` times.
     Its suffix length s_g ~ U{1..max_suffix}; for the s_g - 1 steps before the
@@ -194,6 +197,8 @@ def make_beams(seed: Optional[int] = None, groups: int = 32, beams: int = 6,
     pairs it needs become ``copy_pairs`` and its slots ``slot_mapping``.
     Blocks are handed out in a seeded random order over the pool.
     """
+    if num_seqs:
+        groups = max(1, num_seqs // beams)
     seed = SEEDS["beams"] if seed is None else seed
     rng = np.random.default_rng(seed)
     suffix = rng.integers(1, max_suffix + 1, groups)
