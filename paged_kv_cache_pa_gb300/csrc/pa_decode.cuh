@@ -17,6 +17,10 @@
 //     items in a fixed order and claim the rest with one atomic each, so the
 //     tail is short.  Each item names its sequence, its first token, its
 //     token count and the partial-result slot (partition) it fills.
+//   * A small batch (at most 256 (sequence, KV head) pairs, each context
+//     within one partition, no shared prefixes) runs without the plan: the
+//     kernels' DIRECT form takes each pair as one item, CTA b the pairs b,
+//     b + grid, ...
 //   * Runs of consecutive sequences whose block tables start with the same
 //     full blocks share that prefix: the plan makes the shared prefix one
 //     item whose query rows are all the run's queries (the tensor-core
@@ -343,9 +347,10 @@ template <int D, int GM, typename T, int R, bool DIRECT>
 __device__ __forceinline__ void run_producer(const DecodeParams &P, T *sk, T *sv, T *sq,
                                              StageMeta *meta, uint64_t *full, uint64_t *empty,
                                              volatile int *abort_flag, int lane) {
-    // The plan kernel's lists and counter are ready after this wait.  A
-    // launch after the tensor-core one (after_sibling) only starts once they
-    // are, and waits at its end instead.
+    // The plan kernel's lists and counter (without a plan: whatever the
+    // kernels before wrote, such as the cache write) are ready after this
+    // wait.  A launch after the tensor-core one (after_sibling) only starts
+    // once they are, and waits at its end instead.
     if (!P.after_sibling) pdl_wait();
     const unsigned n_items = DIRECT ? (unsigned)(P.num_seqs * P.num_kv_heads)
                                     : __ldcg(&P.hdr->n_items[P.list]);

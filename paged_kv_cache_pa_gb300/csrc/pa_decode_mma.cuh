@@ -169,7 +169,7 @@ __device__ __forceinline__ void run_producer_mma(const DecodeParams &P, unsigned
         prefetch_tmap(&P.tmap_q);
         if (P.grouping) prefetch_tmap(&P.tmap_qs);
     }
-    pdl_wait();  // the plan kernel's items and counter are ready
+    pdl_wait();  // the plan's lists and counter (without a plan: the kernels before) are ready
     // The shared-prefix launch of a G = 1 call lets the CUDA-core kernel
     // after it launch once every CTA here has seen the plan complete: that
     // kernel reads the plan's lists at once, its CTAs start work as soon as
