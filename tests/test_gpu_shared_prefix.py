@@ -162,3 +162,18 @@ def test_shared_and_unshared_calls_back_to_back_on_one_workspace(H, Hkv, D, dtyp
     assert int(err.item()) == 0
     for i, out in enumerate(outs):
         assert torch.equal(out, ref["a" if i % 2 == 0 else "b"]), i
+
+
+@pytest.mark.parametrize("S,launches", [(4096, 4), (4097, 2)])
+def test_shared_prefixes_at_the_batch_limit(S, launches):
+    """4096 sequences, the most the plan looks for shared prefixes in (its
+    1024 threads keep four sequences each), in runs of four that share 10 to
+    15 leading blocks; and one sequence more, where detection is off and
+    every sequence is read through its own table."""
+    import paged_kv_cache_pa_gb300 as pa
+    rng = np.random.default_rng(S)
+    lens = rng.integers(256, 400, S)
+    share = [0 if s % 4 == 0 else int(rng.integers(10, 16)) for s in range(S)]
+    wl = shared_workload(lens, share, 2, 2, 64, "f16", seed=S)
+    assert pa.decode_kernel_launches(S, 2, 2, 64, wl.max_context_len) == launches
+    _check(wl, poison=False)
