@@ -104,6 +104,7 @@ EDGE_LENS = [1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 
     (8, 8, 64, "f16"), (4, 4, 128, "f16"), (4, 4, 128, "bf16"), (4, 4, 256, "bf16"),
     (8, 4, 128, "f16"), (12, 2, 128, "bf16"), (6, 2, 64, "f16"), (16, 2, 128, "f16"),
     (10, 2, 256, "f16"), (5, 1, 128, "bf16"), (7, 1, 64, "bf16"),
+    (6, 2, 256, "bf16"), (14, 2, 256, "f16"), (16, 2, 256, "bf16"),  # D = 256, G = 3, 7, 8
 ])
 def test_shapes_and_block_edges(H, Hkv, D, dtype):
     wl = custom_workload(EDGE_LENS, H, Hkv, D, dtype, seed=H * 1000 + D)
